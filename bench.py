@@ -1,0 +1,532 @@
+#!/usr/bin/env python
+"""Benchmark of the ReplaySSM SSM-layer decode step on B300.
+
+Default workload: a Mamba-2 layer of hybrid-LLM shape, batch 256, H = 128
+heads, P = 64, N = 128 (4 MiB FP32 state per sequence), W = 16, BF16 vector
+inputs, FP32 checkpoint plus BF16 read copy. One step = consolidate(k_next = 1)
++ replay decode of one token for every sequence, i.e. the whole hot path for
+plain decoding. Prints one JSON line.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload mamba2|gdn|kda] [--read bf16|f32]
+
+Timing: device time with CUDA events on the launching stream, W untimed
+warm-up steps first, a barrier and a synchronize on both sides of the K timed
+steps, max over ranks. The state (1.5 GiB) is larger than L2, so no flush is
+needed between steps. Under torchrun every rank decodes its own batch of 256
+sequences (independent shards, no collective on the data path).
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "SSM-layer decode tokens/s at batch 256 on 1 B300; achieved HBM GB/s vs ~8 TB/s"
+UNIT = "tokens/s"
+
+WORKLOADS = {
+    "mamba2": dict(kind="mamba2", batch=256, heads=128, dk=128, dv=64, window=16, groups=1),
+    "gdn": dict(kind="gdn", batch=256, heads=32, dk=128, dv=128, window=16, groups=1),
+    "kda": dict(kind="kda", batch=256, heads=32, dk=128, dv=128, window=16, groups=1),
+}
+POOL = 16  # distinct synthetic tokens, cycled through the timed steps
+
+
+def parse(argv=None):
+    p = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=4096)
+    p.add_argument("--warmup", type=int, default=64)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--workload", choices=sorted(WORKLOADS), default="mamba2")
+    p.add_argument("--read", choices=["bf16", "f32"], default="bf16")
+    p.add_argument("--batch", type=int, default=None, help="override the batch size")
+    p.add_argument("--no-extras", action="store_true",
+                   help="time the main loop only (no A/B, e2e, CPU baseline, clocks)")
+    p.add_argument("--cpu-seconds", type=float, default=12.0,
+                   help="budget of the CPU-oracle baseline sample")
+    return p.parse_args(argv)
+
+
+# ------------------------------------------------------------- distributed
+def dist_env():
+    return (int(os.environ.get("RANK", 0)), int(os.environ.get("LOCAL_RANK", 0)),
+            int(os.environ.get("WORLD_SIZE", 1)))
+
+
+def max_over_ranks(value: float, world: int) -> float:
+    """Largest value over all ranks (the job ends when its slowest rank does)."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int) -> None:
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+# ------------------------------------------------------------------ peaks
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6400.0, "fallback"
+
+
+# ----------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during a region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.file = None
+
+    def __enter__(self):
+        try:
+            self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.file, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.2)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.file.seek(0)
+        rows = [r.split(",") for r in self.file.read().strip().splitlines() if r.strip()]
+        os.unlink(self.file.name)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            r = [c.strip() for c in r]
+            try:
+                sm.append(float(r[1]))
+                smax.append(float(r[2]))
+            except (ValueError, IndexError):
+                continue
+            for n, v in zip(names, r[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------ our arm
+class Layer:
+    """One SSM layer's state, token pool and step functions on one GPU."""
+
+    def __init__(self, wl: dict, read: str, device, seed: int = 2):
+        import numpy as np
+        import torch
+
+        import synth
+        from recurrent_state_fp32_b300 import api
+
+        self.api, self.torch, self.np = api, torch, np
+        self.wl = wl
+        k = wl["kind"]
+        b, H, dk, dv, W, G = (wl[x] for x in ("batch", "heads", "dk", "dv", "window", "groups"))
+        self.dims = api.LayerDims(k, b, H, dk=dk, dv=dv, window=W, groups=G, in_dtype="bf16")
+        self.state = api.LayerState(self.dims, device=device, read_copy=(read == "bf16"))
+        gen = torch.Generator(device=device)
+        gen.manual_seed(seed)
+        self.state.S_ckpt.normal_(0.0, 0.1, generator=gen)
+        if self.state.S_read is not None:
+            api.refresh_read_copy(self.dims, self.state)
+        self.device = device
+        dt = lambda a, ty: torch.from_numpy(np.ascontiguousarray(a)).to(device, ty)  # noqa: E731
+        self.host_pool, self.pool = [], []
+        if k == "mamba2":
+            A, D, bias = synth.mamba2_params(seed, H)
+            self.A, self.D = dt(A, torch.float32), dt(D, torch.float32)
+            for t in range(POOL):
+                tok = synth.mamba2_step_inputs(seed, t, b, H, G, dv, dk, bias, "bf16")
+                self.host_pool.append(tok)
+            names = ("x", "B", "C", "dt")
+        else:
+            self.A = None
+            for t in range(POOL):
+                self.host_pool.append(synth.delta_step_inputs(seed, t, b, H, dk, dv, k, "bf16"))
+            names = ("q", "k", "v", "alpha", "beta")
+        vec = {"x", "B", "C", "q", "k", "v"}
+        for tok in self.host_pool:
+            self.pool.append({n: dt(tok[n], torch.bfloat16 if n in vec else torch.float32)
+                              for n in names})
+        self.out = torch.empty((b, H, dv), device=device)
+        self.names = names
+        self.vec = vec
+
+    # one decode step on device-resident inputs
+    def consolidate(self, stream=None):
+        self.api.consolidate(self.dims, self.state, self.A, 1, False, stream)
+
+    def decode(self, tok, stream=None):
+        a = self.api
+        if self.wl["kind"] == "mamba2":
+            a.mamba2_decode(self.dims, self.state, self.A, self.D, tok["x"], tok["B"], tok["C"],
+                            tok["dt"], self.out, stream)
+        else:
+            a.gdn_decode(self.dims, self.state, tok["q"], tok["k"], tok["v"], tok["alpha"],
+                         tok["beta"], 1.0, self.out, stream)
+
+    def conventional(self, S, tok, stream=None):
+        a = self.api
+        if self.wl["kind"] == "mamba2":
+            a.conventional_mamba2_step(self.dims, S, self.A, self.D, tok["x"], tok["B"], tok["C"],
+                                       tok["dt"], self.out, stream)
+        else:
+            a.conventional_gdn_step(self.dims, S, tok["q"], tok["k"], tok["v"], tok["alpha"],
+                                    tok["beta"], 1.0, self.out, stream)
+
+    # ------------------------------------------------ algorithmic bytes
+    def token_bytes(self):
+        """Bytes of one token's inputs for the whole batch (as read, and as ring-written)."""
+        return sum(t.numel() * t.element_size() for t in self.pool[0].values())
+
+    def ring_entry_bytes(self):
+        """Bytes of one ring entry for the whole batch that the replay reads back."""
+        wl, b = self.wl, self.wl["batch"]
+        H, dk, dv, G = wl["heads"], wl["dk"], wl["dv"], wl["groups"]
+        if wl["kind"] == "mamba2":
+            return b * (H * dv * 2 + G * dk * 2 + H * 4)          # x, B, dt
+        gate = H * 4 if wl["kind"] == "gdn" else H * dk * 4
+        return b * (H * dk * 2 + H * dv * 2 + gate + H * 4)       # k, v, alpha, beta
+
+    def state_elems(self):
+        wl = self.wl
+        return wl["batch"] * wl["heads"] * wl["dv"] * wl["dk"]
+
+    def decode_bytes(self, n_prior):
+        """Algorithmic bytes of one decode launch with n_prior committed entries.
+
+        Read copy (or FP32 checkpoint) once + token inputs read + the token
+        written to the ring + the n_prior buffered entries read + the output.
+        """
+        ts = 2 if self.state.S_read is not None else 4
+        out = self.out.numel() * 4
+        return self.state_elems() * ts + 2 * self.token_bytes() + n_prior * self.ring_entry_bytes() + out
+
+    def fold_bytes(self, n):
+        """Algorithmic bytes of one consolidate that folds n entries for every sequence."""
+        rd = 2 if self.state.S_read is not None else 0
+        return self.state_elems() * (4 + 4 + rd) + n * self.ring_entry_bytes()
+
+    def conventional_bytes(self):
+        return self.state_elems() * 8 + self.token_bytes() + self.out.numel() * 4
+
+
+def run_ours(args, rank, local_rank, world):
+    import torch
+
+    device = torch.device("cuda", local_rank)
+    torch.cuda.set_device(device)
+    wl = dict(WORKLOADS[args.workload])
+    if args.batch:
+        wl["batch"] = args.batch
+    W = wl["window"]
+    layer = Layer(wl, args.read, device)
+    stream = torch.cuda.current_stream(device)
+    K, Wm = args.steps, args.warmup
+
+    # warm-up
+    for i in range(Wm):
+        layer.consolidate()
+        layer.decode(layer.pool[i % POOL])
+    torch.cuda.synchronize()
+    # ring length before timed step i (all sequences move in lockstep)
+    len0 = int(layer.state.ring_len[0].item())
+
+    ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+    start, end = ev(), ev()
+    d0 = [ev() for _ in range(K)]
+    d1 = [ev() for _ in range(K)]
+    clocks = ClockSampler(local_rank) if not args.no_extras else None
+    if clocks:
+        clocks.__enter__()
+    barrier(world)
+    torch.cuda.synchronize()
+    start.record(stream)
+    for i in range(K):
+        layer.consolidate()
+        d0[i].record(stream)
+        layer.decode(layer.pool[i % POOL])
+        d1[i].record(stream)
+    end.record(stream)
+    end.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    if clocks:
+        clocks.__exit__(None, None, None)
+    ms = max_over_ranks(start.elapsed_time(end), world)
+    dec_ms = [d0[i].elapsed_time(d1[i]) for i in range(K)]
+
+    # algorithmic bytes of the timed region
+    dec_bytes, fold_bytes, ln = 0, 0, len0
+    for i in range(K):
+        if ln + 1 > W:
+            fold_bytes += layer.fold_bytes(ln)
+            ln = 0
+        dec_bytes += layer.decode_bytes(ln)
+        ln += 1
+    peak, peak_kind = measured_peaks()
+    dec_s = sum(dec_ms) / 1e3
+    achieved = dec_bytes / dec_s / 1e9
+    tokens = wl["batch"] * K * world
+    value = tokens / (ms / 1e3)
+    step_gbs = (dec_bytes + fold_bytes) / (ms / 1e3) / 1e9
+
+    res = {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
+        "steps": K, "warmup": Wm, "ms_per_step": round(ms / K, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32", "data": "synthetic (seeded; no weights or datasets)",
+        "config": {
+            "workload": f"{wl['kind']}_decode_b{wl['batch']}_h{wl['heads']}_"
+                        f"{'p' if wl['kind'] == 'mamba2' else 'dv'}{wl['dv']}_"
+                        f"{'n' if wl['kind'] == 'mamba2' else 'dk'}{wl['dk']}_w{W}",
+            "batch_per_gpu": wl["batch"], "heads": wl["heads"], "dk_or_N": wl["dk"],
+            "dv_or_P": wl["dv"], "window": W, "read_copy": args.read, "inputs": "bf16",
+            "checkpoint": "f32", "step": "consolidate(k_next=1) + replay decode",
+            "l2": "state larger than L2 (no flush)", "parallelism": f"replicas x{world}",
+        },
+        "step_hbm_gbs": round(step_gbs, 1),
+        "roofline": {
+            "kernel": f"{wl['kind']}_replay_decode", "bound": "hbm", "achieved": round(achieved, 1),
+            "peak": peak, "peak_source": peak_kind, "unit": "GB/s",
+            "frac": round(achieved / peak, 4), "traffic": None,
+            "bytes_per_launch": int(dec_bytes / K),
+            "avg_launch_us": round(1e3 * sum(dec_ms) / K, 3),
+        },
+        "gpu_launches": 2 * K,
+    }
+    if clocks:
+        res["clocks"] = clocks.summary()
+    if not args.no_extras:
+        res["ab"] = run_ab(layer, K, Wm, stream, world)
+        res["e2e"] = run_e2e(layer, args, stream, world)
+        if rank == 0:
+            res["cpu_baseline"] = cpu_baseline(wl, args.cpu_seconds)
+    return res
+
+
+def run_ab(layer, K, Wm, stream, world):
+    """In-library conventional read-modify-write step on the same workload."""
+    import torch
+
+    S = layer.state.S_ckpt.clone()
+    for i in range(Wm):
+        layer.conventional(S, layer.pool[i % POOL])
+    Kc = max(16, K // 4)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    a.record(stream)
+    for i in range(Kc):
+        layer.conventional(S, layer.pool[i % POOL])
+    b.record(stream)
+    b.synchronize()
+    ms = max_over_ranks(a.elapsed_time(b), world)
+    del S
+    torch.cuda.empty_cache()
+    tok_s = layer.wl["batch"] * Kc * world / (ms / 1e3)
+    return {"conventional_tokens_per_s": round(tok_s, 1),
+            "conventional_ms_per_step": round(ms / Kc, 5),
+            "conventional_hbm_gbs": round(layer.conventional_bytes() / (ms / Kc / 1e3) / 1e9, 1),
+            "conventional_bytes_per_step": layer.conventional_bytes(), "steps": Kc}
+
+
+def run_e2e(layer, args, stream, world):
+    """The same step through the public API with host buffers: every step copies
+    its inputs from pinned host memory and reads the output back."""
+    import torch
+
+    host = [{n: t.cpu().pin_memory() for n, t in tok.items()} for tok in layer.pool]
+    stage = {n: torch.empty_like(t) for n, t in layer.pool[0].items()}
+    y_host = torch.empty(layer.out.shape, dtype=torch.float32).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host[0].values())
+    d2h = y_host.numel() * 4
+    K = max(16, args.steps // 4)
+
+    def step(i):
+        for n, t in host[i % POOL].items():
+            stage[n].copy_(t, non_blocking=True)
+        layer.consolidate()
+        layer.decode(stage)
+        y_host.copy_(layer.out, non_blocking=True)
+
+    for i in range(8):
+        step(i)
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for i in range(K):
+        step(i)
+    b.record(stream)
+    b.synchronize()
+    ms = max_over_ranks(a.elapsed_time(b), world)
+    return {"value": round(layer.wl["batch"] * K * world / (ms / 1e3), 1), "unit": UNIT,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": K}
+
+
+# --------------------------------------------------------- oracle timing
+def oracle_sample(wl: dict, heads: int, seed: int = 2):
+    """A one-sequence, `heads`-head slice of the workload for the CPU oracle."""
+    import numpy as np
+
+    import synth
+    from oracle.method import ReplayOracle
+
+    k, W, dk, dv = wl["kind"], wl["window"], wl["dk"], wl["dv"]
+    H = wl["heads"]
+    if k == "mamba2":
+        A, D, bias = synth.mamba2_params(seed, H)
+        S0 = synth.mamba2_initial_state(seed, 1, heads, dv, dk)
+        orc = ReplayOracle(k, S0, W, A=A[:heads], D=D[:heads])
+        toks = []
+        for t in range(POOL):
+            tok = synth.mamba2_step_inputs(seed, t, 1, H, 1, dv, dk, bias, "bf16")
+            toks.append({"x": tok["x"][:, :heads], "B": tok["B"], "C": tok["C"],
+                         "dt": tok["dt"][:, :heads]})
+    else:
+        S0 = synth.delta_initial_state(seed, 1, heads, dv, dk)
+        orc = ReplayOracle(k, S0, W)
+        toks = []
+        for t in range(POOL):
+            tok = synth.delta_step_inputs(seed, t, 1, H, dk, dv, k, "bf16")
+            toks.append({n: v[:, :heads] for n, v in tok.items()})
+    return orc, toks, np
+
+
+def _single_thread():
+    try:
+        from threadpoolctl import threadpool_limits
+
+        return threadpool_limits(limits=1)
+    except ImportError:  # pragma: no cover
+        import contextlib
+
+        return contextlib.nullcontext()
+
+
+def cpu_baseline(wl: dict, seconds: float):
+    """The oracle as it stands, single-threaded on the host, on a bounded sample
+    (one sequence, all heads) of the same workload; scaled to tokens/s."""
+    heads = wl["heads"]
+    orc, toks, _ = oracle_sample(wl, heads)
+    with _single_thread():
+        t0 = time.perf_counter()
+        n = 0
+        while True:
+            orc.consolidate(1)
+            orc.decode(toks[n % POOL])
+            n += 1
+            if time.perf_counter() - t0 > seconds and n % wl["window"] == 0:
+                break
+        dt = time.perf_counter() - t0
+    return {"value": round(n / dt, 3), "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"1 sequence x {heads} heads, {n} consecutive decode steps "
+                      f"(consolidate + decode), float64 numpy, {dt:.1f} s"}
+
+
+def run_reference(args, rank, world):
+    """The CPU oracle as the reference arm: K timed steps (after W warm-up), each
+    a bounded sample of the workload (one sequence, a slice of its heads)."""
+    if rank != 0:
+        return None
+    wl = dict(WORKLOADS[args.workload])
+    heads = max(1, wl["heads"] // 16)
+    orc, toks, _ = oracle_sample(wl, heads)
+    with _single_thread():
+        for i in range(args.warmup):
+            orc.consolidate(1)
+            orc.decode(toks[i % POOL])
+        t0 = time.perf_counter()
+        for i in range(args.steps):
+            orc.consolidate(1)
+            orc.decode(toks[i % POOL])
+        dt = time.perf_counter() - t0
+    frac = heads / wl["heads"]
+    value = args.steps * frac / dt
+    sample = (f"1 sequence x {heads} of {wl['heads']} heads per step ({frac:.4f} of a "
+              f"layer token), float64 numpy oracle, single thread")
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(1e3 * dt / args.steps, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded; no weights or datasets)",
+        "config": {"workload": f"{wl['kind']}_decode_b{wl['batch']}_h{wl['heads']}_w{wl['window']}",
+                   "sample": sample},
+        "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main(argv=None):
+    args = parse(argv)
+    rank, local_rank, world = dist_env()
+    if args.impl == "reference":
+        res = run_reference(args, rank, world)
+        if res is not None:
+            print(json.dumps(res), flush=True)
+        return 0
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    res = run_ours(args, rank, local_rank, world)
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

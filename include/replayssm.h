@@ -1,0 +1,232 @@
+/*
+ * replayssm.h -- C ABI of the ReplaySSM batched decode library (sm_103a).
+ *
+ * The method (described on "ReplaySSM: o ganho aparece na carga concorrente,
+ * não no nome da otimização", introduction, and "NVIDIA y Princeton aceleran
+ * modelos híbridos al guardar entradas recientes en lugar del estado
+ * completo", paragraphs 2-4): each sequence's SSM-layer state is kept as an
+ * FP32 checkpoint S_c, an optional BF16 read copy of it, and a ring of the
+ * last W token inputs. A decode step appends the token to the ring and
+ * computes the output from the checkpoint plus the buffered inputs, writing
+ * no state; the checkpoint is only rewritten when the ring fills
+ * (consolidate). Speculative drafts are verified from one read of S_c and
+ * accepted by moving a per-sequence pointer. The layer types are those named
+ * on "NVIDIA présente ReplaySSM : accélérer le décodage des modèles hybrides
+ * Mamba et GDN", section "Pourquoi les hybrides sont devenus la norme":
+ * Mamba-2, Gated DeltaNet (GDN) and a Kimi-Delta-Attention-style
+ * per-channel gate (KDA).
+ *
+ * Conventions for every entry point:
+ *  - All tensor pointers are DEVICE pointers owned by the caller, dense
+ *    (row-major, no padding) in the layouts stated below, and 16-byte
+ *    aligned. The library never allocates, frees or synchronises.
+ *  - Every call is asynchronous on `stream` (a cudaStream_t passed as void*;
+ *    NULL means the legacy default stream) and returns a replayssm_status.
+ *    Argument errors are detected on the host before any CUDA call and
+ *    nothing is launched; REPLAYSSM_ERR_CUDA reports a launch error.
+ *  - Data-dependent precondition failures (for example a full ring) are
+ *    reported per sequence on the device by OR-ing bits into state->status;
+ *    the affected sequence is left untouched and the others proceed. Kernels
+ *    never trap and every wait they make is bounded (about one second), after
+ *    which they set REPLAYSSM_SEQ_TIMEOUT and skip the remaining work.
+ *  - Calls on one layer state must be ordered (one stream, or events);
+ *    calls that overlap on the GPU race.
+ *
+ * Layouts (b = batch, H = heads, G = Mamba-2 B/C groups, W = window):
+ *  Mamba-2 state    S_ckpt f32 [b, H, P, N] (N contiguous); S_read bf16 same
+ *  delta state      S_ckpt f32 [b, H, d_v, d_k] (d_k contiguous); S_read same
+ *  Mamba-2 token    x [b, H, P], B [b, G, N], C [b, G, N] (in_dtype);
+ *                   dt [b, H] f32 (already activated, > 0)
+ *  delta token      q, k [b, H, d_k], v [b, H, d_v] (in_dtype);
+ *                   alpha f32 [b, H] (GDN) or [b, H, d_k] (KDA); beta f32 [b, H]
+ *  ring fields      the token layout with a W axis after b: [b, W, ...]
+ *  pointers         ring_head, ring_len, status, sync: int32 [b]
+ *  outputs          f32: y [b, H, P]; o [b, H, d_v]; verify o [b, K, H, d_v]
+ *
+ * Supported sizes (else REPLAYSSM_ERR_UNSUPPORTED): N or d_k in {64, 128};
+ * P or d_v a multiple of 32 in [32, 256]; 1 <= W <= 64; heads >= 1;
+ * groups divides heads; 1 <= K <= 8 and K <= W. batch == 0 is a no-op.
+ */
+#ifndef REPLAYSSM_H
+#define REPLAYSSM_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define REPLAYSSM_API __attribute__((visibility("default")))
+
+typedef int32_t replayssm_status;
+
+/* Host-side return codes. */
+#define REPLAYSSM_OK 0
+#define REPLAYSSM_ERR_INVALID_ARG 1 /* null pointer, non-positive size, bad flag */
+#define REPLAYSSM_ERR_UNSUPPORTED 2 /* sizes outside the compiled tile shapes */
+#define REPLAYSSM_ERR_MISALIGNED 3  /* a tensor pointer not 16-byte aligned */
+#define REPLAYSSM_ERR_CUDA 4        /* the kernel launch reported an error */
+
+/* Per-sequence device status bits, OR-ed into state->status[seq]. */
+#define REPLAYSSM_SEQ_RING_FULL 1  /* decode/verify would overflow the ring */
+#define REPLAYSSM_SEQ_BAD_ACCEPT 2 /* accept count m < 0, m > K or len + m > W */
+#define REPLAYSSM_SEQ_TIMEOUT 4    /* a bounded wait expired; work skipped */
+#define REPLAYSSM_SEQ_BAD_POINTER 8 /* head outside [0, W) or len outside [0, W]; untouched */
+
+/* Layer kinds and element types. */
+#define REPLAYSSM_MAMBA2 0
+#define REPLAYSSM_GDN 1
+#define REPLAYSSM_KDA 2
+#define REPLAYSSM_F32 0
+#define REPLAYSSM_BF16 1
+
+/* Sizes of one SSM layer for a batch of sequences. */
+typedef struct replayssm_dims {
+  int32_t kind;     /* REPLAYSSM_MAMBA2, _GDN or _KDA */
+  int32_t batch;    /* sequences */
+  int32_t heads;    /* H */
+  int32_t groups;   /* Mamba-2 B/C groups G (G divides H); 1 for delta kinds */
+  int32_t dk;       /* columns of a state row: Mamba-2 N, delta d_k */
+  int32_t dv;       /* rows of a head's state: Mamba-2 P, delta d_v */
+  int32_t window;   /* W, ring entries per sequence */
+  int32_t in_dtype; /* element type of the vector inputs and their ring copies */
+} replayssm_dims;
+
+/*
+ * Device pointers of one layer's decode state (all caller-owned).
+ * A Mamba-2 state uses ring_x, ring_B, ring_C, ring_dt; a delta state uses
+ * ring_q, ring_k, ring_v, ring_alpha, ring_beta; the other ring pointers are
+ * ignored. ring_C and ring_q are optional (NULL: not stored; the decode
+ * arithmetic never reads them back). S_read NULL selects the FP32 read path.
+ * At initialisation the caller zeroes ring_head, ring_len, status and sync
+ * and fills S_ckpt (then calls replayssm_refresh_read_copy if S_read is set).
+ * `sync` is scratch used by the kernels to order the per-sequence pointer
+ * update after every block of that sequence has read it; each call leaves it
+ * at zero.
+ */
+typedef struct replayssm_state {
+  float* S_ckpt;      /* f32 checkpoint, never rounded */
+  void* S_read;       /* bf16 read copy or NULL */
+  void* ring_x;       /* Mamba-2 [b, W, H, P]    in_dtype */
+  void* ring_B;       /* Mamba-2 [b, W, G, N]    in_dtype */
+  void* ring_C;       /* Mamba-2 [b, W, G, N]    in_dtype, optional */
+  float* ring_dt;     /* Mamba-2 [b, W, H]       f32 */
+  void* ring_q;       /* delta   [b, W, H, d_k]  in_dtype, optional */
+  void* ring_k;       /* delta   [b, W, H, d_k]  in_dtype */
+  void* ring_v;       /* delta   [b, W, H, d_v]  in_dtype */
+  float* ring_alpha;  /* GDN [b, W, H]; KDA [b, W, H, d_k] f32 */
+  float* ring_beta;   /* delta   [b, W, H]       f32 */
+  int32_t* ring_head; /* slot of the oldest entry after the checkpoint */
+  int32_t* ring_len;  /* committed entries after the checkpoint, 0..W */
+  int32_t* status;    /* REPLAYSSM_SEQ_* bits; the library only sets bits */
+  int32_t* sync;      /* scratch arrival counters, zero between calls */
+} replayssm_state;
+
+/*
+ * Mamba-2 replay decode of one token per sequence ("NVIDIA y Princeton
+ * aceleran modelos híbridos…", paragraph 2: append, then output from the
+ * checkpoint). Precondition per sequence: ring_len + 1 <= W (call
+ * replayssm_consolidate(k_next = 1) first), else RING_FULL and the sequence
+ * (ring, pointers, y) is untouched. Effects: writes the token into slot
+ * (head + len) mod W, sets len += 1 and writes
+ *   y = (prod_i dA_i) (h_c C) + sum_j w_j (C . B_j) x_j + D x,
+ *   dA_i = exp(dt_i A), w_j = dt_j prod_{i > j} dA_i,
+ * over the n = len + 1 buffered tokens, reading h_c from S_read (bf16) when
+ * set, else S_ckpt. A, D: f32 [H]. No state is written.
+ */
+REPLAYSSM_API replayssm_status replayssm_mamba2_decode(
+    const replayssm_dims* dims, const replayssm_state* state, const float* A, const float* D,
+    const void* x, const void* B, const void* C, const float* dt, float* y, void* stream);
+
+/*
+ * Gated DeltaNet / KDA replay decode of one token per sequence (same page
+ * and paragraph; layer kinds from "NVIDIA présente ReplaySSM…", section
+ * "Pourquoi les hybrides sont devenus la norme"). dims->kind selects the
+ * gate shape. Precondition and ring/pointer effects as for
+ * replayssm_mamba2_decode. Output o = scale * S_t q, evaluated as
+ *   u <- q; for j = n..1: s = k_j . u; o += beta_j s v_j;
+ *           u <- alpha_j (elementwise) (u - beta_j s k_j);
+ *   o += S_c u,
+ * with A_j = Diag(alpha_j)(I - beta_j k_j k_j^T), S_t = S_{t-1} A_t + beta_t v_t k_t^T.
+ */
+REPLAYSSM_API replayssm_status replayssm_gdn_decode(
+    const replayssm_dims* dims, const replayssm_state* state, const void* q, const void* k,
+    const void* v, const float* alpha, const float* beta, float scale, float* o, void* stream);
+
+/*
+ * Consolidate ("NVIDIA y Princeton aceleran modelos híbridos…", paragraph 2:
+ * the persistent state is only updated when the buffer fills; paragraph 4:
+ * the recurrence runs at high precision, the read copy is refreshed from it).
+ * For every sequence with len + k_next > W, or with force != 0 and len > 0,
+ * folds its len committed entries into S_ckpt in FP32, writes S_ckpt once,
+ * refreshes S_read = bf16_rne(S_ckpt) when S_read is set, and sets
+ * head = (head + len) mod W, len = 0. Other sequences are untouched.
+ * A: f32 [H] for Mamba-2, ignored (may be NULL) for the delta kinds.
+ * k_next >= 0; force is 0 or 1.
+ */
+REPLAYSSM_API replayssm_status replayssm_consolidate(
+    const replayssm_dims* dims, const replayssm_state* state, const float* A, int32_t k_next,
+    int32_t force, void* stream);
+
+/*
+ * Speculative verify for the delta kinds ("ReplaySSM: o ganho aparece…",
+ * section "O que muda para quem desenvolve", and "NVIDIA y Princeton…",
+ * paragraph 3: draft inputs are kept in the buffer, no state copy per
+ * draft). Writes draft i (i < K) of each sequence into slot
+ * (head + len + i) mod W without committing it, and outputs
+ * o[:, i] = scale * S q_i for the state after the committed entries and
+ * drafts 0..i, all K outputs from one read of the checkpoint. Draft fields
+ * are [b, K, H, ...] (alpha [b, K, H] or [b, K, H, d_k], beta [b, K, H]).
+ * Precondition len + K <= W (consolidate with k_next = K first), else
+ * RING_FULL and the sequence is untouched. Mamba-2: REPLAYSSM_ERR_UNSUPPORTED.
+ */
+REPLAYSSM_API replayssm_status replayssm_spec_verify(
+    const replayssm_dims* dims, const replayssm_state* state, int32_t K, const void* q,
+    const void* k, const void* v, const float* alpha, const float* beta, float scale, float* o,
+    void* stream);
+
+/*
+ * Accept the first m[s] verified drafts of each sequence by moving its
+ * pointer: len += m[s] ("ReplaySSM: o ganho aparece…", section "O que muda
+ * para quem desenvolve"; "NVIDIA y Princeton…", paragraph 3). m: int32 [b]
+ * on the device. Requires 0 <= m <= K and len + m <= W, else BAD_ACCEPT and
+ * no change. Rejected drafts stay in their slots until overwritten.
+ */
+REPLAYSSM_API replayssm_status replayssm_accept(
+    const replayssm_dims* dims, const replayssm_state* state, const int32_t* m, int32_t K,
+    void* stream);
+
+/* S_read = bf16_rne(S_ckpt) for the whole batch (initialisation). S_read must be set. */
+REPLAYSSM_API replayssm_status replayssm_refresh_read_copy(
+    const replayssm_dims* dims, const replayssm_state* state, void* stream);
+
+/*
+ * Conventional per-token read-modify-write Mamba-2 step, the baseline the
+ * method replaces ("ReplaySSM: o ganho aparece…", introduction: the whole
+ * state matrix is read and written every token). S: f32 [b, H, P, N],
+ * updated in place: h = exp(dt A) h + dt x B^T; y = h C + D x.
+ */
+REPLAYSSM_API replayssm_status replayssm_conventional_mamba2_step(
+    const replayssm_dims* dims, float* S, const float* A, const float* D, const void* x,
+    const void* B, const void* C, const float* dt, float* y, void* stream);
+
+/*
+ * Conventional per-token read-modify-write GDN/KDA step (same baseline).
+ * S: f32 [b, H, d_v, d_k] updated in place: S = S A_t + beta v k^T;
+ * o = scale * S q.
+ */
+REPLAYSSM_API replayssm_status replayssm_conventional_gdn_step(
+    const replayssm_dims* dims, float* S, const void* q, const void* k, const void* v,
+    const float* alpha, const float* beta, float scale, float* o, void* stream);
+
+/* Static, NUL-terminated description of a return code. */
+REPLAYSSM_API const char* replayssm_status_string(replayssm_status status);
+
+/* Library version as major * 10000 + minor * 100 + patch. */
+REPLAYSSM_API int32_t replayssm_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* REPLAYSSM_H */

@@ -1,0 +1,22 @@
+"""ReplaySSM batched SSM-layer decode for B300 (sm_103a).
+
+The compute lives in the CUDA library ``libreplayssm.so`` (C ABI in
+``include/replayssm.h``); this package is its Python binding. Importing it
+fails if the library has not been built: run
+``python -m recurrent_state_fp32_b300.build``.
+"""
+
+from .api import (  # noqa: F401
+    LayerDims,
+    LayerState,
+    ReplaySSMError,
+    accept,
+    consolidate,
+    conventional_gdn_step,
+    conventional_mamba2_step,
+    gdn_decode,
+    mamba2_decode,
+    refresh_read_copy,
+    spec_verify,
+    version,
+)

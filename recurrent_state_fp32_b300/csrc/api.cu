@@ -1,0 +1,305 @@
+// C ABI of the ReplaySSM library: host-side argument validation, dispatch to
+// the kernel launchers, and the two small kernels (accept, read-copy refresh).
+// Argument errors return before any CUDA call; nothing allocates or syncs.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <mutex>
+
+#include "common.cuh"
+#include "launch.h"
+#include "replayssm.h"
+
+namespace rs {
+
+const DeviceInfo& device_info() {
+  static DeviceInfo info[64];
+  static std::once_flag once[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 0;
+  std::call_once(once[dev], [dev] {
+    int sms = 0, optin = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) sms = 148;
+    if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
+        cudaSuccess)
+      optin = 227 * 1024;
+    info[dev] = DeviceInfo{sms, optin};
+  });
+  return info[dev];
+}
+
+int fold_grid(long long tiles) {
+  const long long min_blocks = (tiles + kMaxFoldTiles - 1) / kMaxFoldTiles;
+  const long long want = std::min<long long>(tiles, (long long)device_info().sms * 8);
+  return (int)std::max<long long>(std::max(min_blocks, want), 1);
+}
+
+namespace {
+
+__global__ void accept_kernel(int batch, int W, int K, const int32_t* __restrict__ m,
+                              int32_t* __restrict__ len, int32_t* __restrict__ status) {
+  const int s = blockIdx.x * blockDim.x + threadIdx.x;
+  if (s >= batch) return;
+  const int mv = m[s], l = len[s];
+  if (l < 0 || l > W)
+    status[s] |= REPLAYSSM_SEQ_BAD_POINTER;
+  else if (mv < 0 || mv > K || l + mv > W)
+    status[s] |= REPLAYSSM_SEQ_BAD_ACCEPT;
+  else
+    len[s] = l + mv;
+}
+
+__global__ void refresh_kernel(const float4* __restrict__ S, uint2* __restrict__ R, long long n4) {
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n4;
+       i += (long long)gridDim.x * blockDim.x) {
+    const float4 v = S[i];
+    R[i] = make_uint2(pack_bf16x2(v.x, v.y), pack_bf16x2(v.z, v.w));
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_accept(const replayssm_dims& d, const replayssm_state& s, const int32_t* m,
+                          int K, cudaStream_t st) {
+  accept_kernel<<<(d.batch + 255) / 256, 256, 0, st>>>(d.batch, d.window, K, m, s.ring_len,
+                                                       s.status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_refresh(const replayssm_dims& d, const replayssm_state& s, cudaStream_t st) {
+  const long long n4 = (long long)d.batch * d.heads * d.dv * d.dk / 4;
+  const long long want = (n4 + 255) / 256;
+  const int grid = (int)std::min<long long>(want, (long long)device_info().sms * 16);
+  refresh_kernel<<<std::max(grid, 1), 256, 0, st>>>(reinterpret_cast<const float4*>(s.S_ckpt),
+                                                    reinterpret_cast<uint2*>(s.S_read), n4);
+  return cudaGetLastError();
+}
+
+}  // namespace rs
+
+// --------------------------------------------------------------- validation
+
+namespace {
+
+using rs::DeviceInfo;
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Null -> INVALID_ARG, misaligned -> MISALIGNED, else OK.
+replayssm_status check_ptr(const void* p) {
+  if (!p) return REPLAYSSM_ERR_INVALID_ARG;
+  return aligned16(p) ? REPLAYSSM_OK : REPLAYSSM_ERR_MISALIGNED;
+}
+
+replayssm_status check_opt(const void* p) {
+  return (!p || aligned16(p)) ? REPLAYSSM_OK : REPLAYSSM_ERR_MISALIGNED;
+}
+
+#define RS_TRY(expr)                               \
+  do {                                             \
+    const replayssm_status rs_st_ = (expr);        \
+    if (rs_st_ != REPLAYSSM_OK) return rs_st_;     \
+  } while (0)
+
+replayssm_status check_dims(const replayssm_dims* d) {
+  if (!d) return REPLAYSSM_ERR_INVALID_ARG;
+  if (d->kind < REPLAYSSM_MAMBA2 || d->kind > REPLAYSSM_KDA) return REPLAYSSM_ERR_INVALID_ARG;
+  if (d->batch < 0 || d->heads < 1 || d->groups < 1 || d->dk < 1 || d->dv < 1 || d->window < 1)
+    return REPLAYSSM_ERR_INVALID_ARG;
+  if (d->in_dtype != REPLAYSSM_F32 && d->in_dtype != REPLAYSSM_BF16)
+    return REPLAYSSM_ERR_INVALID_ARG;
+  if (d->kind == REPLAYSSM_MAMBA2 && d->heads % d->groups) return REPLAYSSM_ERR_INVALID_ARG;
+  if (d->dk != 64 && d->dk != 128) return REPLAYSSM_ERR_UNSUPPORTED;
+  if (d->dv % 32 || d->dv > 256) return REPLAYSSM_ERR_UNSUPPORTED;
+  if (d->window > 64) return REPLAYSSM_ERR_UNSUPPORTED;
+  return REPLAYSSM_OK;
+}
+
+replayssm_status check_state(const replayssm_dims* d, const replayssm_state* s) {
+  if (!s) return REPLAYSSM_ERR_INVALID_ARG;
+  RS_TRY(check_ptr(s->S_ckpt));
+  RS_TRY(check_opt(s->S_read));
+  RS_TRY(check_ptr(s->ring_head));
+  RS_TRY(check_ptr(s->ring_len));
+  RS_TRY(check_ptr(s->status));
+  RS_TRY(check_ptr(s->sync));
+  if (d->kind == REPLAYSSM_MAMBA2) {
+    RS_TRY(check_ptr(s->ring_x));
+    RS_TRY(check_ptr(s->ring_B));
+    RS_TRY(check_opt(s->ring_C));
+    RS_TRY(check_ptr(s->ring_dt));
+  } else {
+    RS_TRY(check_opt(s->ring_q));
+    RS_TRY(check_ptr(s->ring_k));
+    RS_TRY(check_ptr(s->ring_v));
+    RS_TRY(check_ptr(s->ring_alpha));
+    RS_TRY(check_ptr(s->ring_beta));
+  }
+  return REPLAYSSM_OK;
+}
+
+replayssm_status check_mamba2_token(const void* x, const void* B, const void* C, const float* dt) {
+  RS_TRY(check_ptr(x));
+  RS_TRY(check_ptr(B));
+  RS_TRY(check_ptr(C));
+  return check_ptr(dt);
+}
+
+replayssm_status check_delta_token(const void* q, const void* k, const void* v,
+                                   const float* alpha, const float* beta) {
+  RS_TRY(check_ptr(q));
+  RS_TRY(check_ptr(k));
+  RS_TRY(check_ptr(v));
+  RS_TRY(check_ptr(alpha));
+  return check_ptr(beta);
+}
+
+replayssm_status finish(cudaError_t e) {
+  return e == cudaSuccess ? REPLAYSSM_OK : REPLAYSSM_ERR_CUDA;
+}
+
+// Shared memory the replay kernels need must fit one block.
+replayssm_status check_smem(size_t bytes) {
+  return bytes <= (size_t)rs::device_info().smem_optin ? REPLAYSSM_OK : REPLAYSSM_ERR_UNSUPPORTED;
+}
+
+size_t delta_replay_smem(const replayssm_dims* d, int K, bool read16) {
+  const size_t ts = read16 ? 2 : 4;
+  const size_t kda = d->kind == REPLAYSSM_KDA;
+  // one full-head tile (the worst case over row blocks) plus the staged entries
+  return (size_t)d->dv * d->dk * ts + 16 + 4 * ((size_t)d->window * d->dk * (1 + kda) +
+         (size_t)d->window * (2 - kda) + (size_t)d->window * d->dv + (size_t)K * d->dk +
+         (size_t)K * d->window + (size_t)K * d->dv);
+}
+
+}  // namespace
+
+extern "C" {
+
+REPLAYSSM_API replayssm_status replayssm_mamba2_decode(
+    const replayssm_dims* dims, const replayssm_state* state, const float* A, const float* D,
+    const void* x, const void* B, const void* C, const float* dt, float* y, void* stream) {
+  RS_TRY(check_dims(dims));
+  if (dims->kind != REPLAYSSM_MAMBA2) return REPLAYSSM_ERR_INVALID_ARG;
+  RS_TRY(check_state(dims, state));
+  RS_TRY(check_ptr(A));
+  RS_TRY(check_ptr(D));
+  RS_TRY(check_mamba2_token(x, B, C, dt));
+  RS_TRY(check_ptr(y));
+  if (dims->batch == 0) return REPLAYSSM_OK;
+  return finish(rs::launch_mamba2_decode(*dims, *state, A, D, x, B, C, dt, y,
+                                         static_cast<cudaStream_t>(stream)));
+}
+
+REPLAYSSM_API replayssm_status replayssm_gdn_decode(
+    const replayssm_dims* dims, const replayssm_state* state, const void* q, const void* k,
+    const void* v, const float* alpha, const float* beta, float scale, float* o, void* stream) {
+  RS_TRY(check_dims(dims));
+  if (dims->kind == REPLAYSSM_MAMBA2) return REPLAYSSM_ERR_INVALID_ARG;
+  RS_TRY(check_state(dims, state));
+  RS_TRY(check_delta_token(q, k, v, alpha, beta));
+  RS_TRY(check_ptr(o));
+  if (dims->batch == 0) return REPLAYSSM_OK;
+  RS_TRY(check_smem(delta_replay_smem(dims, 1, state->S_read != nullptr)));
+  return finish(rs::launch_delta_decode(*dims, *state, q, k, v, alpha, beta, scale, o,
+                                        static_cast<cudaStream_t>(stream)));
+}
+
+REPLAYSSM_API replayssm_status replayssm_consolidate(const replayssm_dims* dims,
+                                                     const replayssm_state* state, const float* A,
+                                                     int32_t k_next, int32_t force, void* stream) {
+  RS_TRY(check_dims(dims));
+  RS_TRY(check_state(dims, state));
+  if (k_next < 0 || k_next > dims->window || (force != 0 && force != 1))
+    return REPLAYSSM_ERR_INVALID_ARG;
+  if (dims->kind == REPLAYSSM_MAMBA2) RS_TRY(check_ptr(A));
+  if (dims->batch == 0) return REPLAYSSM_OK;
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (dims->kind == REPLAYSSM_MAMBA2)
+    return finish(rs::launch_mamba2_fold(*dims, *state, A, k_next, force, st));
+  return finish(rs::launch_delta_fold(*dims, *state, k_next, force, st));
+}
+
+REPLAYSSM_API replayssm_status replayssm_spec_verify(
+    const replayssm_dims* dims, const replayssm_state* state, int32_t K, const void* q,
+    const void* k, const void* v, const float* alpha, const float* beta, float scale, float* o,
+    void* stream) {
+  RS_TRY(check_dims(dims));
+  if (dims->kind == REPLAYSSM_MAMBA2) return REPLAYSSM_ERR_UNSUPPORTED;
+  if (K < 1 || K > 8) return REPLAYSSM_ERR_INVALID_ARG;
+  if (K > dims->window) return REPLAYSSM_ERR_INVALID_ARG;
+  RS_TRY(check_state(dims, state));
+  RS_TRY(check_delta_token(q, k, v, alpha, beta));
+  RS_TRY(check_ptr(o));
+  if (dims->batch == 0) return REPLAYSSM_OK;
+  RS_TRY(check_smem(delta_replay_smem(dims, K, state->S_read != nullptr)));
+  return finish(rs::launch_delta_verify(*dims, *state, K, q, k, v, alpha, beta, scale, o,
+                                        static_cast<cudaStream_t>(stream)));
+}
+
+REPLAYSSM_API replayssm_status replayssm_accept(const replayssm_dims* dims,
+                                                const replayssm_state* state, const int32_t* m,
+                                                int32_t K, void* stream) {
+  RS_TRY(check_dims(dims));
+  if (K < 0) return REPLAYSSM_ERR_INVALID_ARG;
+  if (!state) return REPLAYSSM_ERR_INVALID_ARG;
+  RS_TRY(check_ptr(state->ring_len));
+  RS_TRY(check_ptr(state->status));
+  RS_TRY(check_ptr(m));
+  if (dims->batch == 0) return REPLAYSSM_OK;
+  return finish(rs::launch_accept(*dims, *state, m, K, static_cast<cudaStream_t>(stream)));
+}
+
+REPLAYSSM_API replayssm_status replayssm_refresh_read_copy(const replayssm_dims* dims,
+                                                           const replayssm_state* state,
+                                                           void* stream) {
+  RS_TRY(check_dims(dims));
+  if (!state) return REPLAYSSM_ERR_INVALID_ARG;
+  RS_TRY(check_ptr(state->S_ckpt));
+  RS_TRY(check_ptr(state->S_read));
+  if (dims->batch == 0) return REPLAYSSM_OK;
+  return finish(rs::launch_refresh(*dims, *state, static_cast<cudaStream_t>(stream)));
+}
+
+REPLAYSSM_API replayssm_status replayssm_conventional_mamba2_step(
+    const replayssm_dims* dims, float* S, const float* A, const float* D, const void* x,
+    const void* B, const void* C, const float* dt, float* y, void* stream) {
+  RS_TRY(check_dims(dims));
+  if (dims->kind != REPLAYSSM_MAMBA2) return REPLAYSSM_ERR_INVALID_ARG;
+  RS_TRY(check_ptr(S));
+  RS_TRY(check_ptr(A));
+  RS_TRY(check_ptr(D));
+  RS_TRY(check_mamba2_token(x, B, C, dt));
+  RS_TRY(check_ptr(y));
+  if (dims->batch == 0) return REPLAYSSM_OK;
+  return finish(rs::launch_mamba2_conventional(*dims, S, A, D, x, B, C, dt, y,
+                                               static_cast<cudaStream_t>(stream)));
+}
+
+REPLAYSSM_API replayssm_status replayssm_conventional_gdn_step(
+    const replayssm_dims* dims, float* S, const void* q, const void* k, const void* v,
+    const float* alpha, const float* beta, float scale, float* o, void* stream) {
+  RS_TRY(check_dims(dims));
+  if (dims->kind == REPLAYSSM_MAMBA2) return REPLAYSSM_ERR_INVALID_ARG;
+  RS_TRY(check_ptr(S));
+  RS_TRY(check_delta_token(q, k, v, alpha, beta));
+  RS_TRY(check_ptr(o));
+  if (dims->batch == 0) return REPLAYSSM_OK;
+  return finish(rs::launch_delta_conventional(*dims, S, q, k, v, alpha, beta, scale, o,
+                                              static_cast<cudaStream_t>(stream)));
+}
+
+REPLAYSSM_API const char* replayssm_status_string(replayssm_status status) {
+  switch (status) {
+    case REPLAYSSM_OK: return "ok";
+    case REPLAYSSM_ERR_INVALID_ARG: return "invalid argument";
+    case REPLAYSSM_ERR_UNSUPPORTED: return "unsupported sizes";
+    case REPLAYSSM_ERR_MISALIGNED: return "tensor pointer not 16-byte aligned";
+    case REPLAYSSM_ERR_CUDA: return "CUDA launch error";
+    default: return "unknown status";
+  }
+}
+
+REPLAYSSM_API int32_t replayssm_version(void) { return 100; }
+
+}  // extern "C"

@@ -1,0 +1,271 @@
+// Device helpers shared by the ReplaySSM kernels: bulk copies with mbarrier
+// completion (bounded waits), bf16 unpacking, warp reductions, and the
+// row-dot engine that streams a state tile from shared memory.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "replayssm.h"
+
+namespace rs {
+
+constexpr int kThreads = 128;  // every ReplaySSM kernel runs 4-warp blocks
+constexpr int kWarps = kThreads / 32;
+constexpr unsigned kFull = 0xffffffffu;
+// Upper bound for any wait on an mbarrier (nanoseconds of %globaltimer).
+constexpr uint64_t kWaitLimitNs = 1000000000ull;
+// Backstop on the number of polls, in case the timer does not advance.
+constexpr uint32_t kWaitLimitPolls = 1u << 26;
+
+typedef __nv_bfloat16 bf16;
+
+// ------------------------------------------------------------ PTX wrappers
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
+               : "memory");
+}
+
+// Makes initialised mbarriers visible to the async (bulk-copy) proxy.
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
+// Bulk (non-tensor) copy global -> shared; completion counted on `bar` in bytes.
+// dst, src and bytes must be multiples of 16. The state stream is read once
+// per step, so it is tagged evict-first to leave L2 to the ring.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes,
+                                         uint64_t* bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1], %2, [%3], %4;" ::"r"(smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Waits for phase `parity` of `bar` to complete; false after ~kWaitLimitNs.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  for (uint32_t i = 0; i < kWaitLimitPolls; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (global_ns() - t0 > kWaitLimitNs) break;
+  }
+  return false;
+}
+
+// ------------------------------------------------------------ element I/O
+
+template <typename T>
+__device__ __forceinline__ float to_f(T v);
+template <>
+__device__ __forceinline__ float to_f<float>(float v) {
+  return v;
+}
+template <>
+__device__ __forceinline__ float to_f<bf16>(bf16 v) {
+  return __bfloat162float(v);
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+// 16 bytes of T as floats: 4 (f32) or 8 (bf16) values.
+template <typename T>
+struct Chunk {
+  static constexpr int kElems = 16 / sizeof(T);
+};
+
+template <typename T>
+__device__ __forceinline__ void unpack(const uint4 raw, float (&f)[Chunk<T>::kElems]);
+template <>
+__device__ __forceinline__ void unpack<float>(const uint4 raw, float (&f)[4]) {
+  f[0] = __uint_as_float(raw.x);
+  f[1] = __uint_as_float(raw.y);
+  f[2] = __uint_as_float(raw.z);
+  f[3] = __uint_as_float(raw.w);
+}
+template <>
+__device__ __forceinline__ void unpack<bf16>(const uint4 raw, float (&f)[8]) {
+  f[0] = bf16_lo(raw.x);
+  f[1] = bf16_hi(raw.x);
+  f[2] = bf16_lo(raw.y);
+  f[3] = bf16_hi(raw.y);
+  f[4] = bf16_lo(raw.z);
+  f[5] = bf16_hi(raw.z);
+  f[6] = bf16_lo(raw.w);
+  f[7] = bf16_hi(raw.w);
+}
+
+// Round-to-nearest-even pack of two floats into a bf16x2 word (low = a).
+__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// Copies `bytes` (a multiple of 16) between 16-byte aligned buffers with
+// every thread of the block taking strided 16-byte chunks.
+__device__ __forceinline__ void block_copy16(void* dst, const void* src, int bytes) {
+  const uint4* s = reinterpret_cast<const uint4*>(src);
+  uint4* d = reinterpret_cast<uint4*>(dst);
+  for (int i = threadIdx.x; i < (bytes >> 4); i += blockDim.x) d[i] = s[i];
+}
+
+// ------------------------------------------------------------ reductions
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
+  return v;
+}
+
+// Reduce-scatter across groups of L lanes: lane l holds L partial sums
+// v[0..L-1]; on return lane l holds the total, over its group, of partial
+// (l mod L). L - 1 shuffles instead of L * log2(L).
+template <int L>
+__device__ __forceinline__ float reduce_scatter(float (&v)[L], int lane) {
+#pragma unroll
+  for (int o = L / 2; o >= 1; o >>= 1) {
+    const bool upper = (lane & o) != 0;
+#pragma unroll
+    for (int k = 0; k < o; ++k) {
+      const float send = upper ? v[k] : v[k + o];
+      const float keep = upper ? v[k + o] : v[k];
+      v[k] = keep + __shfl_xor_sync(kFull, send, o);
+    }
+  }
+  return v[0];
+}
+
+// ------------------------------------------------------------ row-dot engine
+//
+// A state tile sits in shared memory row-major, `COLS` elements of type TS
+// per row. For 32 consecutive rows the engine computes dot(row, vec) with
+// 16-byte loads: lane l reads chunk (l mod LPR) of row (k * RPI + l / LPR) at
+// step k, so each group of 8 lanes reads 128 contiguous bytes (no bank
+// conflicts), then a reduce-scatter leaves row
+//   row0 + (l mod LPR) * RPI + l / LPR
+// in lane l. Each lane needs only the vector elements of its own chunk.
+template <int COLS, typename TS>
+struct RowDot {
+  static constexpr int kEpc = Chunk<TS>::kElems;        // elements per chunk
+  static constexpr int kCpr = COLS / kEpc;              // chunks per row
+  static constexpr int kLpr = kCpr < 32 ? kCpr : 32;    // lanes per row
+  static constexpr int kRpi = 32 / kLpr;                // rows per step
+  static_assert(kCpr == kLpr, "one chunk per lane per row");
+
+  __device__ __forceinline__ static int chunk_of(int lane) { return lane % kLpr; }
+  __device__ __forceinline__ static int row_of(int lane) {
+    return (lane % kLpr) * kRpi + lane / kLpr;
+  }
+
+  // vec: this lane's kEpc vector elements (chunk chunk_of(lane)).
+  __device__ __forceinline__ static float rows32(const TS* tile, int row0, const float (&vec)[kEpc],
+                                                 int lane) {
+    float acc[kLpr];
+    const TS* base = tile + (size_t)(row0 + lane / kLpr) * COLS + chunk_of(lane) * kEpc;
+#pragma unroll
+    for (int k = 0; k < kLpr; ++k) {
+      const uint4 raw = *reinterpret_cast<const uint4*>(base + (size_t)k * kRpi * COLS);
+      float f[kEpc];
+      unpack<TS>(raw, f);
+      float s = 0.f;
+#pragma unroll
+      for (int e = 0; e < kEpc; ++e) s = fmaf(f[e], vec[e], s);
+      acc[k] = s;
+    }
+    return reduce_scatter<kLpr>(acc, lane);
+  }
+};
+
+// Marks the end of one block's share of a sequence's work; the block that
+// completes the sequence (`units` of `total`) runs `last()` after every other
+// block of that sequence has finished (and therefore read the pointers).
+// Call from one thread.
+template <typename F>
+__device__ __forceinline__ void arrive_and_finish(int32_t* sync, int units, int total, F last) {
+  __threadfence();
+  const int old = atomicAdd(sync, units);
+  if (old + units == total) {
+    __threadfence();
+    last();
+    *sync = 0;
+  }
+}
+
+// Tiles of one block (grid-stride over `tiles` tiles, H tiles per sequence)
+// whose sequence folds: len + k_next > W, or force and len > 0. Sequences
+// with out-of-range pointers get REPLAYSSM_SEQ_BAD_POINTER and are skipped. One parallel
+// load of the pointers per block, so a launch with nothing to fold is cheap.
+// The list order is arbitrary; every listed tile is independent.
+constexpr int kMaxFoldTiles = 128;
+struct FoldList {
+  int count;
+  int tile[kMaxFoldTiles];
+  int len[kMaxFoldTiles];
+  int head[kMaxFoldTiles];
+};
+
+// True when a sequence's ring pointers are in range (head < W, len <= W).
+__device__ __forceinline__ bool pointers_ok(int head, int len, int W) {
+  return head >= 0 && head < W && len >= 0 && len <= W;
+}
+
+__device__ __forceinline__ void collect_folds(FoldList& fl, long long tiles, int H,
+                                              const int32_t* ring_len, const int32_t* ring_head,
+                                              int32_t* status, int W, int k_next, int force) {
+  if (threadIdx.x == 0) fl.count = 0;
+  __syncthreads();
+  for (int k = threadIdx.x; k < kMaxFoldTiles; k += blockDim.x) {
+    const long long t = blockIdx.x + (long long)k * gridDim.x;
+    if (t >= tiles) break;
+    const int seq = (int)(t / H);
+    const int len = ring_len[seq], head = ring_head[seq];
+    if (!pointers_ok(head, len, W)) {
+      if (t % H == 0) atomicOr(status + seq, REPLAYSSM_SEQ_BAD_POINTER);
+    } else if (len + k_next > W || (force && len > 0)) {
+      const int pos = atomicAdd(&fl.count, 1);
+      fl.tile[pos] = (int)t;
+      fl.len[pos] = len;
+      fl.head[pos] = head;
+    }
+  }
+  __syncthreads();
+}
+
+}  // namespace rs

@@ -1,0 +1,50 @@
+// Internal launcher interface between the C ABI (api.cu) and the kernel files.
+// Arguments are validated by the caller; launchers only pick tile shapes,
+// grids and template instances.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "replayssm.h"
+
+namespace rs {
+
+// Device facts cached per device (SM count, opt-in shared memory per block).
+struct DeviceInfo {
+  int sms;
+  int smem_optin;
+};
+const DeviceInfo& device_info();
+
+cudaError_t launch_mamba2_decode(const replayssm_dims& d, const replayssm_state& s, const float* A,
+                                 const float* D, const void* x, const void* B, const void* C,
+                                 const float* dt, float* y, cudaStream_t st);
+cudaError_t launch_mamba2_fold(const replayssm_dims& d, const replayssm_state& s, const float* A,
+                               int k_next, int force, cudaStream_t st);
+cudaError_t launch_mamba2_conventional(const replayssm_dims& d, float* S, const float* A,
+                                       const float* D, const void* x, const void* B, const void* C,
+                                       const float* dt, float* y, cudaStream_t st);
+
+cudaError_t launch_delta_decode(const replayssm_dims& d, const replayssm_state& s, const void* q,
+                                const void* k, const void* v, const float* alpha,
+                                const float* beta, float scale, float* o, cudaStream_t st);
+cudaError_t launch_delta_verify(const replayssm_dims& d, const replayssm_state& s, int K,
+                                const void* q, const void* k, const void* v, const float* alpha,
+                                const float* beta, float scale, float* o, cudaStream_t st);
+cudaError_t launch_delta_fold(const replayssm_dims& d, const replayssm_state& s, int k_next,
+                              int force, cudaStream_t st);
+cudaError_t launch_delta_conventional(const replayssm_dims& d, float* S, const void* q,
+                                      const void* k, const void* v, const float* alpha,
+                                      const float* beta, float scale, float* o, cudaStream_t st);
+
+cudaError_t launch_accept(const replayssm_dims& d, const replayssm_state& s, const int32_t* m,
+                          int K, cudaStream_t st);
+cudaError_t launch_refresh(const replayssm_dims& d, const replayssm_state& s, cudaStream_t st);
+
+// Grid for the fold kernels: every block examines at most kFoldTilesPerBlock
+// tiles, so its pre-scan of the ring pointers is a single parallel load.
+constexpr int kFoldTilesPerBlock = 128;
+int fold_grid(long long tiles);
+
+}  // namespace rs

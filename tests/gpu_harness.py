@@ -1,0 +1,192 @@
+"""Runs the CUDA path (through the C-ABI binding) and the CPU oracle side by side
+on the same seeded inputs, and compares them.
+
+Tolerances (the ones the parity bar states):
+  FP32 read path: |gpu - ref| <= 1e-4 + 1e-4 |ref| elementwise.
+  BF16 read copy: per output vector, max |gpu - ref| <= 2e-2 * max |ref|.
+  Consolidated FP32 checkpoint: 1e-4 + 1e-4 |ref| elementwise.
+  Ring slots, head, len, status: bit-exact.
+"""
+
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import synth
+from oracle.method import ReplayOracle
+from recurrent_state_fp32_b300 import api
+
+DEV = "cuda"
+
+
+def dev(a, dtype=torch.float32):
+    return torch.from_numpy(np.ascontiguousarray(a)).to(DEV, dtype)
+
+
+def f32_close(gpu, ref, what, atol=1e-4, rtol=1e-4):
+    gpu = np.asarray(gpu, np.float64)
+    ref = np.asarray(ref, np.float64)
+    assert gpu.shape == ref.shape, f"{what}: {gpu.shape} vs {ref.shape}"
+    err = np.abs(gpu - ref)
+    bad = err > atol + rtol * np.abs(ref)
+    assert not bad.any(), (f"{what}: {int(bad.sum())} of {bad.size} outside tolerance, "
+                           f"max abs err {err.max():.3e}")
+    return float(err.max()) if err.size else 0.0
+
+
+def bf16_close(gpu, ref, what, rel=2e-2):
+    gpu = np.asarray(gpu, np.float64)
+    ref = np.asarray(ref, np.float64)
+    assert gpu.shape == ref.shape, f"{what}: {gpu.shape} vs {ref.shape}"
+    err = np.abs(gpu - ref).max(axis=-1)
+    scale = np.abs(ref).max(axis=-1)
+    bad = err > rel * scale
+    assert not bad.any(), f"{what}: {int(bad.sum())} vectors outside 2e-2, worst {np.max(err / scale):.3e}"
+    return float(np.max(err / np.maximum(scale, 1e-30)))
+
+
+def host(t: torch.Tensor) -> np.ndarray:
+    return t.detach().float().cpu().numpy()
+
+
+def bits(a: np.ndarray) -> np.ndarray:
+    return np.ascontiguousarray(a, np.float32).view(np.uint32)
+
+
+class Session:
+    """One layer state on the GPU plus its oracle twin on a sample of (seq, head).
+
+    kind: "mamba2", "gdn" or "kda"; wl: synth workload; read: "f32" or "bf16".
+    seqs/heads: the sequences and heads the oracle follows (default: all).
+    """
+
+    def __init__(self, kind, wl, read="bf16", seqs=None, heads=None, scale=1.0,
+                 store_optional=True):
+        self.kind, self.wl, self.read, self.scale = kind, wl, read, scale
+        b, H = wl.batch, wl.heads
+        self.seqs = np.arange(b) if seqs is None else np.asarray(seqs)
+        self.heads = np.arange(H) if heads is None else np.asarray(heads)
+        if kind == "mamba2":
+            self.A, self.D, self.dt_bias = synth.mamba2_params(wl.seed, H)
+            S0 = synth.mamba2_initial_state(wl.seed, b, H, wl.P, wl.N)
+            self.dims = api.LayerDims("mamba2", b, H, dk=wl.N, dv=wl.P, window=wl.window,
+                                      groups=wl.groups, in_dtype=wl.in_dtype)
+            if wl.groups > 1 and len(self.heads) != H:
+                raise ValueError("head sampling needs groups == 1")
+        else:
+            S0 = synth.delta_initial_state(wl.seed, b, H, wl.dv, wl.dk)
+            self.dims = api.LayerDims(kind, b, H, dk=wl.dk, dv=wl.dv, window=wl.window,
+                                      in_dtype=wl.in_dtype)
+        self.state = api.LayerState(self.dims, read_copy=(read == "bf16"),
+                                    store_optional=store_optional)
+        self.state.set_checkpoint(dev(S0))
+        sub = S0[self.seqs][:, self.heads]
+        if kind == "mamba2":
+            self.dA, self.dD = dev(self.A), dev(self.D)
+            self.oracle = ReplayOracle(kind, sub, wl.window, A=self.A[self.heads],
+                                       D=self.D[self.heads], groups=wl.groups,
+                                       store_optional=store_optional)
+        else:
+            self.oracle = ReplayOracle(kind, sub, wl.window, scale=scale,
+                                       store_optional=store_optional)
+        self.vt = self.dims.vec_dtype
+        self.worst = 0.0
+
+    # --------------------------------------------------------------- inputs
+    def token(self, t):
+        wl = self.wl
+        if self.kind == "mamba2":
+            return synth.mamba2_step_inputs(wl.seed, t, wl.batch, wl.heads, wl.groups, wl.P,
+                                            wl.N, self.dt_bias, wl.in_dtype)
+        return synth.delta_step_inputs(wl.seed, t, wl.batch, wl.heads, wl.dk, wl.dv, self.kind,
+                                       wl.in_dtype)
+
+    def _sub(self, tok, axis_heads=1):
+        out = {}
+        for k, v in tok.items():
+            v = v[self.seqs]
+            if not (self.kind == "mamba2" and k in ("B", "C")):
+                v = np.take(v, self.heads, axis=axis_heads)
+            out[k] = v
+        return out
+
+    def _vec(self, name):
+        return name in ("x", "B", "C", "q", "k", "v")
+
+    def _to_dev(self, tok):
+        return {k: dev(v, self.vt if self._vec(k) else torch.float32) for k, v in tok.items()}
+
+    # ---------------------------------------------------------------- calls
+    def consolidate(self, k_next=1, force=False):
+        api.consolidate(self.dims, self.state, self.dA if self.kind == "mamba2" else None,
+                        k_next, force)
+        return self.oracle.consolidate(k_next, force)
+
+    def decode(self, t, check=True):
+        tok = self.token(t)
+        g = self._to_dev(tok)
+        rows = self.wl.P if self.kind == "mamba2" else self.wl.dv
+        y = torch.full((self.wl.batch, self.wl.heads, rows), float("nan"), device=DEV)
+        if self.kind == "mamba2":
+            api.mamba2_decode(self.dims, self.state, self.dA, self.dD, g["x"], g["B"], g["C"],
+                              g["dt"], y)
+        else:
+            api.gdn_decode(self.dims, self.state, g["q"], g["k"], g["v"], g["alpha"], g["beta"],
+                           self.scale, y)
+        ref = self.oracle.decode(self._sub(tok))
+        if check:
+            got = host(y)[self.seqs][:, self.heads]
+            self.compare_out(got, ref, f"step {t}")
+        return y, ref
+
+    def compare_out(self, got, ref, what):
+        ok = ~np.isnan(ref).any(axis=-1)
+        assert np.array_equal(np.isnan(got).any(axis=-1), ~ok), f"{what}: refused rows differ"
+        if self.read == "f32":
+            self.worst = max(self.worst, f32_close(got[ok], ref[ok], what))
+        else:
+            self.worst = max(self.worst, bf16_close(got[ok], ref[ok], what))
+
+    def verify(self, r, K):
+        wl = self.wl
+        d = synth.spec_draft_inputs(wl.seed, r, wl.batch, K, wl.heads, wl.dk, wl.dv, self.kind,
+                                    wl.in_dtype)
+        g = self._to_dev(d)
+        o = torch.full((wl.batch, K, wl.heads, wl.dv), float("nan"), device=DEV)
+        api.spec_verify(self.dims, self.state, K, g["q"], g["k"], g["v"], g["alpha"], g["beta"],
+                        self.scale, o)
+        sub = {k: np.take(v[self.seqs], self.heads, axis=2) for k, v in d.items()}
+        ref = self.oracle.spec_verify(K, sub)
+        got = host(o)[self.seqs][:, :, self.heads]
+        self.compare_out(got, ref, f"verify round {r}")
+        return o, ref
+
+    def accept(self, m, K):
+        api.accept(self.dims, self.state, dev(m, torch.int32), K)
+        self.oracle.accept(np.asarray(m)[self.seqs], K)
+
+    # ------------------------------------------------------------- checks
+    def check_pointers(self, what=""):
+        st = self.state
+        for name, g, o in (("head", st.ring_head, self.oracle.head),
+                           ("len", st.ring_len, self.oracle.len),
+                           ("status", st.status, self.oracle.status)):
+            got = g.cpu().numpy()[self.seqs]
+            assert np.array_equal(got, o), f"{what} {name}: gpu {got} oracle {o}"
+        assert int(st.sync.abs().sum()) == 0, "arrival counters not back at zero"
+
+    def check_ring(self, what=""):
+        for name, ref in self.oracle.ring.items():
+            g = host(self.state.ring[name])[self.seqs]
+            if not (self.kind == "mamba2" and name in ("B", "C")):
+                g = np.take(g, self.heads, axis=2)
+            assert np.array_equal(bits(g), bits(ref)), f"{what} ring field {name} differs"
+
+    def check_checkpoint(self, what=""):
+        got = host(self.state.S_ckpt)[self.seqs][:, self.heads]
+        f32_close(got, self.oracle.ckpt, f"{what} checkpoint")
+        if self.state.S_read is not None:
+            rd = self.state.S_read.view(torch.int16)
+            want = self.state.S_ckpt.to(torch.bfloat16).view(torch.int16)
+            assert torch.equal(rd, want), f"{what} read copy is not bf16_rne(checkpoint)"

@@ -1,0 +1,143 @@
+"""The C-ABI library on the host: it loads, exports every declared entry point,
+and rejects bad arguments before any CUDA call (no GPU needed).
+
+Every call here either fails validation or has batch == 0, so nothing is ever
+launched; fake device addresses are never dereferenced.
+"""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from recurrent_state_fp32_b300 import _abi
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "replayssm.h")
+
+FAKE = 0x10000  # 16-byte aligned, never dereferenced
+MISALIGNED = 0x10008
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"REPLAYSSM_API\s+[\w\s\*]+?\b(replayssm_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_symbols()
+    for n in ("replayssm_mamba2_decode", "replayssm_gdn_decode", "replayssm_consolidate",
+              "replayssm_spec_verify", "replayssm_accept"):
+        assert n in names
+    assert set(names) == set(_abi.SIGNATURES), "binding and header disagree"
+
+
+def test_library_exports_every_declared_symbol():
+    lib = ctypes.CDLL(_abi.LIB_PATH)
+    for n in declared_symbols():
+        assert hasattr(lib, n), n
+
+
+def test_version_and_strings():
+    assert _abi.lib.replayssm_version() == 100
+    for code in range(5):
+        assert _abi.lib.replayssm_status_string(code)
+    assert b"unknown" in _abi.lib.replayssm_status_string(99)
+
+
+def dims(kind=_abi.MAMBA2, batch=2, heads=4, groups=1, dk=128, dv=64, window=16,
+         in_dtype=_abi.BF16):
+    return _abi.Dims(kind, batch, heads, groups, dk, dv, window, in_dtype)
+
+
+def state(**over):
+    f = {name: FAKE for name, _ in _abi.State._fields_}
+    f.update(over)
+    return _abi.State(**f)
+
+
+def m2_decode(d, s, y=FAKE, A=FAKE):
+    r = ctypes.byref
+    return _abi.lib.replayssm_mamba2_decode(r(d) if d is not None else None,
+                                            r(s) if s is not None else None,
+                                            A, FAKE, FAKE, FAKE, FAKE, FAKE, y, None)
+
+
+def test_null_and_bad_dims():
+    assert m2_decode(None, state()) == _abi.ERR_INVALID_ARG
+    assert m2_decode(dims(), None) == _abi.ERR_INVALID_ARG
+    assert m2_decode(dims(kind=7), state()) == _abi.ERR_INVALID_ARG
+    assert m2_decode(dims(kind=_abi.GDN), state()) == _abi.ERR_INVALID_ARG  # wrong entry point
+    assert m2_decode(dims(batch=-1), state()) == _abi.ERR_INVALID_ARG
+    assert m2_decode(dims(heads=0), state()) == _abi.ERR_INVALID_ARG
+    assert m2_decode(dims(groups=3), state()) == _abi.ERR_INVALID_ARG   # 3 does not divide 4
+    assert m2_decode(dims(in_dtype=5), state()) == _abi.ERR_INVALID_ARG
+    assert m2_decode(dims(window=0), state()) == _abi.ERR_INVALID_ARG
+
+
+def test_unsupported_sizes():
+    assert m2_decode(dims(dk=96), state()) == _abi.ERR_UNSUPPORTED
+    assert m2_decode(dims(dv=48), state()) == _abi.ERR_UNSUPPORTED
+    assert m2_decode(dims(dv=288), state()) == _abi.ERR_UNSUPPORTED
+    assert m2_decode(dims(window=65), state()) == _abi.ERR_UNSUPPORTED
+
+
+def test_null_and_misaligned_pointers():
+    assert m2_decode(dims(), state(S_ckpt=None)) == _abi.ERR_INVALID_ARG
+    assert m2_decode(dims(), state(ring_len=None)) == _abi.ERR_INVALID_ARG
+    assert m2_decode(dims(), state(sync=None)) == _abi.ERR_INVALID_ARG
+    assert m2_decode(dims(), state(), y=None) == _abi.ERR_INVALID_ARG
+    assert m2_decode(dims(), state(), A=None) == _abi.ERR_INVALID_ARG
+    assert m2_decode(dims(), state(S_read=MISALIGNED)) == _abi.ERR_MISALIGNED
+    assert m2_decode(dims(), state(ring_x=MISALIGNED)) == _abi.ERR_MISALIGNED
+    assert m2_decode(dims(), state(), y=MISALIGNED) == _abi.ERR_MISALIGNED
+
+
+def test_empty_batch_is_a_noop():
+    assert m2_decode(dims(batch=0), state()) == _abi.OK
+    r = ctypes.byref
+    d = dims(kind=_abi.GDN, batch=0, dv=128)
+    assert _abi.lib.replayssm_gdn_decode(r(d), r(state()), FAKE, FAKE, FAKE, FAKE, FAKE,
+                                         1.0, FAKE, None) == _abi.OK
+    assert _abi.lib.replayssm_consolidate(r(d), r(state()), None, 1, 0, None) == _abi.OK
+    assert _abi.lib.replayssm_spec_verify(r(d), r(state()), 4, FAKE, FAKE, FAKE, FAKE, FAKE,
+                                          1.0, FAKE, None) == _abi.OK
+    assert _abi.lib.replayssm_accept(r(d), r(state()), FAKE, 4, None) == _abi.OK
+
+
+def test_call_specific_checks():
+    r = ctypes.byref
+    g = dims(kind=_abi.GDN, dv=128)
+    m = dims()
+    # consolidate: k_next in [0, W], force in {0, 1}, A required for Mamba-2
+    assert _abi.lib.replayssm_consolidate(r(g), r(state()), None, 17, 0, None) == _abi.ERR_INVALID_ARG
+    assert _abi.lib.replayssm_consolidate(r(g), r(state()), None, -1, 0, None) == _abi.ERR_INVALID_ARG
+    assert _abi.lib.replayssm_consolidate(r(g), r(state()), None, 1, 2, None) == _abi.ERR_INVALID_ARG
+    assert _abi.lib.replayssm_consolidate(r(m), r(state()), None, 1, 0, None) == _abi.ERR_INVALID_ARG
+    # verify: K in [1, 8] and K <= W; Mamba-2 not built
+    sv = _abi.lib.replayssm_spec_verify
+    assert sv(r(g), r(state()), 0, FAKE, FAKE, FAKE, FAKE, FAKE, 1.0, FAKE, None) == _abi.ERR_INVALID_ARG
+    assert sv(r(g), r(state()), 9, FAKE, FAKE, FAKE, FAKE, FAKE, 1.0, FAKE, None) == _abi.ERR_INVALID_ARG
+    g4 = dims(kind=_abi.GDN, dv=128, window=3)
+    assert sv(r(g4), r(state()), 4, FAKE, FAKE, FAKE, FAKE, FAKE, 1.0, FAKE, None) == _abi.ERR_INVALID_ARG
+    assert sv(r(m), r(state()), 4, FAKE, FAKE, FAKE, FAKE, FAKE, 1.0, FAKE, None) == _abi.ERR_UNSUPPORTED
+    # accept: K >= 0, m required
+    assert _abi.lib.replayssm_accept(r(g), r(state()), FAKE, -1, None) == _abi.ERR_INVALID_ARG
+    assert _abi.lib.replayssm_accept(r(g), r(state()), None, 4, None) == _abi.ERR_INVALID_ARG
+    # refresh needs a read copy
+    assert _abi.lib.replayssm_refresh_read_copy(r(g), r(state(S_read=None)), None) == _abi.ERR_INVALID_ARG
+    # conventional steps check their kind
+    assert _abi.lib.replayssm_conventional_mamba2_step(r(g), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE,
+                                                       FAKE, FAKE, None) == _abi.ERR_INVALID_ARG
+    assert _abi.lib.replayssm_conventional_gdn_step(r(m), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1.0,
+                                                    FAKE, None) == _abi.ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("missing", ["ring_k", "ring_v", "ring_alpha", "ring_beta"])
+def test_delta_state_requires_its_ring(missing):
+    r = ctypes.byref
+    g = dims(kind=_abi.KDA, dv=128)
+    st = state(**{missing: None})
+    assert _abi.lib.replayssm_gdn_decode(r(g), r(st), FAKE, FAKE, FAKE, FAKE, FAKE, 1.0, FAKE,
+                                         None) == _abi.ERR_INVALID_ARG
