@@ -301,6 +301,10 @@ def run_ours(args, rank, local_rank, world):
         clocks.__exit__(None, None, None)
     ms = max_over_ranks(start.elapsed_time(end), world)
     dec_ms = [d0[i].elapsed_time(d1[i]) for i in range(K)]
+    bad = int(layer.state.status.ne(0).sum().item())
+    if bad:
+        print(f"warning: {bad} sequences report device status bits "
+              f"{sorted(set(layer.state.status.tolist()))}", file=sys.stderr)
 
     # algorithmic bytes of the timed region
     dec_bytes, fold_bytes, ln = 0, 0, len0
@@ -340,6 +344,7 @@ def run_ours(args, rank, local_rank, world):
             "avg_launch_us": round(1e3 * sum(dec_ms) / K, 3),
         },
         "gpu_launches": 2 * K,
+        "device_status_ok": bad == 0,
     }
     if clocks:
         res["clocks"] = clocks.summary()

@@ -39,7 +39,13 @@
  *                   dt [b, H] f32 (already activated, > 0)
  *  delta token      q, k [b, H, d_k], v [b, H, d_v] (in_dtype);
  *                   alpha f32 [b, H] (GDN) or [b, H, d_k] (KDA); beta f32 [b, H]
- *  ring fields      the token layout with a W axis after b: [b, W, ...]
+ *  ring fields      per head, slot-major inside the head so that a head's W
+ *                   entries are contiguous: x [b, H, W, P]; q, k [b, H, W, d_k];
+ *                   v [b, H, W, d_v]; KDA alpha [b, H, W, d_k]. Scalar fields
+ *                   (dt, beta, GDN alpha) are [b, H, Wd] with Wd = W rounded up
+ *                   to a multiple of 4 (pad entries unused). Mamba-2 B and C are
+ *                   per group: [b, W, G, N]. Slot s of a sequence holds entry
+ *                   (s - head) mod W after its checkpoint.
  *  pointers         ring_head, ring_len, status, sync: int32 [b]
  *  outputs          f32: y [b, H, P]; o [b, H, d_v]; verify o [b, K, H, d_v]
  *
@@ -107,15 +113,15 @@ typedef struct replayssm_dims {
 typedef struct replayssm_state {
   float* S_ckpt;      /* f32 checkpoint, never rounded */
   void* S_read;       /* bf16 read copy or NULL */
-  void* ring_x;       /* Mamba-2 [b, W, H, P]    in_dtype */
+  void* ring_x;       /* Mamba-2 [b, H, W, P]    in_dtype */
   void* ring_B;       /* Mamba-2 [b, W, G, N]    in_dtype */
   void* ring_C;       /* Mamba-2 [b, W, G, N]    in_dtype, optional */
-  float* ring_dt;     /* Mamba-2 [b, W, H]       f32 */
-  void* ring_q;       /* delta   [b, W, H, d_k]  in_dtype, optional */
-  void* ring_k;       /* delta   [b, W, H, d_k]  in_dtype */
-  void* ring_v;       /* delta   [b, W, H, d_v]  in_dtype */
-  float* ring_alpha;  /* GDN [b, W, H]; KDA [b, W, H, d_k] f32 */
-  float* ring_beta;   /* delta   [b, W, H]       f32 */
+  float* ring_dt;     /* Mamba-2 [b, H, Wd]      f32 */
+  void* ring_q;       /* delta   [b, H, W, d_k]  in_dtype, optional */
+  void* ring_k;       /* delta   [b, H, W, d_k]  in_dtype */
+  void* ring_v;       /* delta   [b, H, W, d_v]  in_dtype */
+  float* ring_alpha;  /* GDN [b, H, Wd]; KDA [b, H, W, d_k] f32 */
+  float* ring_beta;   /* delta   [b, H, Wd]      f32 */
   int32_t* ring_head; /* slot of the oldest entry after the checkpoint */
   int32_t* ring_len;  /* committed entries after the checkpoint, 0..W */
   int32_t* status;    /* REPLAYSSM_SEQ_* bits; the library only sets bits */

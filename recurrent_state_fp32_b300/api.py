@@ -68,11 +68,17 @@ def _stream(stream) -> int | None:
     return int(stream)
 
 
+def ring_wd(W: int) -> int:
+    """Entries per (sequence, head) of a scalar ring field: W rounded up to 4."""
+    return (W + 3) & ~3
+
+
 class LayerState:
     """Caller-owned device buffers of one layer's decode state.
 
-    S_ckpt f32 [b,H,dv,dk]; S_read bf16 (optional); ring fields [b,W,...];
-    ring_head, ring_len, status, sync int32 [b], zero-initialised.
+    S_ckpt f32 [b,H,dv,dk]; S_read bf16 (optional); per-head ring fields
+    [b,H,W,...] (scalar ones [b,H,Wd]); Mamba-2 B/C [b,W,G,N]; ring_head,
+    ring_len, status, sync int32 [b], zero-initialised.
     """
 
     def __init__(self, dims: LayerDims, device="cuda", read_copy: bool = True,
@@ -84,21 +90,22 @@ class LayerState:
         self.S_ckpt = torch.zeros((b, H, d.dv, d.dk), dtype=torch.float32, **z)
         self.S_read = torch.zeros_like(self.S_ckpt, dtype=torch.bfloat16) if read_copy else None
         vt = d.vec_dtype
+        Wd = ring_wd(W)
         self.ring = {}
         if d.kind == "mamba2":
-            self.ring["x"] = torch.zeros((b, W, H, d.dv), dtype=vt, **z)
+            self.ring["x"] = torch.zeros((b, H, W, d.dv), dtype=vt, **z)
             self.ring["B"] = torch.zeros((b, W, d.groups, d.dk), dtype=vt, **z)
             if store_optional:
                 self.ring["C"] = torch.zeros((b, W, d.groups, d.dk), dtype=vt, **z)
-            self.ring["dt"] = torch.zeros((b, W, H), dtype=torch.float32, **z)
+            self.ring["dt"] = torch.zeros((b, H, Wd), dtype=torch.float32, **z)
         else:
             if store_optional:
-                self.ring["q"] = torch.zeros((b, W, H, d.dk), dtype=vt, **z)
-            self.ring["k"] = torch.zeros((b, W, H, d.dk), dtype=vt, **z)
-            self.ring["v"] = torch.zeros((b, W, H, d.dv), dtype=vt, **z)
-            ashape = (b, W, H) if d.kind == "gdn" else (b, W, H, d.dk)
+                self.ring["q"] = torch.zeros((b, H, W, d.dk), dtype=vt, **z)
+            self.ring["k"] = torch.zeros((b, H, W, d.dk), dtype=vt, **z)
+            self.ring["v"] = torch.zeros((b, H, W, d.dv), dtype=vt, **z)
+            ashape = (b, H, Wd) if d.kind == "gdn" else (b, H, W, d.dk)
             self.ring["alpha"] = torch.zeros(ashape, dtype=torch.float32, **z)
-            self.ring["beta"] = torch.zeros((b, W, H), dtype=torch.float32, **z)
+            self.ring["beta"] = torch.zeros((b, H, Wd), dtype=torch.float32, **z)
         self.ring_head = torch.zeros(b, dtype=torch.int32, **z)
         self.ring_len = torch.zeros(b, dtype=torch.int32, **z)
         self.status = torch.zeros(b, dtype=torch.int32, **z)

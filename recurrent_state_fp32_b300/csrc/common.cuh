@@ -11,7 +11,7 @@
 
 namespace rs {
 
-constexpr int kThreads = 128;  // every ReplaySSM kernel runs 4-warp blocks
+constexpr int kThreads = 128;  // block size of the non-persistent kernels
 constexpr int kWarps = kThreads / 32;
 constexpr unsigned kFull = 0xffffffffu;
 // Upper bound for any wait on an mbarrier (nanoseconds of %globaltimer).
@@ -20,6 +20,13 @@ constexpr uint64_t kWaitLimitNs = 1000000000ull;
 constexpr uint32_t kWaitLimitPolls = 1u << 26;
 
 typedef __nv_bfloat16 bf16;
+
+// Scalar-per-entry ring fields (Mamba-2 dt, delta beta and GDN alpha) keep
+// W entries per (sequence, head) padded to a multiple of 4 floats, so that a
+// head's row is a 16-byte multiple and can be bulk-copied.
+__host__ __device__ constexpr int ring_wd(int W) { return (W + 3) & ~3; }
+
+__host__ __device__ constexpr size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 // ------------------------------------------------------------ PTX wrappers
 
@@ -43,6 +50,36 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
                : "memory");
 }
 
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_cnt(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
+               : "memory");
+}
+
+// Per-thread asynchronous copies global -> shared (completion: cp_async_wait_all).
+__device__ __forceinline__ void cp_async4(void* dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst)), "l"(src)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.wait_all;" ::: "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+// Waits until at most N of this thread's committed groups are still pending.
+template <int N>
+__device__ __forceinline__ void cp_async_wait_group() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
 __device__ __forceinline__ uint64_t l2_evict_first_policy() {
   uint64_t pol;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
@@ -58,6 +95,16 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
       "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes.L2::cache_hint"
       " [%0], [%1], %2, [%3], %4;" ::"r"(smem_u32(dst)),
       "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
+
+// Same without a cache-policy operand (default L2 behaviour).
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes,
+                                         uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1], %2, [%3];" ::"r"(smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
       : "memory");
 }
 
@@ -87,6 +134,12 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
     if (global_ns() - t0 > kWaitLimitNs) break;
   }
   return false;
+}
+
+// Warp-uniform bounded wait: every lane waits, then the lanes agree, so a
+// timeout never splits the warp's control flow.
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity) {
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity)) != 0;
 }
 
 // ------------------------------------------------------------ element I/O
@@ -130,6 +183,19 @@ __device__ __forceinline__ void unpack<bf16>(const uint4 raw, float (&f)[8]) {
   f[5] = bf16_hi(raw.z);
   f[6] = bf16_lo(raw.w);
   f[7] = bf16_hi(raw.w);
+}
+
+// Two consecutive elements as floats (4- or 8-byte aligned load).
+template <typename T>
+__device__ __forceinline__ float2 load2(const T* p);
+template <>
+__device__ __forceinline__ float2 load2<float>(const float* p) {
+  return *reinterpret_cast<const float2*>(p);
+}
+template <>
+__device__ __forceinline__ float2 load2<bf16>(const bf16* p) {
+  const uint32_t w = *reinterpret_cast<const uint32_t*>(p);
+  return make_float2(bf16_lo(w), bf16_hi(w));
 }
 
 // Round-to-nearest-even pack of two floats into a bf16x2 word (low = a).
@@ -210,6 +276,58 @@ struct RowDot {
       acc[k] = s;
     }
     return reduce_scatter<kLpr>(acc, lane);
+  }
+
+  // Split form of rows32 for a consumer that frees the shared tile early:
+  // load32 copies this lane's chunks of 32 rows into registers, dot32 does
+  // the arithmetic and the reduce-scatter on them.
+  __device__ __forceinline__ static void load32(const TS* tile, int row0, int lane,
+                                                uint4 (&raw)[kLpr]) {
+    const TS* base = tile + (size_t)(row0 + lane / kLpr) * COLS + chunk_of(lane) * kEpc;
+#pragma unroll
+    for (int k = 0; k < kLpr; ++k)
+      raw[k] = *reinterpret_cast<const uint4*>(base + (size_t)k * kRpi * COLS);
+  }
+  __device__ __forceinline__ static float dot32(const uint4 (&raw)[kLpr], const float (&vec)[kEpc],
+                                                int lane) {
+    float acc[kLpr];
+#pragma unroll
+    for (int k = 0; k < kLpr; ++k) {
+      float f[kEpc];
+      unpack<TS>(raw[k], f);
+      float s = 0.f;
+#pragma unroll
+      for (int e = 0; e < kEpc; ++e) s = fmaf(f[e], vec[e], s);
+      acc[k] = s;
+    }
+    return reduce_scatter<kLpr>(acc, lane);
+  }
+
+  // Two independent 32-row groups at once (loads first, then both reductions).
+  __device__ __forceinline__ static void rows32x2(const TS* tile, int row0a, int row0b,
+                                                  const float (&vec)[kEpc], int lane, float& da,
+                                                  float& db) {
+    float acc_a[kLpr], acc_b[kLpr];
+    const TS* ba = tile + (size_t)(row0a + lane / kLpr) * COLS + chunk_of(lane) * kEpc;
+    const TS* bb = tile + (size_t)(row0b + lane / kLpr) * COLS + chunk_of(lane) * kEpc;
+#pragma unroll
+    for (int k = 0; k < kLpr; ++k) {
+      const uint4 ra = *reinterpret_cast<const uint4*>(ba + (size_t)k * kRpi * COLS);
+      const uint4 rb = *reinterpret_cast<const uint4*>(bb + (size_t)k * kRpi * COLS);
+      float fa[kEpc], fb[kEpc];
+      unpack<TS>(ra, fa);
+      unpack<TS>(rb, fb);
+      float sa = 0.f, sb = 0.f;
+#pragma unroll
+      for (int e = 0; e < kEpc; ++e) {
+        sa = fmaf(fa[e], vec[e], sa);
+        sb = fmaf(fb[e], vec[e], sb);
+      }
+      acc_a[k] = sa;
+      acc_b[k] = sb;
+    }
+    da = reduce_scatter<kLpr>(acc_a, lane);
+    db = reduce_scatter<kLpr>(acc_b, lane);
   }
 };
 

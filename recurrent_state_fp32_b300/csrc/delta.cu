@@ -71,8 +71,11 @@ __device__ __forceinline__ void stage_entries(const DDecode& a, int seq, int h, 
   const TI* rv = reinterpret_cast<const TI*>(a.ring_v);
   const TI* ik = reinterpret_cast<const TI*>(a.k);
   const TI* iv = reinterpret_cast<const TI*>(a.v);
-  // index of (seq, entry j, head h) in a [b, W, H] ring or a [b, K, H] input
-  auto ring_ix = [&](int j) { return ((size_t)seq * W + (hd + j) % W) * H + h; };
+  // ring rows of (seq, h): vector fields [b, H, W, d], scalar fields [b, H, Wd];
+  // inputs [b, K, H, ...]
+  const int Wd = ring_wd(W);
+  auto ring_ix = [&](int j) { return ((size_t)seq * H + h) * W + (hd + j) % W; };
+  auto ring_sx = [&](int j) { return ((size_t)seq * H + h) * Wd + (hd + j) % W; };
   auto in_ix = [&](int j) { return ((size_t)seq * a.K + (j - len)) * H + h; };
   for (int idx = threadIdx.x; idx < n * DK; idx += kThreads) {
     const int j = idx / DK, c = idx - j * DK;
@@ -84,8 +87,8 @@ __device__ __forceinline__ void stage_entries(const DDecode& a, int seq, int h, 
     vbuf[idx] = to_f(j < len ? rv[ring_ix(j) * DV + r] : iv[in_ix(j) * DV + r]);
   }
   for (int j = threadIdx.x; j < n; j += kThreads) {
-    bbuf[j] = j < len ? a.ring_beta[ring_ix(j)] : a.beta[in_ix(j)];
-    if (!KDA) abuf[j] = j < len ? a.ring_alpha[ring_ix(j)] : a.alpha[in_ix(j)];
+    bbuf[j] = j < len ? a.ring_beta[ring_sx(j)] : a.beta[in_ix(j)];
+    if (!KDA) abuf[j] = j < len ? a.ring_alpha[ring_sx(j)] : a.alpha[in_ix(j)];
   }
 }
 
@@ -94,7 +97,8 @@ template <int DK, typename TI, bool KDA>
 __device__ __forceinline__ void append_entry(const DDecode& a, int seq, int h, int i, int slot) {
   const int H = a.H, W = a.W, DV = a.DV;
   const size_t in_ix = ((size_t)seq * a.K + i) * H + h;
-  const size_t ring_ix = ((size_t)seq * W + slot) * H + h;
+  const size_t ring_ix = ((size_t)seq * H + h) * W + slot;
+  const size_t ring_sx = ((size_t)seq * H + h) * ring_wd(W) + slot;
   block_copy16(reinterpret_cast<TI*>(a.ring_k) + ring_ix * DK,
                reinterpret_cast<const TI*>(a.k) + in_ix * DK, DK * (int)sizeof(TI));
   block_copy16(reinterpret_cast<TI*>(a.ring_v) + ring_ix * DV,
@@ -104,8 +108,8 @@ __device__ __forceinline__ void append_entry(const DDecode& a, int seq, int h, i
                  reinterpret_cast<const TI*>(a.q) + in_ix * DK, DK * (int)sizeof(TI));
   if (KDA) block_copy16(a.ring_alpha + ring_ix * DK, a.alpha + in_ix * DK, DK * 4);
   if (threadIdx.x == 0) {
-    a.ring_beta[ring_ix] = a.beta[in_ix];
-    if (!KDA) a.ring_alpha[ring_ix] = a.alpha[in_ix];
+    a.ring_beta[ring_sx] = a.beta[in_ix];
+    if (!KDA) a.ring_alpha[ring_sx] = a.alpha[in_ix];
   }
 }
 
@@ -271,7 +275,8 @@ __global__ void __launch_bounds__(kThreads) delta_fold_kernel(const DFold a) {
     const int t = fl.tile[f], len = fl.len[f], hd = fl.head[f];
     const int seq = t / H, h = t - seq * H;
     const int n = len;
-    auto ring_ix = [&](int j) { return ((size_t)seq * W + (hd + j) % W) * H + h; };
+    auto ring_ix = [&](int j) { return ((size_t)seq * H + h) * W + (hd + j) % W; };
+    auto ring_sx = [&](int j) { return ((size_t)seq * H + h) * ring_wd(W) + (hd + j) % W; };
     for (int idx = tid; idx < n * DK; idx += kThreads) {
       const int j = idx / DK, c = idx - j * DK;
       kbuf[idx] = to_f(rk[ring_ix(j) * DK + c]);
@@ -282,8 +287,8 @@ __global__ void __launch_bounds__(kThreads) delta_fold_kernel(const DFold a) {
       vbuf[idx] = to_f(rv[ring_ix(j) * DV + r]);
     }
     for (int j = tid; j < n; j += kThreads) {
-      bbuf[j] = a.ring_beta[ring_ix(j)];
-      if (!KDA) abuf[j] = a.ring_alpha[ring_ix(j)];
+      bbuf[j] = a.ring_beta[ring_sx(j)];
+      if (!KDA) abuf[j] = a.ring_alpha[ring_sx(j)];
     }
     __syncthreads();
     const int q = lane & 3;
