@@ -108,7 +108,11 @@ typedef struct replayssm_dims {
  * and fills S_ckpt (then calls replayssm_refresh_read_copy if S_read is set).
  * `sync` is scratch used by the kernels to order the per-sequence pointer
  * update after every block of that sequence has read it; each call leaves it
- * at zero.
+ * at zero. `work` is scratch for the per-head values a decode or verify call
+ * derives from the ring before it streams the state (the buffer terms, the
+ * decay or the swept query); it must hold replayssm_workspace_bytes(dims, K)
+ * bytes for the largest K used with this state, needs no initialisation and
+ * is overwritten by every decode and verify call.
  */
 typedef struct replayssm_state {
   float* S_ckpt;      /* f32 checkpoint, never rounded */
@@ -126,6 +130,7 @@ typedef struct replayssm_state {
   int32_t* ring_len;  /* committed entries after the checkpoint, 0..W */
   int32_t* status;    /* REPLAYSSM_SEQ_* bits; the library only sets bits */
   int32_t* sync;      /* scratch arrival counters, zero between calls */
+  float* work;        /* scratch, replayssm_workspace_bytes(dims, K) bytes, any contents */
 } replayssm_state;
 
 /*
@@ -224,6 +229,12 @@ REPLAYSSM_API replayssm_status replayssm_conventional_mamba2_step(
 REPLAYSSM_API replayssm_status replayssm_conventional_gdn_step(
     const replayssm_dims* dims, float* S, const void* q, const void* k, const void* v,
     const float* alpha, const float* beta, float scale, float* o, void* stream);
+
+/*
+ * Size in bytes of state->work for decode calls (K = 1) and verify calls
+ * with up to K drafts on the given sizes (0 if dims is invalid).
+ */
+REPLAYSSM_API int64_t replayssm_workspace_bytes(const replayssm_dims* dims, int32_t K);
 
 /* Static, NUL-terminated description of a return code. */
 REPLAYSSM_API const char* replayssm_status_string(replayssm_status status);

@@ -31,7 +31,7 @@ class State(ctypes.Structure):
     _fields_ = [("S_ckpt", _P), ("S_read", _P), ("ring_x", _P), ("ring_B", _P), ("ring_C", _P),
                 ("ring_dt", _P), ("ring_q", _P), ("ring_k", _P), ("ring_v", _P),
                 ("ring_alpha", _P), ("ring_beta", _P), ("ring_head", _P), ("ring_len", _P),
-                ("status", _P), ("sync", _P)]
+                ("status", _P), ("sync", _P), ("work", _P)]
 
 
 _DP = ctypes.POINTER(Dims)
@@ -49,6 +49,7 @@ SIGNATURES = {
     "replayssm_refresh_read_copy": [_DP, _SP, _P],
     "replayssm_conventional_mamba2_step": [_DP, _P, _P, _P, _P, _P, _P, _P, _P, _P],
     "replayssm_conventional_gdn_step": [_DP, _P, _P, _P, _P, _P, _P, _F, _P, _P],
+    "replayssm_workspace_bytes": [_DP, _I],
     "replayssm_status_string": [_I],
     "replayssm_version": [],
 }
@@ -63,7 +64,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     for name, args in SIGNATURES.items():
         fn = getattr(lib, name)
         fn.argtypes = args
-        fn.restype = ctypes.c_char_p if name == "replayssm_status_string" else ctypes.c_int32
+        fn.restype = {"replayssm_status_string": ctypes.c_char_p,
+                      "replayssm_workspace_bytes": ctypes.c_int64}.get(name, ctypes.c_int32)
     return lib
 
 

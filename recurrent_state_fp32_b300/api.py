@@ -82,7 +82,7 @@ class LayerState:
     """
 
     def __init__(self, dims: LayerDims, device="cuda", read_copy: bool = True,
-                 store_optional: bool = True):
+                 store_optional: bool = True, max_drafts: int = 1):
         d = dims
         b, W, H = d.batch, d.window, d.heads
         z = dict(device=device)
@@ -110,6 +110,8 @@ class LayerState:
         self.ring_len = torch.zeros(b, dtype=torch.int32, **z)
         self.status = torch.zeros(b, dtype=torch.int32, **z)
         self.sync = torch.zeros(b, dtype=torch.int32, **z)
+        nbytes = workspace_bytes(d, max_drafts)
+        self.work = torch.empty((nbytes + 3) // 4, dtype=torch.float32, **z)
         self._c = None
 
     def c(self) -> _abi.State:
@@ -121,7 +123,7 @@ class LayerState:
         self._c = _abi.State(_ptr(self.S_ckpt), _ptr(self.S_read), g("x"), g("B"), g("C"),
                              g("dt"), g("q"), g("k"), g("v"), g("alpha"), g("beta"),
                              _ptr(self.ring_head), _ptr(self.ring_len), _ptr(self.status),
-                             _ptr(self.sync))
+                             _ptr(self.sync), _ptr(self.work))
         return self._c
 
     def set_checkpoint(self, S: torch.Tensor, stream=None) -> None:
@@ -180,6 +182,11 @@ def conventional_mamba2_step(dims, S, A, D, x, B, C, dt, y, stream=None):
 def conventional_gdn_step(dims, S, q, k, v, alpha, beta, scale, o, stream=None):
     _call("replayssm_conventional_gdn_step", ctypes.byref(dims.c()), _ptr(S), _ptr(q), _ptr(k),
           _ptr(v), _ptr(alpha), _ptr(beta), float(scale), _ptr(o), _stream(stream))
+
+
+def workspace_bytes(dims: LayerDims, K: int = 1) -> int:
+    """Bytes of scratch a state needs for decode (K = 1) and verify with up to K drafts."""
+    return int(_abi.lib.replayssm_workspace_bytes(ctypes.byref(dims.c()), int(K)))
 
 
 def version() -> int:

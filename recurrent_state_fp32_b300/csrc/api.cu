@@ -123,6 +123,7 @@ replayssm_status check_state(const replayssm_dims* d, const replayssm_state* s) 
   RS_TRY(check_ptr(s->ring_len));
   RS_TRY(check_ptr(s->status));
   RS_TRY(check_ptr(s->sync));
+  RS_TRY(check_ptr(s->work));
   if (d->kind == REPLAYSSM_MAMBA2) {
     RS_TRY(check_ptr(s->ring_x));
     RS_TRY(check_ptr(s->ring_B));
@@ -287,6 +288,11 @@ REPLAYSSM_API replayssm_status replayssm_conventional_gdn_step(
   if (dims->batch == 0) return REPLAYSSM_OK;
   return finish(rs::launch_delta_conventional(*dims, S, q, k, v, alpha, beta, scale, o,
                                               static_cast<cudaStream_t>(stream)));
+}
+
+REPLAYSSM_API int64_t replayssm_workspace_bytes(const replayssm_dims* dims, int32_t K) {
+  if (check_dims(dims) != REPLAYSSM_OK || K < 0) return 0;
+  return rs::WorkLayout(*dims, K < 1 ? 1 : K).bytes();
 }
 
 REPLAYSSM_API const char* replayssm_status_string(replayssm_status status) {

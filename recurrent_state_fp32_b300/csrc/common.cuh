@@ -155,6 +155,9 @@ __device__ __forceinline__ float to_f<bf16>(bf16 v) {
   return __bfloat162float(v);
 }
 
+// exp with full float accuracy (the library's expf).
+__device__ __forceinline__ float __expf_acc(float x) { return expf(x); }
+
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 

@@ -10,6 +10,23 @@
 
 namespace rs {
 
+// Layout of state.work: rows of `row` floats per (sequence, draft, head) --
+// Mamba-2: buffer terms [0, P) and decay at P; delta: swept query [0, d_k)
+// and buffer terms [d_k, d_k + d_v) -- then one int32 flag per sequence.
+struct WorkLayout {
+  int row;         // floats per row (a multiple of 4)
+  long long rows;  // batch * K * heads
+  long long batch;
+  WorkLayout(const replayssm_dims& d, int K) {
+    const int need = d.kind == REPLAYSSM_MAMBA2 ? d.dv + 1 : d.dk + d.dv;
+    row = (need + 3) & ~3;
+    batch = d.batch;
+    rows = batch * (K < 1 ? 1 : K) * d.heads;
+  }
+  long long bytes() const { return rows * row * 4 + ((batch * 4 + 15) & ~15LL); }
+  int32_t* flags(float* work) const { return reinterpret_cast<int32_t*>(work + rows * row); }
+};
+
 // Device facts cached per device (SM count, opt-in shared memory per block).
 struct DeviceInfo {
   int sms;

@@ -81,7 +81,8 @@ class Session:
             self.dims = api.LayerDims(kind, b, H, dk=wl.dk, dv=wl.dv, window=wl.window,
                                       in_dtype=wl.in_dtype)
         self.state = api.LayerState(self.dims, read_copy=(read == "bf16"),
-                                    store_optional=store_optional)
+                                    store_optional=store_optional,
+                                    max_drafts=max(1, getattr(wl, "K", 1)))
         self.state.set_checkpoint(dev(S0))
         sub = S0[self.seqs][:, self.heads]
         if kind == "mamba2":

@@ -141,3 +141,16 @@ def test_delta_state_requires_its_ring(missing):
     st = state(**{missing: None})
     assert _abi.lib.replayssm_gdn_decode(r(g), r(st), FAKE, FAKE, FAKE, FAKE, FAKE, 1.0, FAKE,
                                          None) == _abi.ERR_INVALID_ARG
+
+
+def test_workspace_size():
+    r = ctypes.byref
+    m = dims(batch=2, heads=4, dk=128, dv=64)            # Mamba-2: P + 1 floats, padded to 4
+    assert _abi.lib.replayssm_workspace_bytes(r(m), 1) == 2 * 4 * 68 * 4 + 16
+    g = dims(kind=_abi.GDN, batch=3, heads=2, dk=128, dv=96)
+    assert _abi.lib.replayssm_workspace_bytes(r(g), 1) == 3 * 2 * 224 * 4 + 16
+    assert _abi.lib.replayssm_workspace_bytes(r(g), 4) == 3 * 4 * 2 * 224 * 4 + 16
+    assert _abi.lib.replayssm_workspace_bytes(r(dims(dk=96)), 1) == 0
+    assert _abi.lib.replayssm_workspace_bytes(None, 1) == 0
+    assert m2_decode(dims(), state(work=None)) == _abi.ERR_INVALID_ARG
+    assert m2_decode(dims(), state(work=MISALIGNED)) == _abi.ERR_MISALIGNED
