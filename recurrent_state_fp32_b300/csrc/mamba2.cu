@@ -320,8 +320,11 @@ __global__ void __launch_bounds__(32 * kPrepWarps) mamba2_prep_kernel(const M2Pr
     arrive_and_finish(a.sync + cur_seq, v1 - seq_first, H, [&] { a.len[cur_seq] = len + 1; });
 }
 
+constexpr int kFoldThreads = 256;
+constexpr int kFoldRows = 8;  // contiguous state rows per thread (loads in flight)
+
 struct M2Fold {
-  int batch, H, G, P, W, k_next, force;
+  int batch, H, G, P, W, HB, k_next, force;  // HB: heads per unit
   float* S;
   bf16* Sr;
   const float* A;
@@ -334,84 +337,155 @@ struct M2Fold {
   int32_t* sync;
 };
 
-// Grid-stride over (sequence, head) tiles; only tiles of folding sequences do
-// work. Per tile: stage B_j and w_j x_j in shared memory, then every float4 of
-// the FP32 checkpoint is read once, updated in registers and written once
-// (plus its bf16 read copy).
+// Shared memory of the fold block (byte offsets).
+struct M2FoldSmem {
+  size_t xr, Br, dtr, Av, coef, Bf, wts, dec, total;
+  __host__ __device__ M2FoldSmem(int HB, int P, int N, int W, int ti) {
+    xr = 0;                                                  // [HB][W][P] x_j (in_dtype)
+    Br = align_up((size_t)HB * W * P * ti, 16);              // [W][N] B_j (in_dtype)
+    dtr = Br + align_up((size_t)W * N * ti, 16);             // [HB][Wd] ring dt rows
+    Av = dtr + (size_t)HB * ring_wd(W) * 4;                  // [HB] A
+    coef = Av + align_up((size_t)HB * 4, 16);                // [HB][W][P] w_j x_j[p]
+    Bf = coef + (size_t)HB * W * P * 4;                      // [W][N] B_j as float
+    wts = Bf + (size_t)W * N * 4;                            // [HB][W] w_j
+    dec = wts + (size_t)HB * W * 4;                          // [HB] decay
+    total = dec + (size_t)HB * 4;
+  }
+};
+
+// Consolidate for Mamba-2. Units are (sequence, HB consecutive heads); only
+// units of folding sequences do work (one parallel pre-scan of the pointers
+// per block). For a unit with n = len buffered entries the fold is the
+// rank-n update
+//   h_new[p][c] = decay h[p][c] + sum_j coef[j][p] B_j[c],
+//   coef[j][p] = w_j x_j[p],  w_j = dt_j exp(A sum_{i>j} dt_i),
+//   decay = exp(A sum_i dt_i).
+// The unit's ring rows are staged with async copies, then coef and B are
+// expanded to float in shared memory. Each thread owns a tile of kFoldRows
+// contiguous rows by one float4 of columns: per entry j it reads two float4
+// of coef (the same address across the lanes of a row: a broadcast) and one
+// float4 of B, and issues 32 FMAs. The FP32 checkpoint and its BF16 read copy
+// are written once.
 template <int N, typename TI>
-__global__ void __launch_bounds__(kThreads) mamba2_fold_kernel(const M2Fold a) {
+__global__ void __launch_bounds__(kFoldThreads, 3) mamba2_fold_kernel(const M2Fold a) {
   extern __shared__ __align__(128) unsigned char smem[];
   __shared__ FoldList fl;
-  __shared__ float s_w[64];
-  __shared__ float s_decay;
-  const int tid = threadIdx.x;
-  const int H = a.H, G = a.G, P = a.P, W = a.W;
-  float* Bs = reinterpret_cast<float*>(smem);  // [W][N]
-  float* xw = Bs + (size_t)W * N;              // [W][P]
-  const TI* rx = reinterpret_cast<const TI*>(a.ring_x);
-  const TI* rB = reinterpret_cast<const TI*>(a.ring_B);
+  constexpr int CT = N / 4;              // lanes across a row (one float4 each)
+  constexpr int SUB = 32 / CT;           // row tiles per warp
+  constexpr int kWarps = kFoldThreads / 32;
+  constexpr int kRowStep = kWarps * SUB * kFoldRows;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int c4 = lane % CT, sub = lane / CT;
+  const int H = a.H, G = a.G, P = a.P, W = a.W, HB = a.HB, hpg = H / G, Wd = ring_wd(W);
+  const int per_seq = (H + HB - 1) / HB;
+  const M2FoldSmem L(HB, P, N, W, sizeof(TI));
+  const TI* xr = reinterpret_cast<const TI*>(smem + L.xr);
+  const TI* Br = reinterpret_cast<const TI*>(smem + L.Br);
+  const float* dtr = reinterpret_cast<const float*>(smem + L.dtr);
+  const float* Av = reinterpret_cast<const float*>(smem + L.Av);
+  float* coef = reinterpret_cast<float*>(smem + L.coef);
+  float* Bf = reinterpret_cast<float*>(smem + L.Bf);
+  float* wts = reinterpret_cast<float*>(smem + L.wts);
+  float* dec = reinterpret_cast<float*>(smem + L.dec);
+  const unsigned char* rx = reinterpret_cast<const unsigned char*>(a.ring_x);
+  const unsigned char* rB = reinterpret_cast<const unsigned char*>(a.ring_B);
+  const int xrow = P * (int)sizeof(TI), xcpr = xrow / 16;  // x row bytes, 16 B chunks
+  const int brow = N * (int)sizeof(TI), bcpr = brow / 16;  // B row bytes, chunks
 
-  collect_folds(fl, (long long)a.batch * H, H, a.len, a.head, a.status, W, a.k_next, a.force);
-  for (int f = 0; f < fl.count; ++f) {
-    const int t = fl.tile[f], len = fl.len[f], hd = fl.head[f];
-    const int seq = t / H, h = t - seq * H, g = h / (H / G);
-    const int n = len;
-    for (int idx = tid; idx < n * N; idx += kThreads) {
-      const int j = idx / N, c = idx - j * N;
-      Bs[idx] = to_f(rB[(((size_t)seq * W + (hd + j) % W) * G + g) * N + c]);
+  collect_folds(fl, (long long)a.batch * per_seq, per_seq, a.len, a.head, a.status, W, a.k_next,
+                a.force);
+  // B rows (entries 0..n-1) of group g of sequence seq, as float
+  auto stage_B = [&](int seq, int g, int n, int hd) {
+    for (int idx = tid; idx < n * bcpr; idx += kFoldThreads) {
+      const int j = idx / bcpr, c = idx - j * bcpr;
+      const int slot = hd + j < W ? hd + j : hd + j - W;
+      cp_async16(smem + L.Br + (size_t)j * brow + c * 16,
+                 rB + (((size_t)seq * W + slot) * G + g) * brow + c * 16);
     }
-    if (tid == 0) {
-      const float Ah = a.A[h];
+    cp_async_wait_all();
+    __syncthreads();
+    for (int i = tid; i < n * N; i += kFoldThreads) Bf[i] = to_f(Br[i]);
+  };
+  for (int f = 0; f < fl.count; ++f) {
+    const int t = fl.tile[f], n = fl.len[f], hd = fl.head[f];
+    const int seq = t / per_seq, h0 = (t - seq * per_seq) * HB, nh = min(HB, H - h0);
+    // stage the unit's x rows, dt rows and A
+    for (int idx = tid; idx < nh * n * xcpr; idx += kFoldThreads) {
+      const int hh = idx / (n * xcpr), rem = idx - hh * (n * xcpr);
+      const int j = rem / xcpr, c = rem - j * xcpr;
+      const int slot = hd + j < W ? hd + j : hd + j - W;
+      cp_async16(smem + L.xr + ((size_t)hh * W + j) * xrow + c * 16,
+                 rx + (((size_t)seq * H + h0 + hh) * W + slot) * xrow + c * 16);
+    }
+    for (int idx = tid; idx < nh * Wd / 4; idx += kFoldThreads)
+      cp_async16(smem + L.dtr + 16 * idx, a.ring_dt + ((size_t)seq * H + h0) * Wd + 4 * idx);
+    for (int hh = tid; hh < nh; hh += kFoldThreads)
+      cp_async4(smem + L.Av + 4 * hh, a.A + h0 + hh);
+    int g_loaded = h0 / hpg;
+    stage_B(seq, g_loaded, n, hd);  // waits for all copies above too
+    // weights and decay, one thread per head
+    for (int hh = tid; hh < nh; hh += kFoldThreads) {
+      const float Ah = Av[hh];
       float acc = 0.f;
       for (int j = n - 1; j >= 0; --j) {
-        const float dtj = a.ring_dt[((size_t)seq * H + h) * ring_wd(W) + (hd + j) % W];
-        s_w[j] = dtj * expf(Ah * acc);
+        const float dtj = dtr[hh * Wd + (hd + j < W ? hd + j : hd + j - W)];
+        wts[hh * W + j] = dtj * expf(Ah * acc);
         acc += dtj;
       }
-      s_decay = expf(Ah * acc);
+      dec[hh] = expf(Ah * acc);
     }
     __syncthreads();
-    for (int idx = tid; idx < n * P; idx += kThreads) {
-      const int j = idx / P, p = idx - j * P;
-      xw[idx] = s_w[j] * to_f(rx[(((size_t)seq * H + h) * W + (hd + j) % W) * P + p]);
+    for (int i = tid; i < nh * n * P; i += kFoldThreads) {
+      const int hh = i / (n * P), rem = i - hh * (n * P), j = rem / P;
+      coef[(size_t)hh * W * P + rem] = wts[hh * W + j] * to_f(xr[(size_t)hh * W * P + rem]);
     }
     __syncthreads();
-    const float decay = s_decay;
-    float4* St = reinterpret_cast<float4*>(a.S + (size_t)t * P * N);
-    uint2* Rt = a.Sr ? reinterpret_cast<uint2*>(a.Sr + (size_t)t * P * N) : nullptr;
-    constexpr int kC4 = N / 4;  // float4 chunks per row
-    const int chunks = P * kC4;
-    constexpr int kU = 4;
-    for (int base = tid; base < chunks; base += kThreads * kU) {
-      float4 hv[kU];
-#pragma unroll
-      for (int u = 0; u < kU; ++u) {
-        const int ci = base + u * kThreads;
-        if (ci < chunks) hv[u] = St[ci];
+    for (int hh = 0; hh < nh; ++hh) {
+      const int g = (h0 + hh) / hpg;
+      if (g != g_loaded) {  // B rows of this head's group
+        __syncthreads();
+        stage_B(seq, g, n, hd);
+        __syncthreads();
+        g_loaded = g;
       }
+      const float decay = dec[hh];
+      const float* ch = coef + (size_t)hh * W * P;
+      float4* St = reinterpret_cast<float4*>(a.S + ((size_t)seq * H + h0 + hh) * P * N);
+      uint2* Rt = a.Sr ? reinterpret_cast<uint2*>(a.Sr + ((size_t)seq * H + h0 + hh) * P * N) : nullptr;
+      for (int p0 = (warp * SUB + sub) * kFoldRows; p0 < P; p0 += kRowStep) {
+        float4 acc[kFoldRows];
 #pragma unroll
-      for (int u = 0; u < kU; ++u) {
-        const int ci = base + u * kThreads;
-        if (ci >= chunks) break;
-        const int p = ci / kC4, c4 = (ci - p * kC4) * 4;
-        float r0 = decay * hv[u].x, r1 = decay * hv[u].y, r2 = decay * hv[u].z,
-              r3 = decay * hv[u].w;
-        for (int j = 0; j < n; ++j) {
-          const float xv = xw[j * P + p];
-          const float4 b = *reinterpret_cast<const float4*>(Bs + j * N + c4);
-          r0 = fmaf(xv, b.x, r0);
-          r1 = fmaf(xv, b.y, r1);
-          r2 = fmaf(xv, b.z, r2);
-          r3 = fmaf(xv, b.w, r3);
+        for (int r = 0; r < kFoldRows; ++r) {
+          const float4 hv = St[(size_t)(p0 + r) * CT + c4];
+          acc[r] = make_float4(decay * hv.x, decay * hv.y, decay * hv.z, decay * hv.w);
         }
-        St[ci] = make_float4(r0, r1, r2, r3);
-        if (Rt) Rt[ci] = make_uint2(pack_bf16x2(r0, r1), pack_bf16x2(r2, r3));
+#pragma unroll 2
+        for (int j = 0; j < n; ++j) {
+          const float4 b = reinterpret_cast<const float4*>(Bf + j * N)[c4];
+          const float4 cl = reinterpret_cast<const float4*>(ch + j * P + p0)[0];
+          const float4 ch4 = reinterpret_cast<const float4*>(ch + j * P + p0)[1];
+          const float cr[kFoldRows] = {cl.x, cl.y, cl.z, cl.w, ch4.x, ch4.y, ch4.z, ch4.w};
+#pragma unroll
+          for (int r = 0; r < kFoldRows; ++r) {
+            acc[r].x = fmaf(cr[r], b.x, acc[r].x);
+            acc[r].y = fmaf(cr[r], b.y, acc[r].y);
+            acc[r].z = fmaf(cr[r], b.z, acc[r].z);
+            acc[r].w = fmaf(cr[r], b.w, acc[r].w);
+          }
+        }
+#pragma unroll
+        for (int r = 0; r < kFoldRows; ++r) {
+          St[(size_t)(p0 + r) * CT + c4] = acc[r];
+          if (Rt)
+            Rt[(size_t)(p0 + r) * CT + c4] =
+                make_uint2(pack_bf16x2(acc[r].x, acc[r].y), pack_bf16x2(acc[r].z, acc[r].w));
+        }
       }
     }
     __syncthreads();
     if (tid == 0)
-      arrive_and_finish(a.sync + seq, 1, H, [&] {
-        a.head[seq] = (hd + len) % W;
+      arrive_and_finish(a.sync + seq, nh, H, [&] {
+        a.head[seq] = (hd + n) % W;
         a.len[seq] = 0;
       });
   }
@@ -547,25 +621,27 @@ cudaError_t launch_mamba2_decode(const replayssm_dims& d, const replayssm_state&
 
 cudaError_t launch_mamba2_fold(const replayssm_dims& d, const replayssm_state& s, const float* A,
                                int k_next, int force, cudaStream_t st) {
-  M2Fold a{d.batch, d.heads, d.groups, d.dv, d.window, k_next, force, s.S_ckpt,
+  // heads per unit: the staged rows and coefficients stay under 48 KB
+  const int ti = d.in_dtype == REPLAYSSM_BF16 ? 2 : 4;
+  int HB = 8;
+  while (HB > 1 && (size_t)HB * d.window * d.dv * (ti + 4) > 48 * 1024) HB /= 2;
+  M2Fold a{d.batch, d.heads, d.groups, d.dv, d.window, HB, k_next, force, s.S_ckpt,
            reinterpret_cast<bf16*>(s.S_read), A, s.ring_x, s.ring_B, s.ring_dt,
            s.ring_head, s.ring_len, s.status, s.sync};
-  const long long tiles = (long long)d.batch * d.heads;
-  const size_t smem = (size_t)d.window * (d.dk + d.dv) * sizeof(float);
-  const int grid = fold_grid(tiles);
+  const long long units = (long long)d.batch * ((d.heads + HB - 1) / HB);
+  const M2FoldSmem L(HB, d.dv, d.dk, d.window, ti);
+  const int grid = std::max<long long>((units + kMaxFoldTiles - 1) / kMaxFoldTiles,
+                                       std::min<long long>(units, (long long)device_info().sms * 3));
   const bool in16 = d.in_dtype == REPLAYSSM_BF16;
   cudaError_t e;
-  if (d.dk == 128) {
-    auto kern = in16 ? mamba2_fold_kernel<128, bf16> : mamba2_fold_kernel<128, float>;
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    kern<<<grid, kThreads, smem, st>>>(a);
-  } else {
-    auto kern = in16 ? mamba2_fold_kernel<64, bf16> : mamba2_fold_kernel<64, float>;
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    kern<<<grid, kThreads, smem, st>>>(a);
-  }
+  void (*kern)(const M2Fold);
+  if (d.dk == 128)
+    kern = in16 ? mamba2_fold_kernel<128, bf16> : mamba2_fold_kernel<128, float>;
+  else
+    kern = in16 ? mamba2_fold_kernel<64, bf16> : mamba2_fold_kernel<64, float>;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L.total);
+  if (e != cudaSuccess) return e;
+  kern<<<grid, kFoldThreads, L.total, st>>>(a);
   return cudaGetLastError();
 }
 
