@@ -72,6 +72,7 @@ typedef int32_t replayssm_status;
 #define REPLAYSSM_ERR_UNSUPPORTED 2 /* sizes outside the compiled tile shapes */
 #define REPLAYSSM_ERR_MISALIGNED 3  /* a tensor pointer not 16-byte aligned */
 #define REPLAYSSM_ERR_CUDA 4        /* the kernel launch reported an error */
+#define REPLAYSSM_ERR_SCRATCH_LIMIT 5 /* sizes need more than the fixed no-alloc scratch */
 
 /* Per-sequence device status bits, OR-ed into state->status[seq]. */
 #define REPLAYSSM_SEQ_RING_FULL 1  /* decode/verify would overflow the ring */
@@ -229,6 +230,44 @@ REPLAYSSM_API replayssm_status replayssm_conventional_mamba2_step(
 REPLAYSSM_API replayssm_status replayssm_conventional_gdn_step(
     const replayssm_dims* dims, float* S, const void* q, const void* k, const void* v,
     const float* alpha, const float* beta, float scale, float* o, void* stream);
+
+/*
+ * Mamba-2 replay decode that allocates nothing and needs no caller scratch.
+ * The paper has no counterpart: this is a library convenience.
+ *
+ * Some callers cannot allocate device memory when they decode: a plugin or
+ * custom operator whose host framework owns all device memory and allows no
+ * allocation inside its execution step, or a serving loop that reserved the
+ * whole device for its state pool up front, where a late cudaMalloc can fail
+ * and a cudaFree synchronizes the device. This entry point computes exactly
+ * what replayssm_mamba2_decode computes, with the same arguments, but takes
+ * its scratch -- the per-head workspace and the per-sequence arrival counters
+ * that replayssm_mamba2_decode reads from state->work and state->sync -- from
+ * one fixed array of REPLAYSSM_NOALLOC_SCRATCH_BYTES (16 MiB) in the
+ * library's own device memory. state->work and state->sync are not read and
+ * may be NULL; every other state field, input and output is as for
+ * replayssm_mamba2_decode, and the caller still owns all of them.
+ *
+ * Limit: align256(replayssm_workspace_bytes(dims, 1)) + 4 * batch bytes must
+ * not exceed REPLAYSSM_NOALLOC_SCRATCH_BYTES, else the call returns
+ * REPLAYSSM_ERR_SCRATCH_LIMIT before any CUDA call. (Batch 256 x 128 heads
+ * at P = 64 needs about 8.5 MiB.)
+ *
+ * The array exists once per GPU that loads the library and is held until the
+ * process exits. The first call on a device (with that device current) looks
+ * up the array's device address, once; make that first call before any stream
+ * capture. Each call clears the arrival counters (the only part that must
+ * start at zero) on `stream` before its kernels; the workspace rows and flags
+ * are written before they are read. All calls share the one array, so calls
+ * whose work overlaps on the GPU (other streams, other host threads) race and
+ * give wrong results: serialize them, e.g. on one stream.
+ */
+REPLAYSSM_API replayssm_status replayssm_mamba2_decode_noalloc(
+    const replayssm_dims* dims, const replayssm_state* state, const float* A, const float* D,
+    const void* x, const void* B, const void* C, const float* dt, float* y, void* stream);
+
+/* Size of the fixed scratch of replayssm_mamba2_decode_noalloc. */
+#define REPLAYSSM_NOALLOC_SCRATCH_BYTES (16u << 20)
 
 /*
  * Size in bytes of state->work for decode calls (K = 1) and verify calls

@@ -16,6 +16,7 @@ from .api import (  # noqa: F401
     conventional_mamba2_step,
     gdn_decode,
     mamba2_decode,
+    mamba2_decode_noalloc,
     refresh_read_copy,
     spec_verify,
     version,

@@ -13,6 +13,8 @@ LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libreplayss
 
 # Return codes and per-sequence status bits (values fixed by the header).
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_MISALIGNED, ERR_CUDA = 0, 1, 2, 3, 4
+ERR_SCRATCH_LIMIT = 5
+NOALLOC_SCRATCH_BYTES = 16 << 20  # fixed scratch of replayssm_mamba2_decode_noalloc
 SEQ_RING_FULL, SEQ_BAD_ACCEPT, SEQ_TIMEOUT, SEQ_BAD_POINTER = 1, 2, 4, 8
 MAMBA2, GDN, KDA = 0, 1, 2
 F32, BF16 = 0, 1
@@ -42,6 +44,7 @@ _F = ctypes.c_float
 # name -> argtypes (every entry point returns int32 except the two helpers)
 SIGNATURES = {
     "replayssm_mamba2_decode": [_DP, _SP, _P, _P, _P, _P, _P, _P, _P, _P],
+    "replayssm_mamba2_decode_noalloc": [_DP, _SP, _P, _P, _P, _P, _P, _P, _P, _P],
     "replayssm_gdn_decode": [_DP, _SP, _P, _P, _P, _P, _P, _F, _P, _P],
     "replayssm_consolidate": [_DP, _SP, _P, _I, _I, _P],
     "replayssm_spec_verify": [_DP, _SP, _I, _P, _P, _P, _P, _P, _F, _P, _P],

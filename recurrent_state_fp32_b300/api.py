@@ -147,6 +147,17 @@ def mamba2_decode(dims, state, A, D, x, B, C, dt, y, stream=None):
           _ptr(dt), _ptr(y), _stream(stream))
 
 
+def mamba2_decode_noalloc(dims, state, A, D, x, B, C, dt, y, stream=None):
+    """mamba2_decode for callers that cannot allocate device memory when they
+    decode (a plugin whose host framework owns all device memory, a serving
+    loop that reserved the device for its state pool): the scratch comes from
+    the library's fixed 16 MiB array instead of state.work and state.sync.
+    Calls that overlap on the GPU share that array and race."""
+    d, s = _refs(dims, state)
+    _call("replayssm_mamba2_decode_noalloc", d, s, _ptr(A), _ptr(D), _ptr(x), _ptr(B), _ptr(C),
+          _ptr(dt), _ptr(y), _stream(stream))
+
+
 def gdn_decode(dims, state, q, k, v, alpha, beta, scale, o, stream=None):
     d, s = _refs(dims, state)
     _call("replayssm_gdn_decode", d, s, _ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(beta),

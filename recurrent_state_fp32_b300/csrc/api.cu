@@ -175,6 +175,49 @@ size_t delta_replay_smem(const replayssm_dims* d, int K, bool read16) {
 
 }  // namespace
 
+// ------------------------------------------------ fixed scratch (no allocation)
+
+// Scratch of replayssm_mamba2_decode_noalloc: module memory that every device
+// loading this library holds until exit; never allocated by a call. Host code
+// must not pass the symbol itself to a kernel (on the host it names a
+// stand-in, not device memory): it uses the address looked up per device.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[REPLAYSSM_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+
+// Where the decode scratch lives in the fixed array: the workspace (per-head
+// rows, then per-sequence flags), then the per-sequence arrival counters.
+struct NoallocLayout {
+  long long sync_off, total;
+  explicit NoallocLayout(const replayssm_dims& d) {
+    sync_off = (rs::WorkLayout(d, 1).bytes() + 255) & ~255LL;
+    total = sync_off + 4LL * d.batch;
+  }
+};
+
+// Device address of g_noalloc_scratch on the current device, looked up once
+// per device with that device current.
+cudaError_t noalloc_scratch(unsigned char** out) {
+  constexpr int kMaxDevices = 64;
+  static std::mutex mu;
+  static unsigned char* addr[kMaxDevices] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!addr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return e;
+    addr[dev] = static_cast<unsigned char*>(p);
+  }
+  *out = addr[dev];
+  return cudaSuccess;
+}
+
+}  // namespace
+
 extern "C" {
 
 REPLAYSSM_API replayssm_status replayssm_mamba2_decode(
@@ -295,6 +338,35 @@ REPLAYSSM_API int64_t replayssm_workspace_bytes(const replayssm_dims* dims, int3
   return rs::WorkLayout(*dims, K < 1 ? 1 : K).bytes();
 }
 
+REPLAYSSM_API replayssm_status replayssm_mamba2_decode_noalloc(
+    const replayssm_dims* dims, const replayssm_state* state, const float* A, const float* D,
+    const void* x, const void* B, const void* C, const float* dt, float* y, void* stream) {
+  RS_TRY(check_dims(dims));
+  if (dims->kind != REPLAYSSM_MAMBA2 || !state) return REPLAYSSM_ERR_INVALID_ARG;
+  replayssm_state s = *state;
+  // work and sync are replaced by the fixed scratch below: give the pointer
+  // checks valid stand-ins for them so that only the caller's fields count.
+  s.work = s.S_ckpt;
+  s.sync = s.ring_len;
+  RS_TRY(check_state(dims, &s));
+  RS_TRY(check_ptr(A));
+  RS_TRY(check_ptr(D));
+  RS_TRY(check_mamba2_token(x, B, C, dt));
+  RS_TRY(check_ptr(y));
+  const NoallocLayout lay(*dims);
+  if (lay.total > (long long)REPLAYSSM_NOALLOC_SCRATCH_BYTES) return REPLAYSSM_ERR_SCRATCH_LIMIT;
+  if (dims->batch == 0) return REPLAYSSM_OK;
+  unsigned char* base = nullptr;
+  if (noalloc_scratch(&base) != cudaSuccess) return REPLAYSSM_ERR_CUDA;
+  s.work = reinterpret_cast<float*>(base);
+  s.sync = reinterpret_cast<int32_t*>(base + lay.sync_off);
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // The arrival counters must start at zero; the previous call's contents stay.
+  if (cudaMemsetAsync(s.sync, 0, (size_t)dims->batch * 4, st) != cudaSuccess)
+    return REPLAYSSM_ERR_CUDA;
+  return finish(rs::launch_mamba2_decode(*dims, s, A, D, x, B, C, dt, y, st));
+}
+
 REPLAYSSM_API const char* replayssm_status_string(replayssm_status status) {
   switch (status) {
     case REPLAYSSM_OK: return "ok";
@@ -302,6 +374,8 @@ REPLAYSSM_API const char* replayssm_status_string(replayssm_status status) {
     case REPLAYSSM_ERR_UNSUPPORTED: return "unsupported sizes";
     case REPLAYSSM_ERR_MISALIGNED: return "tensor pointer not 16-byte aligned";
     case REPLAYSSM_ERR_CUDA: return "CUDA launch error";
+    case REPLAYSSM_ERR_SCRATCH_LIMIT:
+      return "sizes need more than the 16 MiB fixed scratch of replayssm_mamba2_decode_noalloc";
     default: return "unknown status";
   }
 }

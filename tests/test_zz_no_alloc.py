@@ -1,0 +1,127 @@
+"""The allocation-free Mamba-2 decode entry point against the ordinary one.
+
+Some callers cannot allocate device memory when they decode: a plugin whose
+host framework owns all device memory and allows no allocation while it
+executes, or a serving loop that reserved the whole device for its state pool
+up front. replayssm_mamba2_decode_noalloc serves them: it computes what
+replayssm_mamba2_decode computes but takes its scratch (the per-head workspace
+and the per-sequence arrival counters) from one fixed 16 MiB array inside the
+library, so state.work and state.sync may be NULL.
+
+The GPU test calls it through the C ABI twice in a row (the second call finds
+the array as the first left it) and checks each output, ring and pointer
+against replayssm_mamba2_decode on an identical state, with the tolerance of
+the other parity tests. The file's name makes pytest collect it last.
+"""
+
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import synth
+from gpu_harness import f32_close, host
+from recurrent_state_fp32_b300 import _abi, api
+
+FAKE = 0x10000  # 16-byte aligned, never dereferenced
+
+
+def _state(**over):
+    f = {name: FAKE for name, _ in _abi.State._fields_}
+    f.update(over)
+    return _abi.State(**f)
+
+
+def _noalloc(d, s, A=FAKE, y=FAKE):
+    r = ctypes.byref
+    return _abi.lib.replayssm_mamba2_decode_noalloc(
+        r(d) if d is not None else None, r(s) if s is not None else None,
+        A, FAKE, FAKE, FAKE, FAKE, FAKE, y, None)
+
+
+def test_arguments_and_the_size_limit():
+    """Argument errors and the scratch limit are reported before any CUDA call."""
+    no_scratch = dict(work=None, sync=None)
+    big = _abi.Dims(_abi.MAMBA2, 4096, 128, 1, 128, 256, 16, _abi.BF16)
+    assert _noalloc(big, _state(**no_scratch)) == _abi.ERR_SCRATCH_LIMIT
+    assert b"16 MiB" in _abi.lib.replayssm_status_string(_abi.ERR_SCRATCH_LIMIT)
+    # 64 heads more than 16 MiB holds at P = 64 (68 floats a workspace row)
+    rows = (_abi.NOALLOC_SCRATCH_BYTES - 4096) // (68 * 4)
+    over = _abi.Dims(_abi.MAMBA2, 1, rows + 64, 1, 128, 64, 16, _abi.BF16)
+    assert _noalloc(over, _state(**no_scratch)) == _abi.ERR_SCRATCH_LIMIT
+    empty = _abi.Dims(_abi.MAMBA2, 0, 8, 1, 128, 64, 16, _abi.BF16)
+    assert _noalloc(empty, _state(**no_scratch)) == _abi.OK
+    assert _noalloc(None, _state()) == _abi.ERR_INVALID_ARG
+    assert _noalloc(empty, None) == _abi.ERR_INVALID_ARG
+    gdn = _abi.Dims(_abi.GDN, 0, 8, 1, 128, 64, 16, _abi.BF16)
+    assert _noalloc(gdn, _state()) == _abi.ERR_INVALID_ARG
+    assert _noalloc(empty, _state(ring_len=None)) == _abi.ERR_INVALID_ARG
+    assert _noalloc(empty, _state(S_read=FAKE + 8)) == _abi.ERR_MISALIGNED
+    assert _noalloc(empty, _state(), A=None) == _abi.ERR_INVALID_ARG
+
+
+CASES = {
+    # ragged: P = 96, N = 64, 2 B/C groups, W = 5, FP32 inputs, FP32 read
+    "ragged": dict(batch=5, heads=6, P=96, N=64, groups=2, window=5, in_dtype="f32",
+                   read=False),
+    # 64 sequences of the 128-head, P = 64, N = 128, W = 16 layer, BF16 read copy
+    "layer": dict(batch=64, heads=128, P=64, N=128, groups=1, window=16, in_dtype="bf16",
+                  read=True),
+}
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("case", sorted(CASES))
+def test_matches_the_allocating_entry_point(case):
+    c = CASES[case]
+    b, H, P, N, G, W = (c[k] for k in ("batch", "heads", "P", "N", "groups", "window"))
+    seed = 11
+    dims = api.LayerDims("mamba2", b, H, dk=N, dv=P, window=W, groups=G, in_dtype=c["in_dtype"])
+    vt = torch.float32 if c["in_dtype"] == "f32" else torch.bfloat16
+    A, D, bias = synth.mamba2_params(seed, H)
+    A, D = torch.from_numpy(A).cuda(), torch.from_numpy(D).cuda()
+    S0 = torch.from_numpy(synth.mamba2_initial_state(seed, b, H, P, N)).cuda()
+    ref = api.LayerState(dims, read_copy=c["read"])
+    new = api.LayerState(dims, read_copy=c["read"])
+    for st in (ref, new):
+        st.set_checkpoint(S0)
+
+    def token(t):
+        tok = synth.mamba2_step_inputs(seed, t, b, H, G, P, N, bias, c["in_dtype"])
+        return {k: torch.from_numpy(np.ascontiguousarray(tok[k])).cuda().to(
+            torch.float32 if k == "dt" else vt) for k in ("x", "B", "C", "dt")}
+
+    def args(tok, y):
+        return [tok["x"].data_ptr(), tok["B"].data_ptr(), tok["C"].data_ptr(),
+                tok["dt"].data_ptr(), y.data_ptr()]
+
+    # a few buffered tokens first, so that the replay sums are not trivial
+    for t in range(W - 2):
+        tok = token(t)
+        y = torch.empty((b, H, P), device="cuda")
+        for st in (ref, new):
+            api.mamba2_decode(dims, st, A, D, tok["x"], tok["B"], tok["C"], tok["dt"], y)
+
+    # the caller's scratch is withheld from the allocation-free call
+    c_new = _abi.State.from_buffer_copy(new.c())
+    c_new.work = None
+    c_new.sync = None
+    for t in (W - 2, W - 1):  # two calls in a row
+        tok = token(t)
+        y_ref = torch.full((b, H, P), float("nan"), device="cuda")
+        y_new = torch.full((b, H, P), float("nan"), device="cuda")
+        _abi.check("replayssm_mamba2_decode", _abi.lib.replayssm_mamba2_decode(
+            ctypes.byref(dims.c()), ctypes.byref(ref.c()), A.data_ptr(), D.data_ptr(),
+            *args(tok, y_ref), None))
+        _abi.check("replayssm_mamba2_decode_noalloc", _abi.lib.replayssm_mamba2_decode_noalloc(
+            ctypes.byref(dims.c()), ctypes.byref(c_new), A.data_ptr(), D.data_ptr(),
+            *args(tok, y_new), None))
+        torch.cuda.synchronize()
+        f32_close(host(y_new), host(y_ref), f"{case} token {t}: y")
+        for name in ("ring_len", "ring_head", "status"):
+            assert torch.equal(getattr(new, name), getattr(ref, name)), f"{case} token {t}: {name}"
+        for k, v in ref.ring.items():
+            assert torch.equal(new.ring[k], v), f"{case} token {t}: ring {k}"
+        assert int(ref.status.abs().sum()) == 0
+        assert (host(ref.ring_len) == t + 1).all()
