@@ -164,15 +164,6 @@ replayssm_status check_smem(size_t bytes) {
   return bytes <= (size_t)rs::device_info().smem_optin ? REPLAYSSM_OK : REPLAYSSM_ERR_UNSUPPORTED;
 }
 
-size_t delta_replay_smem(const replayssm_dims* d, int K, bool read16) {
-  const size_t ts = read16 ? 2 : 4;
-  const size_t kda = d->kind == REPLAYSSM_KDA;
-  // one full-head tile (the worst case over row blocks) plus the staged entries
-  return (size_t)d->dv * d->dk * ts + 16 + 4 * ((size_t)d->window * d->dk * (1 + kda) +
-         (size_t)d->window * (2 - kda) + (size_t)d->window * d->dv + (size_t)K * d->dk +
-         (size_t)K * d->window + (size_t)K * d->dv);
-}
-
 }  // namespace
 
 // ------------------------------------------------ fixed scratch (no allocation)
@@ -244,7 +235,7 @@ REPLAYSSM_API replayssm_status replayssm_gdn_decode(
   RS_TRY(check_delta_token(q, k, v, alpha, beta));
   RS_TRY(check_ptr(o));
   if (dims->batch == 0) return REPLAYSSM_OK;
-  RS_TRY(check_smem(delta_replay_smem(dims, 1, state->S_read != nullptr)));
+  RS_TRY(check_smem(rs::delta_fused_smem(*dims, 1, state->S_read != nullptr)));
   return finish(rs::launch_delta_decode(*dims, *state, q, k, v, alpha, beta, scale, o,
                                         static_cast<cudaStream_t>(stream)));
 }
@@ -276,7 +267,7 @@ REPLAYSSM_API replayssm_status replayssm_spec_verify(
   RS_TRY(check_delta_token(q, k, v, alpha, beta));
   RS_TRY(check_ptr(o));
   if (dims->batch == 0) return REPLAYSSM_OK;
-  RS_TRY(check_smem(delta_replay_smem(dims, K, state->S_read != nullptr)));
+  RS_TRY(check_smem(rs::delta_fused_smem(*dims, K, state->S_read != nullptr)));
   return finish(rs::launch_delta_verify(*dims, *state, K, q, k, v, alpha, beta, scale, o,
                                         static_cast<cudaStream_t>(stream)));
 }

@@ -207,6 +207,38 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
+// E consecutive elements of T at p (aligned to E elements) as float, in one
+// vector load when E * sizeof(T) is 4, 8 or 16 bytes.
+template <typename T, int E>
+__device__ __forceinline__ void load_vec(const T* p, float (&out)[E]) {
+  constexpr int bytes = E * (int)sizeof(T);
+  if constexpr (bytes == 16) {
+    unpack<T>(*reinterpret_cast<const uint4*>(p), out);
+  } else if constexpr (bytes == 8) {
+    const uint2 r = *reinterpret_cast<const uint2*>(p);
+    if constexpr (sizeof(T) == 2) {
+      out[0] = bf16_lo(r.x);
+      out[1] = bf16_hi(r.x);
+      out[2] = bf16_lo(r.y);
+      out[3] = bf16_hi(r.y);
+    } else {
+      out[0] = __uint_as_float(r.x);
+      out[1] = __uint_as_float(r.y);
+    }
+  } else {
+#pragma unroll
+    for (int e = 0; e < E; ++e) out[e] = to_f(p[e]);
+  }
+}
+
+// Copies `bytes` (a multiple of 16, both addresses 16-byte aligned) with the
+// 32 lanes of one warp.
+__device__ __forceinline__ void block_copy_warp(void* dst, const void* src, int bytes, int lane) {
+  uint4* d = reinterpret_cast<uint4*>(dst);
+  const uint4* s = reinterpret_cast<const uint4*>(src);
+  for (int i = lane; i < bytes / 16; i += 32) d[i] = s[i];
+}
+
 // Copies `bytes` (a multiple of 16) between 16-byte aligned buffers with
 // every thread of the block taking strided 16-byte chunks.
 __device__ __forceinline__ void block_copy16(void* dst, const void* src, int bytes) {

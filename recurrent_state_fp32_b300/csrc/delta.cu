@@ -12,8 +12,10 @@
 //   u <- scale q; for j = n..1: s = k_j.u; o += beta_j s v_j; u <- A_j u;
 //   o += S_c u.
 // Verify (same page, paragraph 3) runs that sweep once per draft and reads
-// S_c once for all drafts. The fold applies the n updates row by row in FP32
-// registers: s <- alpha (.) s; s <- s + beta (v_r - s.k) k.
+// S_c once for all drafts. Decode and verify are one persistent kernel whose
+// prep warps run the sweeps while its producer and consumer warps stream S_c
+// and write o = S_c u + buffer terms for every query. The fold applies the n updates
+// row by row in FP32 registers: s <- alpha (.) s; s <- s + beta (v_r - s.k) k.
 #include <algorithm>
 
 #include "common.cuh"
@@ -22,16 +24,25 @@
 namespace rs {
 namespace {
 
-struct DDecode {
-  int batch, H, DV, W, nrb, K;  // nrb: row blocks per head; K: drafts (verify)
-  const void* S;
+// ------------------------------------------------------ fused decode / verify
+
+constexpr int kFGroups = 4;    // consumer groups
+constexpr int kFWarps = 16;    // warps per block: consumers, the producer, prep warps
+constexpr int kFQ = 4;         // queries swept together (verify); decode sweeps one
+constexpr int kFMaxSlots = 16; // per-head vector slots between prep and consumers
+
+struct DFused {
+  int batch, H, DV, W, K, commit;  // K queries per head; commit: decode (len += 1)
+  int RB, nrb, NS, GU;             // rows per unit, units per head, stages, warps per group
+  int NP, depth, NSL;              // prep warps, heads in flight per prep warp, vector slots
+  const void* S;                   // state rows [b, H, DV, DK] (read copy or checkpoint)
   const void* q;
   const void* k;
   const void* v;
   const float* alpha;
   const float* beta;
   float scale;
-  float* o;
+  float* o;                        // [b, K, H, DV]
   void* ring_q;
   void* ring_k;
   void* ring_v;
@@ -43,199 +54,529 @@ struct DDecode {
   int32_t* sync;
 };
 
-// Shared-memory carve-up for decode (K = 1) and verify (K drafts).
-struct DSmem {
-  size_t tile, bar, kbuf, abuf, bbuf, vbuf, ubuf, coef, obuf, total;
-  __host__ __device__ DSmem(int RB, int DK, int W, int K, bool kda, int ts_bytes) {
-    tile = 0;
-    bar = (size_t)RB * DK * ts_bytes;
-    kbuf = bar + 16;
-    abuf = kbuf + 4 * (size_t)W * DK;
-    bbuf = abuf + 4 * (size_t)W * (kda ? DK : 1);
-    vbuf = bbuf + 4 * (size_t)W;
-    ubuf = vbuf + 4 * (size_t)W * RB;
-    coef = ubuf + 4 * (size_t)K * DK;
-    obuf = coef + 4 * (size_t)K * W;
-    total = obuf + 4 * (size_t)K * RB;
+// One head stage of a prep warp (byte offsets): a header (len, head, ok),
+// then the entries 0..n-1 in order (k rows, v rows, gates, beta) and the K
+// queries.
+struct DStage {
+  size_t kr, vr, ar, br, qr, bytes;
+  __host__ __device__ DStage(int DK, int DV, int W, int K, bool kda, int ti) {
+    kr = 16;                                                     // [W][DK] k_j (in_dtype)
+    vr = kr + align_up((size_t)W * DK * ti, 16);                 // [W][DV] v_j (in_dtype)
+    ar = vr + align_up((size_t)W * DV * ti, 16);                 // KDA [W][DK], GDN [W]
+    br = ar + align_up((size_t)W * (kda ? DK : 1) * 4, 16);      // [W] beta_j
+    qr = br + align_up((size_t)W * 4, 16);                       // [K][DK] q_i (in_dtype)
+    bytes = align_up(qr + (size_t)K * DK * ti, 128);
   }
 };
 
-// Entry j of a sequence: j < len is ring slot (head + j) mod W; later entries
-// come from the call's own inputs (the current token or draft j - len).
-template <int DK, typename TI, bool KDA>
-__device__ __forceinline__ void stage_entries(const DDecode& a, int seq, int h, int rb, int RB,
-                                              int len, int hd, int n, float* kbuf, float* abuf,
-                                              float* bbuf, float* vbuf) {
-  const int H = a.H, W = a.W, DV = a.DV;
-  const TI* rk = reinterpret_cast<const TI*>(a.ring_k);
-  const TI* rv = reinterpret_cast<const TI*>(a.ring_v);
-  const TI* ik = reinterpret_cast<const TI*>(a.k);
-  const TI* iv = reinterpret_cast<const TI*>(a.v);
-  // ring rows of (seq, h): vector fields [b, H, W, d], scalar fields [b, H, Wd];
-  // inputs [b, K, H, ...]
-  const int Wd = ring_wd(W);
-  auto ring_ix = [&](int j) { return ((size_t)seq * H + h) * W + (hd + j) % W; };
-  auto ring_sx = [&](int j) { return ((size_t)seq * H + h) * Wd + (hd + j) % W; };
-  auto in_ix = [&](int j) { return ((size_t)seq * a.K + (j - len)) * H + h; };
-  for (int idx = threadIdx.x; idx < n * DK; idx += kThreads) {
-    const int j = idx / DK, c = idx - j * DK;
-    kbuf[idx] = to_f(j < len ? rk[ring_ix(j) * DK + c] : ik[in_ix(j) * DK + c]);
-    if (KDA) abuf[idx] = j < len ? a.ring_alpha[ring_ix(j) * DK + c] : a.alpha[in_ix(j) * DK + c];
+// Shared memory of the fused block: NS state stages and their barriers, NSL
+// vector slots (u[K][DK], e[K][DV], ok) and their barriers, then NP prep
+// warps with `depth` head stages each.
+struct DFusedSmem {
+  size_t stage, bars, slot, slots, vbars, prep, prep_warp, total;
+  __host__ __device__ DFusedSmem(int RB, int DK, int DV, int W, int K, int NS, int NSL, int NP,
+                                 int depth, bool kda, int ts, int ti) {
+    stage = align_up((size_t)RB * DK * ts, 128);
+    bars = (size_t)NS * stage;
+    slots = align_up(bars + 16 * (size_t)NS, 128);
+    slot = align_up((size_t)K * (DK + DV) * 4 + 16, 128);
+    vbars = slots + (size_t)NSL * slot;
+    prep = align_up(vbars + 16 * (size_t)NSL, 128);
+    prep_warp = (size_t)depth * DStage(DK, DV, W, K, kda, ti).bytes;
+    total = prep + (size_t)NP * prep_warp;
   }
-  for (int idx = threadIdx.x; idx < n * RB; idx += kThreads) {
-    const int j = idx / RB, r = idx - j * RB + rb * RB;
-    vbuf[idx] = to_f(j < len ? rv[ring_ix(j) * DV + r] : iv[in_ix(j) * DV + r]);
-  }
-  for (int j = threadIdx.x; j < n; j += kThreads) {
-    bbuf[j] = j < len ? a.ring_beta[ring_sx(j)] : a.beta[in_ix(j)];
-    if (!KDA) abuf[j] = j < len ? a.ring_alpha[ring_sx(j)] : a.alpha[in_ix(j)];
-  }
-}
+};
 
-// Writes input entry i (token or draft) of (seq, h) into ring slot `slot`.
-template <int DK, typename TI, bool KDA>
-__device__ __forceinline__ void append_entry(const DDecode& a, int seq, int h, int i, int slot) {
-  const int H = a.H, W = a.W, DV = a.DV;
-  const size_t in_ix = ((size_t)seq * a.K + i) * H + h;
-  const size_t ring_ix = ((size_t)seq * H + h) * W + slot;
-  const size_t ring_sx = ((size_t)seq * H + h) * ring_wd(W) + slot;
-  block_copy16(reinterpret_cast<TI*>(a.ring_k) + ring_ix * DK,
-               reinterpret_cast<const TI*>(a.k) + in_ix * DK, DK * (int)sizeof(TI));
-  block_copy16(reinterpret_cast<TI*>(a.ring_v) + ring_ix * DV,
-               reinterpret_cast<const TI*>(a.v) + in_ix * DV, DV * (int)sizeof(TI));
-  if (a.ring_q)
-    block_copy16(reinterpret_cast<TI*>(a.ring_q) + ring_ix * DK,
-                 reinterpret_cast<const TI*>(a.q) + in_ix * DK, DK * (int)sizeof(TI));
-  if (KDA) block_copy16(a.ring_alpha + ring_ix * DK, a.alpha + in_ix * DK, DK * 4);
-  if (threadIdx.x == 0) {
-    a.ring_beta[ring_sx] = a.beta[in_ix];
-    if (!KDA) a.ring_alpha[ring_sx] = a.alpha[in_ix];
-  }
-}
-
-// Backward sweep for one query by one warp over entries last..0; leaves u in
-// ubuf and beta_j (k_j . u) in coef[j]. Lane l owns u[l*EPL .. l*EPL+EPL).
-template <int DK, bool KDA>
-__device__ __forceinline__ void sweep(const float* qv, int last, const float* kbuf,
-                                      const float* abuf, const float* bbuf, float* ubuf,
-                                      float* coef, int lane) {
-  constexpr int EPL = DK / 32;
-  float u[EPL];
-#pragma unroll
-  for (int e = 0; e < EPL; ++e) u[e] = qv[lane * EPL + e];
-  for (int j = last; j >= 0; --j) {
-    const float* kj = kbuf + j * DK + lane * EPL;
-    float kk[EPL];
-    float s = 0.f;
-#pragma unroll
-    for (int e = 0; e < EPL; ++e) {
-      kk[e] = kj[e];
-      s = fmaf(kk[e], u[e], s);
-    }
-    s = warp_sum(s);
-    const float bs = bbuf[j] * s;
-    if (lane == 0) coef[j] = bs;
-#pragma unroll
-    for (int e = 0; e < EPL; ++e) {
-      const float g = KDA ? abuf[j * DK + lane * EPL + e] : abuf[j];
-      u[e] = (u[e] - bs * kk[e]) * g;
-    }
-  }
-#pragma unroll
-  for (int e = 0; e < EPL; ++e) ubuf[lane * EPL + e] = u[e];
-}
-
-// One block per (sequence, head, row block). K == 1 is the decode step
-// (appends and commits the token); K > 1 is the speculative verify (appends
-// K drafts, commits nothing, one output per draft).
-template <int DK, typename TS, typename TI, bool KDA, bool VERIFY>
-__global__ void __launch_bounds__(kThreads) delta_replay_kernel(const DDecode a) {
+// Replay decode (K = 1, commits the token) or speculative verify (K drafts,
+// commits nothing) of the delta-rule layers in one persistent kernel; one
+// block per SM owns a contiguous range of heads (flat index seq * H + h),
+// split in units of RB state rows.
+//
+// Prep warps (NP) take the block's heads round robin. For a head they stage
+// its entries with async copies (`depth` heads ahead): entry j < len is ring
+// slot (head + j) mod W, entry len + i is the call's input i. For query i
+// (entry len + i; drafts 0..i visible) the backward sweep over entries
+// len+i..0 is
+//   u <- scale q_i; for j: s = k_j . u; c = beta_j s; e_i += c v_j;
+//   u <- alpha_j (.) (u - c k_j)
+// (queries swept together share each entry's loads). u and e go to the
+// head's vector slot. The warp appends the call's entries to slots
+// (head + len + i) mod W and, for a decode, arrives once per sequence on its
+// arrival counter (the last arrival bumps len). A sequence without room for K
+// entries (or with pointers out of range) gets a status bit and no output.
+//
+// The producer warp streams the state rows unit by unit with bulk copies into
+// NS stages while consumer groups of GU warps take units round robin and
+// write o_i[r] = S[r, :] . u_i + e_i[r] from the slot. The state is read once
+// for all queries. Every wait is bounded; a timeout sets
+// REPLAYSSM_SEQ_TIMEOUT and ends the block.
+template <int DK, typename TS, typename TI, bool KDA, int KMAX>
+__global__ void __launch_bounds__(32 * kFWarps, 1) delta_fused_kernel(const DFused a) {
   extern __shared__ __align__(128) unsigned char smem[];
   using RD = RowDot<DK, TS>;
+  constexpr int kE = RD::kEpc;
+  constexpr int KQ = KMAX == 1 ? 1 : kFQ;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int H = a.H, DV = a.DV, W = a.W, K = a.K;
-  const int RB = DV / a.nrb;
-  const int per_seq = H * a.nrb;
-  const int seq = blockIdx.x / per_seq;
-  const int rem = blockIdx.x - seq * per_seq;
-  const int h = rem / a.nrb, rb = rem - h * a.nrb;
-  const int len = a.len[seq];
-  const int hd = a.head[seq];
-  if (!pointers_ok(hd, len, W) || len + K > W) {
-    if (rem == 0 && tid == 0)
-      atomicOr(a.status + seq, pointers_ok(hd, len, W) ? REPLAYSSM_SEQ_RING_FULL
-                                                       : REPLAYSSM_SEQ_BAD_POINTER);
-    return;
-  }
-  const DSmem L(RB, DK, W, K, KDA, sizeof(TS));
-  TS* tile = reinterpret_cast<TS*>(smem + L.tile);
-  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + L.bar);
-  float* kbuf = reinterpret_cast<float*>(smem + L.kbuf);
-  float* abuf = reinterpret_cast<float*>(smem + L.abuf);
-  float* bbuf = reinterpret_cast<float*>(smem + L.bbuf);
-  float* vbuf = reinterpret_cast<float*>(smem + L.vbuf);
-  float* ubuf = reinterpret_cast<float*>(smem + L.ubuf);
-  float* coef = reinterpret_cast<float*>(smem + L.coef);
-  float* obuf = reinterpret_cast<float*>(smem + L.obuf);
+  const int GU = a.GU, CW = kFGroups * GU, NG = kFGroups, NS = a.NS, NSL = a.NSL;
+  const int H = a.H, DV = a.DV, RB = a.RB, nrb = a.nrb, K = a.K, W = a.W;
+  const DFusedSmem L(RB, DK, DV, W, K, NS, NSL, a.NP, a.depth, KDA, sizeof(TS), sizeof(TI));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bars);
+  uint64_t* empty = full + NS;
+  uint64_t* vfull = reinterpret_cast<uint64_t*>(smem + L.vbars);
+  uint64_t* vempty = vfull + NSL;
+  __shared__ int abort_smem;
+  volatile int& abort_flag = abort_smem;
+  const long long heads = (long long)a.batch * H;
+  const int hb0 = (int)(heads * blockIdx.x / gridDim.x);
+  const int hb1 = (int)(heads * (blockIdx.x + 1) / gridDim.x);
+  const int nh = hb1 - hb0, nu = nh * nrb;
+  const uint32_t tile_bytes = (uint32_t)((size_t)RB * DK * sizeof(TS));
+  // slot layout (floats): u [K][DK], e [K][DV], then the ok flag
+  auto slot_ptr = [&](int li) {
+    return reinterpret_cast<float*>(smem + L.slots + (size_t)(li % NSL) * L.slot);
+  };
+  const int ok_off = K * (DK + DV);
 
   if (tid == 0) {
-    mbar_init(bar, 1);
-    fence_mbar_init();
-  }
-  __syncthreads();
-  if (tid == 0) {
-    const uint32_t bytes = (uint32_t)((size_t)RB * DK * sizeof(TS));
-    const TS* src = reinterpret_cast<const TS*>(a.S) + (((size_t)seq * H + h) * DV + (size_t)rb * RB) * DK;
-    mbar_arrive_expect_tx(bar, bytes);
-    bulk_g2s(tile, src, bytes, bar, l2_evict_first_policy());
-  }
-  if (rb == 0)
-    for (int i = 0; i < K; ++i) append_entry<DK, TI, KDA>(a, seq, h, i, (hd + len + i) % W);
-  const int n = len + K;
-  stage_entries<DK, TI, KDA>(a, seq, h, rb, RB, len, hd, n, kbuf, abuf, bbuf, vbuf);
-  __syncthreads();
-
-  // One backward sweep per query (warp i handles drafts i, i+4, ...).
-  const TI* qin = reinterpret_cast<const TI*>(a.q);
-  for (int i = warp; i < K; i += kWarps) {
-    float* qs = ubuf + i * DK;  // staged scaled query, overwritten by u
-    for (int c = lane; c < DK; c += 32)
-      qs[c] = a.scale * to_f(qin[(((size_t)seq * K + i) * H + h) * DK + c]);
-    __syncwarp();
-    sweep<DK, KDA>(qs, len + i, kbuf, abuf, bbuf, qs, coef + i * W, lane);
-  }
-  __syncthreads();
-  // Buffer terms: obuf[i][r] = sum_{j <= len+i} beta_j s_j v_j[r].
-  for (int idx = tid; idx < K * RB; idx += kThreads) {
-    const int i = idx / RB, r = idx - i * RB;
-    float s = 0.f;
-    for (int j = 0; j <= len + i; ++j) s = fmaf(coef[i * W + j], vbuf[j * RB + r], s);
-    obuf[idx] = s;
-  }
-  __syncthreads();
-
-  // S_c u for every query from the one staged tile.
-  const int passes = RB / 32;
-  bool ok = true;
-  for (int task = warp; task < K * passes; task += kWarps) {
-    const int i = task / passes, row0 = (task - i * passes) * 32;
-    if (!mbar_wait(bar, 0)) {
-      ok = false;
-      break;
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], GU);
     }
-    float vec[RD::kEpc];
-    const float* uv = ubuf + i * DK + RD::chunk_of(lane) * RD::kEpc;
-#pragma unroll
-    for (int e = 0; e < RD::kEpc; ++e) vec[e] = uv[e];
-    const float dot = RD::rows32(tile, row0, vec, lane);
-    const int r = row0 + RD::row_of(lane);
-    a.o[(((size_t)seq * K + i) * H + h) * DV + (size_t)rb * RB + r] = dot + obuf[i * RB + r];
+    for (int s = 0; s < NSL; ++s) {
+      mbar_init(&vfull[s], 32);
+      mbar_init(&vempty[s], nrb * GU);
+    }
+    fence_mbar_init();
+    abort_flag = 0;
   }
-  if (!ok) atomicOr(a.status + seq, REPLAYSSM_SEQ_TIMEOUT);
   __syncthreads();
-  if (tid == 0) {
-    mbar_wait(bar, 0);  // no copy may land after exit
-    if (!VERIFY) arrive_and_finish(a.sync + seq, 1, per_seq, [&] { a.len[seq] = len + 1; });
+
+  if (warp == CW) {
+    // ------------------------------------------------------------ producer
+    const uint64_t pol = l2_evict_first_policy();
+    const TS* Sg = reinterpret_cast<const TS*>(a.S);
+    int ps = 0;
+    uint32_t pk = 0;
+    bool pwrap = false;
+    int li = 0, rb = 0;
+    for (int ul = 0; ul < nu; ++ul) {
+      const int s = ps;
+      if (pwrap && !mbar_wait_warp(&empty[s], pk)) {
+        if (lane == 0) abort_flag = 1;
+        break;
+      }
+      if (++ps == NS) {
+        ps = 0;
+        if (pwrap) pk ^= 1;
+        pwrap = true;
+      }
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&full[s], tile_bytes);
+        bulk_g2s(smem + (size_t)s * L.stage,
+                 Sg + ((size_t)(hb0 + li) * DV + (size_t)rb * RB) * DK, tile_bytes, &full[s], pol);
+      }
+      if (++rb == nrb) {
+        rb = 0;
+        ++li;
+      }
+    }
+  } else if (warp < CW) {
+    // ------------------------------------------------------------ consumers
+    const int gi = warp / GU, part = warp - gi * GU;
+    const int RBp = RB / GU;
+    const int ngr = RBp / 32;
+    auto group_any = [&](bool p) -> bool {
+      if (GU == 1) return p;
+      uint32_t res;
+      asm volatile(
+          "{\n .reg .pred pi, po;\n setp.ne.u32 pi, %1, 0;\n"
+          " bar.red.or.pred po, %2, %3, pi;\n selp.u32 %0, 1, 0, po;\n}"
+          : "=r"(res)
+          : "r"((uint32_t)p), "r"(1 + gi), "r"(32 * GU)
+          : "memory");
+      return res != 0;
+    };
+    const int c0 = RD::chunk_of(lane) * kE;
+    int s = gi;
+    uint32_t ph = 0;
+    for (int ul = gi; ul < nu; ul += NG) {
+      const int li = ul / nrb, rb = ul - li * nrb;
+      const int hg = hb0 + li, seq = hg / H, h = hg - seq * H;
+      const int row0 = rb * RB + part * RBp;
+      const bool aborted0 = __shfl_sync(kFull, abort_flag, 0) != 0;
+      const bool vready = !aborted0 && mbar_wait_warp(&vfull[li % NSL], (li / NSL) & 1);
+      if (!aborted0 && !vready && lane == 0) {
+        abort_flag = 1;
+        atomicOr(a.status + seq, REPLAYSSM_SEQ_TIMEOUT);
+      }
+      if (group_any(!vready)) break;
+      const float* sl = slot_ptr(li);
+      const bool write = reinterpret_cast<const int*>(sl)[ok_off] != 0;
+      float vec[KMAX][kE];
+      float extra[4];
+#pragma unroll
+      for (int kq = 0; kq < KMAX; ++kq) {
+        if (kq >= K) break;
+#pragma unroll
+        for (int e = 0; e < kE; e += 4) {
+          const float4 v4 = *reinterpret_cast<const float4*>(sl + kq * DK + c0 + e);
+          vec[kq][e] = v4.x;
+          vec[kq][e + 1] = v4.y;
+          vec[kq][e + 2] = v4.z;
+          vec[kq][e + 3] = v4.w;
+        }
+      }
+      if constexpr (KMAX == 1) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          if (q < ngr) extra[q] = sl[K * DK + row0 + 32 * q + RD::row_of(lane)];
+      }
+      const bool aborted = __shfl_sync(kFull, abort_flag, 0) != 0;
+      const bool landed = !aborted && mbar_wait_warp(&full[s], ph);
+      if (!aborted && !landed && lane == 0) {
+        abort_flag = 1;
+        atomicOr(a.status + seq, REPLAYSSM_SEQ_TIMEOUT);
+      }
+      if (group_any(!landed)) break;
+      const TS* tile = reinterpret_cast<const TS*>(smem + (size_t)s * L.stage) + (size_t)part * RBp * DK;
+      float* yrow = a.o + ((size_t)seq * K * H + h) * DV + row0;
+      if constexpr (KMAX > 1) {
+        constexpr int KC = KMAX < 64 / RD::kLpr ? KMAX : 64 / RD::kLpr;
+#pragma unroll 1
+        for (int q = 0; q < ngr; ++q) {
+          const int r = 32 * q + RD::row_of(lane);
+#pragma unroll 1
+          for (int k0 = 0; k0 < KMAX; k0 += KC) {
+            if (k0 >= K) break;
+            float ex[KC];
+#pragma unroll
+            for (int c = 0; c < KC; ++c) ex[c] = k0 + c < K ? sl[K * DK + (k0 + c) * DV + row0 + r] : 0.f;
+            float acc[KC][RD::kLpr];
+            const TS* base = tile + (size_t)(32 * q + lane / RD::kLpr) * DK + c0;
+#pragma unroll
+            for (int kk = 0; kk < RD::kLpr; ++kk) {
+              const uint4 raw = *reinterpret_cast<const uint4*>(base + (size_t)kk * RD::kRpi * DK);
+              float f[kE];
+              unpack<TS>(raw, f);
+#pragma unroll
+              for (int c = 0; c < KC; ++c) {
+                float sacc = 0.f;
+#pragma unroll
+                for (int e = 0; e < kE; ++e) sacc = fmaf(f[e], vec[k0 + c][e], sacc);
+                acc[c][kk] = sacc;
+              }
+            }
+#pragma unroll
+            for (int c = 0; c < KC; ++c) {
+              if (k0 + c >= K) break;
+              const float d = reduce_scatter<RD::kLpr>(acc[c], lane);
+              if (write) yrow[(size_t)(k0 + c) * H * DV + r] = d + ex[c];
+            }
+          }
+        }
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&empty[s]);
+          mbar_arrive(&vempty[li % NSL]);
+        }
+      } else {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          if (q >= ngr) break;
+          const float d = RD::rows32(tile, 32 * q, vec[0], lane);
+          if (write) yrow[32 * q + RD::row_of(lane)] = d + extra[q];
+        }
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&empty[s]);
+          mbar_arrive(&vempty[li % NSL]);
+        }
+      }
+      s += NG;
+      if (s >= NS) {
+        s -= NS;
+        ph ^= 1;
+      }
+    }
+  } else if (warp - CW - 1 < a.NP) {
+    // ------------------------------------------------------------ prep
+    constexpr int EPL = DK / 32;
+    constexpr int ti = (int)sizeof(TI);
+    constexpr int kKC = DK * ti / 16;  // 16-byte chunks of a k row (<= 32)
+    constexpr int kKR = 32 / kKC;
+    constexpr int kAC = DK * 4 / 16;   // chunks of a KDA gate row
+    constexpr int kAR = 32 / kAC;
+    const int NP = a.NP, depth = a.depth;
+    const int pw = warp - CW - 1;
+    const int Wd = ring_wd(W);
+    const DStage SL(DK, DV, W, K, KDA, ti);
+    unsigned char* wbase = smem + L.prep + (size_t)pw * L.prep_warp;
+    const size_t krow = (size_t)DK * ti, arow = (size_t)DK * 4, vrow = (size_t)DV * ti;
+    const int vcpr = (int)(vrow / 16);  // 16-byte chunks of a v row
+    const bool vmap = vcpr <= 32 && 32 % vcpr == 0;
+    const int vro = vmap ? lane / vcpr : 0, vch = vmap ? lane - vro * vcpr : 0;
+    const int vstep = vmap ? 32 / vcpr : 0;
+    const int EVL = DV / 32;            // e rows per lane: r = lane + 32 m
+    const int nmine = nh > pw ? (nh - pw + NP - 1) / NP : 0;  // heads of this warp
+
+    // ---- issue side: stage the entries of this warp's head i_t
+    int i_t = 0, i_loaded = -1, i_len = 0, i_hd = 0;
+    bool i_ok = false;
+    int i_v = hb0 + pw, i_seq = i_v / H, i_h = i_v - (i_v / H) * H;
+    auto issue = [&]() {
+      if (i_seq != i_loaded) {
+        int l = 0, hh = 0;
+        if (lane == 0) {
+          l = a.len[i_seq];
+          hh = a.head[i_seq];
+        }
+        i_len = __shfl_sync(kFull, l, 0);
+        i_hd = __shfl_sync(kFull, hh, 0);
+        i_ok = pointers_ok(i_hd, i_len, W) && i_len + K <= W;
+        i_loaded = i_seq;
+      }
+      unsigned char* st = wbase + (size_t)(i_t % depth) * SL.bytes;
+      if (lane == 0) {
+        int* hdr = reinterpret_cast<int*>(st);
+        hdr[0] = i_len;
+        hdr[1] = i_hd;
+        hdr[2] = i_ok ? 1 : 0;
+        hdr[3] = i_seq;
+      }
+      if (i_ok) {
+        const int n = i_len + K, v = i_v;
+        const size_t in0 = (size_t)i_seq * K * H + i_h;  // input row of draft 0 ([b, K, H])
+        const size_t instep = (size_t)H;                 // rows between drafts
+        {
+          const unsigned char* rkh = reinterpret_cast<const unsigned char*>(a.ring_k) + (size_t)v * W * krow;
+          const unsigned char* ikh = reinterpret_cast<const unsigned char*>(a.k) + in0 * krow;
+          const int c = (lane % kKC) * 16;
+          for (int j = lane / kKC; j < n; j += kKR) {
+            const int slot = i_hd + j < W ? i_hd + j : i_hd + j - W;
+            const unsigned char* src = j < i_len ? rkh + slot * krow : ikh + (size_t)(j - i_len) * instep * krow;
+            cp_async16(st + SL.kr + j * krow + c, src + c);
+          }
+          const unsigned char* iqh = reinterpret_cast<const unsigned char*>(a.q) + in0 * krow;
+          for (int i = lane / kKC; i < K; i += kKR)
+            cp_async16(st + SL.qr + i * krow + c, iqh + (size_t)i * instep * krow + c);
+        }
+        {
+          const unsigned char* rvh = reinterpret_cast<const unsigned char*>(a.ring_v) + (size_t)v * W * vrow;
+          const unsigned char* ivh = reinterpret_cast<const unsigned char*>(a.v) + in0 * vrow;
+          if (vmap) {
+            for (int j = vro; j < n; j += vstep) {
+              const int slot = i_hd + j < W ? i_hd + j : i_hd + j - W;
+              const unsigned char* src = j < i_len ? rvh + slot * vrow : ivh + (size_t)(j - i_len) * instep * vrow;
+              cp_async16(st + SL.vr + j * vrow + vch * 16, src + vch * 16);
+            }
+          } else {
+            for (int idx = lane; idx < n * vcpr; idx += 32) {
+              const int j = idx / vcpr, c = idx - j * vcpr;
+              const int slot = i_hd + j < W ? i_hd + j : i_hd + j - W;
+              const unsigned char* src = j < i_len ? rvh + slot * vrow : ivh + (size_t)(j - i_len) * instep * vrow;
+              cp_async16(st + SL.vr + j * vrow + c * 16, src + c * 16);
+            }
+          }
+        }
+        if (KDA) {
+          const unsigned char* rah = reinterpret_cast<const unsigned char*>(a.ring_alpha) + (size_t)v * W * arow;
+          const unsigned char* iah = reinterpret_cast<const unsigned char*>(a.alpha) + in0 * arow;
+          const int c = (lane % kAC) * 16;
+          for (int j = lane / kAC; j < n; j += kAR) {
+            const int slot = i_hd + j < W ? i_hd + j : i_hd + j - W;
+            const unsigned char* src = j < i_len ? rah + slot * arow : iah + (size_t)(j - i_len) * instep * arow;
+            cp_async16(st + SL.ar + j * arow + c, src + c);
+          }
+        }
+        if (lane < n) {
+          const int j = lane;
+          const int slot = i_hd + j < W ? i_hd + j : i_hd + j - W;
+          const size_t rs_ = (size_t)v * Wd + slot, is_ = in0 + (size_t)(j - i_len) * instep;
+          cp_async4(st + SL.br + 4 * j, j < i_len ? a.ring_beta + rs_ : a.beta + is_);
+          if (!KDA) cp_async4(st + SL.ar + 4 * j, j < i_len ? a.ring_alpha + rs_ : a.alpha + is_);
+        }
+        if (lane + 32 < n) {  // windows above 32 entries
+          const int j = lane + 32;
+          const int slot = i_hd + j < W ? i_hd + j : i_hd + j - W;
+          const size_t rs_ = (size_t)v * Wd + slot, is_ = in0 + (size_t)(j - i_len) * instep;
+          cp_async4(st + SL.br + 4 * j, j < i_len ? a.ring_beta + rs_ : a.beta + is_);
+          if (!KDA) cp_async4(st + SL.ar + 4 * j, j < i_len ? a.ring_alpha + rs_ : a.alpha + is_);
+        }
+      }
+      cp_async_commit();  // one group per head (possibly empty)
+      ++i_t;
+      i_v += NP;
+      i_h += NP;
+      while (i_h >= H) {
+        i_h -= H;
+        ++i_seq;
+      }
+    };
+
+    // ---- compute side
+    int cur_seq = -1, len = 0, hd = 0, seq_count = 0;
+    bool ok = false;
+    int h = (hb0 + pw) % H;
+    while (i_t < depth - 1 && i_t < nmine) issue();
+    for (int t = 0; t < nmine; ++t) {
+      if (i_t < nmine) {
+        issue();
+        if (depth == 2)
+          cp_async_wait_group<1>();  // head t has landed
+        else
+          cp_async_wait_all();
+      } else {
+        cp_async_wait_all();
+      }
+      __syncwarp();
+      const int li = pw + t * NP, v = hb0 + li;
+      const unsigned char* st = wbase + (size_t)(t % depth) * SL.bytes;
+      const int* hdr = reinterpret_cast<const int*>(st);
+      const int seq = hdr[3];
+      if (seq != cur_seq) {
+        if (a.commit && cur_seq >= 0 && ok && lane == 0)
+          arrive_and_finish(a.sync + cur_seq, seq_count, H, [&] { a.len[cur_seq] = len + 1; });
+        len = hdr[0];
+        hd = hdr[1];
+        ok = hdr[2] != 0;
+        cur_seq = seq;
+        seq_count = 0;
+        if (h == 0 && lane == 0 && !ok)
+          atomicOr(a.status + seq, pointers_ok(hd, len, W) ? REPLAYSSM_SEQ_RING_FULL
+                                                           : REPLAYSSM_SEQ_BAD_POINTER);
+      }
+      ++seq_count;
+      // the slot must have been released by the consumers of head li - NSL
+      if (li >= NSL) {
+        const bool aborted = __shfl_sync(kFull, abort_flag, 0) != 0;
+        const bool freed = !aborted && mbar_wait_warp(&vempty[li % NSL], ((li / NSL) - 1) & 1);
+        if (!freed) {
+          if (!aborted && lane == 0) {
+            abort_flag = 1;
+            atomicOr(a.status + seq, REPLAYSSM_SEQ_TIMEOUT);
+          }
+          break;
+        }
+      }
+      float* sl = slot_ptr(li);
+      if (ok) {
+        const TI* kr = reinterpret_cast<const TI*>(st + SL.kr);
+        const float* ar = reinterpret_cast<const float*>(st + SL.ar);
+        const float* br = reinterpret_cast<const float*>(st + SL.br);
+        const TI* qr = reinterpret_cast<const TI*>(st + SL.qr);
+        const TI* vr = reinterpret_cast<const TI*>(st + SL.vr);
+        for (int i0 = 0; i0 < K; i0 += KQ) {
+          const int nq = min(KQ, K - i0);
+          float u[KQ][EPL], ev[KQ][8];
+#pragma unroll
+          for (int qi = 0; qi < KQ; ++qi) {
+            float qv[EPL];
+            load_vec<TI, EPL>(qr + (qi < nq ? i0 + qi : i0) * DK + lane * EPL, qv);
+#pragma unroll
+            for (int e = 0; e < EPL; ++e) u[qi][e] = qi < nq ? a.scale * qv[e] : 0.f;
+#pragma unroll
+            for (int m = 0; m < 8; ++m) ev[qi][m] = 0.f;
+          }
+          const int top = len + i0 + nq - 1;  // newest entry any query of the pass sees
+          // entry j's operands, loaded one step ahead
+          float kn[EPL], gn[EPL], bn, vn[8];
+          auto fetch = [&](int j) {
+            load_vec<TI, EPL>(kr + j * DK + lane * EPL, kn);
+            if (KDA) {
+              load_vec<float, EPL>(ar + j * DK + lane * EPL, gn);
+            } else {
+              const float g = ar[j];
+#pragma unroll
+              for (int e = 0; e < EPL; ++e) gn[e] = g;
+            }
+            bn = br[j];
+#pragma unroll
+            for (int m = 0; m < 8; ++m) vn[m] = m < EVL ? to_f(vr[j * DV + lane + 32 * m]) : 0.f;
+          };
+          fetch(top);
+          for (int j = top; j >= 0; --j) {
+            float kk[EPL], g[EPL], vv[8];
+#pragma unroll
+            for (int e = 0; e < EPL; ++e) {
+              kk[e] = kn[e];
+              g[e] = gn[e];
+            }
+#pragma unroll
+            for (int m = 0; m < 8; ++m) vv[m] = vn[m];
+            const float bj = bn;
+            if (j > 0) fetch(j - 1);
+            float sd[KQ];
+#pragma unroll
+            for (int qi = 0; qi < KQ; ++qi) {
+              sd[qi] = 0.f;
+#pragma unroll
+              for (int e = 0; e < EPL; ++e) sd[qi] = fmaf(kk[e], u[qi][e], sd[qi]);
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+#pragma unroll
+              for (int qi = 0; qi < KQ; ++qi) sd[qi] += __shfl_xor_sync(kFull, sd[qi], o);
+            }
+#pragma unroll
+            for (int qi = 0; qi < KQ; ++qi) {
+              if (qi < nq && j <= len + i0 + qi) {
+                const float c = bj * sd[qi];
+#pragma unroll
+                for (int e = 0; e < EPL; ++e) u[qi][e] = (u[qi][e] - c * kk[e]) * g[e];
+#pragma unroll
+                for (int m = 0; m < 8; ++m) ev[qi][m] = fmaf(c, vv[m], ev[qi][m]);
+              }
+            }
+          }
+#pragma unroll
+          for (int qi = 0; qi < KQ; ++qi) {
+            if (qi < nq) {
+#pragma unroll
+              for (int e = 0; e < EPL; ++e) sl[(i0 + qi) * DK + lane * EPL + e] = u[qi][e];
+#pragma unroll
+              for (int m = 0; m < 8; ++m)
+                if (m < EVL) sl[K * DK + (i0 + qi) * DV + lane + 32 * m] = ev[qi][m];
+            }
+          }
+        }
+        // append the call's entries: slot (head + len + i) mod W
+        for (int i = 0; i < K; ++i) {
+          const int j = len + i;
+          const int slot = hd + j < W ? hd + j : hd + j - W;
+          const size_t rr = (size_t)v * W + slot;
+          block_copy_warp(reinterpret_cast<unsigned char*>(a.ring_k) + rr * krow,
+                          st + SL.kr + j * krow, (int)krow, lane);
+          block_copy_warp(reinterpret_cast<unsigned char*>(a.ring_v) + rr * vrow,
+                          st + SL.vr + j * vrow, (int)vrow, lane);
+          if (a.ring_q)
+            block_copy_warp(reinterpret_cast<unsigned char*>(a.ring_q) + rr * krow,
+                            st + SL.qr + i * krow, (int)krow, lane);
+          if (KDA)
+            block_copy_warp(reinterpret_cast<unsigned char*>(a.ring_alpha) + rr * arow,
+                            st + SL.ar + j * arow, (int)arow, lane);
+          if (lane == 0) {
+            a.ring_beta[(size_t)v * Wd + slot] = br[j];
+            if (!KDA) a.ring_alpha[(size_t)v * Wd + slot] = ar[j];
+          }
+        }
+      }
+      if (lane == 0) reinterpret_cast<int*>(sl)[ok_off] = ok ? 1 : 0;
+      __syncwarp();
+      mbar_arrive(&vfull[li % NSL]);  // every lane: its slot writes are released
+      h += NP;
+      while (h >= H) h -= H;
+    }
+    cp_async_wait_all();
+    if (a.commit && cur_seq >= 0 && ok && lane == 0 && !abort_flag)
+      arrive_and_finish(a.sync + cur_seq, seq_count, H, [&] { a.len[cur_seq] = len + 1; });
+  }
+  __syncthreads();
+  // No bulk copy may land after the block exits.
+  if (tid == 0 && abort_flag) {
+    for (int s = 0; s < NS; ++s) {
+      mbar_wait(&full[s], 0);
+      mbar_wait(&full[s], 1);
+    }
   }
 }
 
@@ -439,75 +780,136 @@ __global__ void __launch_bounds__(kThreads) delta_conventional_kernel(const DCon
   }
 }
 
-template <int DK, typename TS, typename TI, bool KDA, bool VERIFY>
-cudaError_t replay_inst(const DDecode& a, cudaStream_t st) {
-  const int RB = a.DV / a.nrb;
-  const DSmem L(RB, DK, a.W, a.K, KDA, sizeof(TS));
-  auto kern = delta_replay_kernel<DK, TS, TI, KDA, VERIFY>;
-  cudaError_t e =
-      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L.total);
+// State rows per unit: about 16 KB (at least 32 rows, dividing DV).
+int fused_rows(int DK, int ts, int DV) {
+  int RB = std::max(32, 16384 / (DK * ts) / 32 * 32);
+  RB = std::min(RB, DV);
+  while (DV % RB) RB -= 32;
+  return RB;
+}
+
+// Fused-kernel configuration: state stages, vector slots, prep warps and
+// their pipeline depth. Among the settings that fit in shared memory with at
+// least kMinStages state stages, the one with most heads in flight in the
+// prep warps (NP x depth) wins; ties go to depth 2, then to more stages.
+struct FusedConfig {
+  int NS, NSL, NP, depth;
+  size_t smem;
+};
+constexpr int kMinStages = 8;
+
+FusedConfig fused_config(int RB, int DK, int DV, int W, int K, int GU, bool kda, int ts, int ti,
+                         size_t optin) {
+  FusedConfig best{0, 0, 0, 0, 0};
+  const int np_max = kFWarps - 1 - kFGroups * GU;
+  for (int depth = 2; depth >= 1; --depth) {
+    for (int NP = np_max; NP >= 1; --NP) {
+      const int NSL = std::min(kFMaxSlots, NP + 4);
+      const DFusedSmem L0(RB, DK, DV, W, K, 0, NSL, NP, depth, kda, ts, ti);
+      const size_t fixed = L0.total + 1024;
+      if (fixed >= optin) continue;
+      const int fit = (int)((optin - fixed) / (L0.stage + 16));
+      const int NS = std::min(fit, 12) / kFGroups * kFGroups;
+      if (NS < kMinStages) continue;
+      const bool better = NP * depth > best.NP * best.depth ||
+                          (NP * depth == best.NP * best.depth && NS > best.NS);
+      if (better) {
+        const DFusedSmem L(RB, DK, DV, W, K, NS, NSL, NP, depth, kda, ts, ti);
+        best = FusedConfig{NS, NSL, NP, depth, L.total};
+      }
+      break;  // fewer warps at this depth only lowers NP * depth
+    }
+  }
+  if (best.NP == 0) {  // tight: the fewest stages that still run
+    const int NSL = 5;
+    const DFusedSmem L0(RB, DK, DV, W, K, 0, NSL, 1, 1, kda, ts, ti);
+    const size_t fixed = L0.total + 1024;
+    if (fixed < optin) {
+      const int NS = std::min((int)((optin - fixed) / (L0.stage + 16)), 12) / kFGroups * kFGroups;
+      if (NS >= kFGroups) {
+        const DFusedSmem L(RB, DK, DV, W, K, NS, NSL, 1, 1, kda, ts, ti);
+        best = FusedConfig{NS, NSL, 1, 1, L.total};
+      }
+    }
+  }
+  return best;
+}
+
+// Tile shape, stage count and template instance of the fused kernel.
+template <int DK, typename TS, typename TI, bool KDA, int KMAX>
+cudaError_t launch_fused(DFused a, cudaStream_t st) {
+  const DeviceInfo& dev = device_info();
+  const int RB = fused_rows(DK, sizeof(TS), a.DV);
+  a.RB = RB;
+  a.nrb = a.DV / RB;
+  a.GU = RB % 64 == 0 ? 2 : 1;  // each warp's share must be whole 32-row groups
+  if (RB / a.GU > 128 || a.K > KMAX) return cudaErrorInvalidValue;
+  const FusedConfig c = fused_config(RB, DK, a.DV, a.W, a.K, a.GU, KDA, sizeof(TS), sizeof(TI),
+                                     (size_t)dev.smem_optin);
+  if (c.NP == 0) return cudaErrorInvalidConfiguration;
+  a.NS = c.NS;
+  a.NSL = c.NSL;
+  a.NP = c.NP;
+  a.depth = c.depth;
+  auto kern = delta_fused_kernel<DK, TS, TI, KDA, KMAX>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)c.smem);
   if (e != cudaSuccess) return e;
-  const long long blocks = (long long)a.batch * a.H * a.nrb;
-  kern<<<(unsigned)blocks, kThreads, L.total, st>>>(a);
+  const long long heads = (long long)a.batch * a.H;
+  const int grid = (int)std::min<long long>(heads, dev.sms);
+  kern<<<grid, 32 * (kFGroups * a.GU + 1 + c.NP), c.smem, st>>>(a);
   return cudaGetLastError();
 }
 
-template <bool VERIFY>
-cudaError_t replay_dispatch(const replayssm_dims& d, const DDecode& a, bool rd16, cudaStream_t st) {
-  const bool in16 = d.in_dtype == REPLAYSSM_BF16;
+template <int DK, typename TS, typename TI, bool KDA>
+cudaError_t launch_fused_k(const DFused& a, cudaStream_t st) {
+  if (a.K == 1) return launch_fused<DK, TS, TI, KDA, 1>(a, st);
+  if (a.K <= 4) return launch_fused<DK, TS, TI, KDA, 4>(a, st);
+  return launch_fused<DK, TS, TI, KDA, 8>(a, st);
+}
+
+cudaError_t launch_delta(const replayssm_dims& d, const replayssm_state& s, int K, int commit,
+                         const void* q, const void* k, const void* v, const float* alpha,
+                         const float* beta, float scale, float* o, cudaStream_t st) {
+  DFused a{d.batch, d.heads, d.dv, d.window, K, commit, 0, 0, 0, 0, 0, 0, 0,
+           s.S_read ? (const void*)s.S_read : (const void*)s.S_ckpt,
+           q, k, v, alpha, beta, scale, o,
+           s.ring_q, s.ring_k, s.ring_v, s.ring_alpha, s.ring_beta,
+           s.ring_head, s.ring_len, s.status, s.sync};
+  const bool rd16 = s.S_read != nullptr, in16 = d.in_dtype == REPLAYSSM_BF16;
   const bool kda = d.kind == REPLAYSSM_KDA;
-#define RS_REPLAY(DK_)                                                                          \
-  if (rd16) {                                                                                   \
-    if (in16) return kda ? replay_inst<DK_, bf16, bf16, true, VERIFY>(a, st)                    \
-                         : replay_inst<DK_, bf16, bf16, false, VERIFY>(a, st);                  \
-    return kda ? replay_inst<DK_, bf16, float, true, VERIFY>(a, st)                             \
-               : replay_inst<DK_, bf16, float, false, VERIFY>(a, st);                           \
-  }                                                                                             \
-  if (in16) return kda ? replay_inst<DK_, float, bf16, true, VERIFY>(a, st)                     \
-                       : replay_inst<DK_, float, bf16, false, VERIFY>(a, st);                   \
-  return kda ? replay_inst<DK_, float, float, true, VERIFY>(a, st)                              \
-             : replay_inst<DK_, float, float, false, VERIFY>(a, st);
+#define RS_FUSED(DK_, TS_)                                                                     \
+  return in16 ? (kda ? launch_fused_k<DK_, TS_, bf16, true>(a, st)                             \
+                     : launch_fused_k<DK_, TS_, bf16, false>(a, st))                           \
+              : (kda ? launch_fused_k<DK_, TS_, float, true>(a, st)                            \
+                     : launch_fused_k<DK_, TS_, float, false>(a, st));
   if (d.dk == 128) {
-    RS_REPLAY(128)
+    if (rd16) { RS_FUSED(128, bf16) }
+    RS_FUSED(128, float)
   }
-  RS_REPLAY(64)
-#undef RS_REPLAY
-}
-
-// Row blocks per head: split heads when the batch cannot fill the SMs.
-int pick_row_blocks(const replayssm_dims& d) {
-  int nrb = 1;
-  const int sms = device_info().sms;
-  while (nrb < 8 && d.dv / (nrb * 2) >= 32 && (d.dv / (nrb * 2)) % 32 == 0 &&
-         (long long)d.batch * d.heads * nrb < 2LL * sms)
-    nrb *= 2;
-  return nrb;
-}
-
-DDecode make_args(const replayssm_dims& d, const replayssm_state& s, int K, const void* q,
-                  const void* k, const void* v, const float* alpha, const float* beta,
-                  float scale, float* o) {
-  return DDecode{d.batch, d.heads, d.dv, d.window, pick_row_blocks(d), K,
-                 s.S_read ? (const void*)s.S_read : (const void*)s.S_ckpt,
-                 q, k, v, alpha, beta, scale, o,
-                 s.ring_q, s.ring_k, s.ring_v, s.ring_alpha, s.ring_beta,
-                 s.ring_head, s.ring_len, s.status, s.sync};
+  if (rd16) { RS_FUSED(64, bf16) }
+  RS_FUSED(64, float)
+#undef RS_FUSED
 }
 
 }  // namespace
 
+size_t delta_fused_smem(const replayssm_dims& d, int K, bool read16) {
+  // the smallest fused block that runs (one prep warp, one stage per group)
+  const int ti = d.in_dtype == REPLAYSSM_BF16 ? 2 : 4, ts = read16 ? 2 : 4;
+  return DFusedSmem(fused_rows(d.dk, ts, d.dv), d.dk, d.dv, d.window, K, kFGroups, 5, 1, 1,
+                    d.kind == REPLAYSSM_KDA, ts, ti).total + 1024;
+}
+
 cudaError_t launch_delta_decode(const replayssm_dims& d, const replayssm_state& s, const void* q,
                                 const void* k, const void* v, const float* alpha,
                                 const float* beta, float scale, float* o, cudaStream_t st) {
-  return replay_dispatch<false>(d, make_args(d, s, 1, q, k, v, alpha, beta, scale, o),
-                                s.S_read != nullptr, st);
+  return launch_delta(d, s, 1, 1, q, k, v, alpha, beta, scale, o, st);
 }
 
 cudaError_t launch_delta_verify(const replayssm_dims& d, const replayssm_state& s, int K,
                                 const void* q, const void* k, const void* v, const float* alpha,
                                 const float* beta, float scale, float* o, cudaStream_t st) {
-  return replay_dispatch<true>(d, make_args(d, s, K, q, k, v, alpha, beta, scale, o),
-                               s.S_read != nullptr, st);
+  return launch_delta(d, s, K, 0, q, k, v, alpha, beta, scale, o, st);
 }
 
 cudaError_t launch_delta_fold(const replayssm_dims& d, const replayssm_state& s, int k_next,

@@ -49,6 +49,8 @@ cudaError_t launch_delta_decode(const replayssm_dims& d, const replayssm_state& 
 cudaError_t launch_delta_verify(const replayssm_dims& d, const replayssm_state& s, int K,
                                 const void* q, const void* k, const void* v, const float* alpha,
                                 const float* beta, float scale, float* o, cudaStream_t st);
+// Shared memory the fused delta decode / verify block needs at least.
+size_t delta_fused_smem(const replayssm_dims& d, int K, bool read16);
 cudaError_t launch_delta_fold(const replayssm_dims& d, const replayssm_state& s, int k_next,
                               int force, cudaStream_t st);
 cudaError_t launch_delta_conventional(const replayssm_dims& d, float* S, const void* q,

@@ -138,8 +138,8 @@ __global__ void __launch_bounds__(kStreamMaxThreads, 1) stream_kernel(const Stre
       const bool write = a.flags[seq] != 0;
       const float* w0 = a.work + ((size_t)seq * K * H + h) * a.wrow;
       float vec[KMAX][kE];
-      float scale[KMAX], extra[KMAX][4];  // [k][32-row group]
-      const int ngr = RBp / 32;           // 32-row groups of this warp (1..4)
+      float scale[KMAX], extra[4];  // extra: single-vector case, per 32-row group
+      const int ngr = RBp / 32;     // 32-row groups of this warp (1..4)
 #pragma unroll
       for (int k = 0; k < KMAX; ++k) {
         if (k >= K) break;
@@ -160,9 +160,11 @@ __global__ void __launch_bounds__(kStreamMaxThreads, 1) stream_kernel(const Stre
           for (int e = 0; e < kE; ++e) vec[k][e] = to_f(vin[e]);
         }
         scale[k] = a.scale_off >= 0 ? wk[a.scale_off] : 1.f;
+      }
+      if constexpr (KMAX == 1) {
 #pragma unroll
         for (int q = 0; q < 4; ++q)
-          if (q < ngr) extra[k][q] = wk[a.extra_off + row0 + 32 * q + RD::row_of(lane)];
+          if (q < ngr) extra[q] = w0[a.extra_off + row0 + 32 * q + RD::row_of(lane)];
       }
       const bool aborted = __shfl_sync(kFull, abort_flag, 0) != 0;
       const bool landed = !aborted && mbar_wait_warp(&full[s], ph);
@@ -173,28 +175,59 @@ __global__ void __launch_bounds__(kStreamMaxThreads, 1) stream_kernel(const Stre
       if (group_any(!landed)) break;  // one decision per group
       const TS* tile = reinterpret_cast<const TS*>(smem + (size_t)s * stage) + (size_t)part * RBp * N;
       float* yrow = a.out + ((size_t)seq * K * H + h) * P + row0;
-      if (kEarly && ngr == 1) {
+      if constexpr (KMAX > 1) {
+        // Several vectors: read the tile from shared memory once per chunk of
+        // KC vectors (KC * kLpr accumulators stay in registers); the additive
+        // terms are loaded per 32-row group.
+        constexpr int KC = KMAX < 64 / RD::kLpr ? KMAX : 64 / RD::kLpr;
+#pragma unroll 1
+        for (int q = 0; q < ngr; ++q) {
+          const int r = 32 * q + RD::row_of(lane);
+#pragma unroll 1
+          for (int k0 = 0; k0 < KMAX; k0 += KC) {
+            if (k0 >= K) break;
+            float ex[KC];
+#pragma unroll
+            for (int c = 0; c < KC; ++c)
+              ex[c] = k0 + c < K ? w0[(size_t)(k0 + c) * H * a.wrow + a.extra_off + row0 + r] : 0.f;
+            float acc[KC][RD::kLpr];
+            const TS* base = tile + (size_t)(32 * q + lane / RD::kLpr) * N + c0;
+#pragma unroll
+            for (int kk = 0; kk < RD::kLpr; ++kk) {
+              const uint4 raw = *reinterpret_cast<const uint4*>(base + (size_t)kk * RD::kRpi * N);
+              float f[kE];
+              unpack<TS>(raw, f);
+#pragma unroll
+              for (int c = 0; c < KC; ++c) {
+                float sacc = 0.f;
+#pragma unroll
+                for (int e = 0; e < kE; ++e) sacc = fmaf(f[e], vec[k0 + c][e], sacc);
+                acc[c][kk] = sacc;
+              }
+            }
+#pragma unroll
+            for (int c = 0; c < KC; ++c) {
+              if (k0 + c >= K) break;
+              const float d = reduce_scatter<RD::kLpr>(acc[c], lane);
+              if (write) yrow[(size_t)(k0 + c) * H * P + r] = fmaf(scale[k0 + c], d, ex[c]);
+            }
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);
+      } else if (kEarly && ngr == 1) {
         uint4 raw[RD::kLpr];
         RD::load32(tile, 0, lane, raw);
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[s]);
-#pragma unroll
-        for (int k = 0; k < KMAX; ++k) {
-          if (k >= K) break;
-          const float d = RD::dot32(raw, vec[k], lane);
-          if (write) yrow[(size_t)k * H * P + RD::row_of(lane)] = fmaf(scale[k], d, extra[k][0]);
-        }
+        const float d = RD::dot32(raw, vec[0], lane);
+        if (write) yrow[RD::row_of(lane)] = fmaf(scale[0], d, extra[0]);
       } else {
 #pragma unroll
-        for (int k = 0; k < KMAX; ++k) {
-          if (k >= K) break;
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            if (q >= ngr) break;
-            const float d = RD::rows32(tile, 32 * q, vec[k], lane);
-            if (write)
-              yrow[(size_t)k * H * P + 32 * q + RD::row_of(lane)] = fmaf(scale[k], d, extra[k][q]);
-          }
+        for (int q = 0; q < 4; ++q) {
+          if (q >= ngr) break;
+          const float d = RD::rows32(tile, 32 * q, vec[0], lane);
+          if (write) yrow[32 * q + RD::row_of(lane)] = fmaf(scale[0], d, extra[q]);
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[s]);
