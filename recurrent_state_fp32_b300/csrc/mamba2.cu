@@ -49,10 +49,11 @@ struct M2Prep {
 // (buffered x rows in entry order, current x, ring dt row, dt/A/D) and the
 // warp's cache for the current (sequence, group): C, B of the token, C.B_j.
 struct M2PrepSmem {
-  size_t xr, xt, dtr, sc, stage, Cf, Bt, CB, warp_bytes;
+  size_t hdr, xr, xt, dtr, sc, stage, Cf, Bt, CB, warp_bytes;
   __host__ __device__ M2PrepSmem(int P, int N, int W, int ti) {
-    xr = 0;
-    xt = align_up((size_t)W * P * ti, 16);
+    hdr = 0;                             // len, head, ok, seq as the issue side read them
+    xr = 16;
+    xt = xr + align_up((size_t)W * P * ti, 16);
     dtr = xt + align_up((size_t)P * ti, 16);
     sc = dtr + (size_t)ring_wd(W) * 4;   // dt, A, D of the head
     stage = align_up(sc + 16, 16);
@@ -88,6 +89,7 @@ __global__ void __launch_bounds__(32 * kPrepWarps) mamba2_prep_kernel(const M2Pr
   const int Wd = ring_wd(W);
   const M2PrepSmem L(P, N, W, sizeof(TI));
   unsigned char* wbase = smem + (size_t)warp * L.warp_bytes;
+  griddep_launch_dependents();  // the stream kernel may start streaming state rows
   const long long heads = (long long)a.batch * H;
   const long long nw = (long long)gridDim.x * kPrepWarps;
   const long long gw = (long long)blockIdx.x * kPrepWarps + warp;
@@ -127,6 +129,12 @@ __global__ void __launch_bounds__(32 * kPrepWarps) mamba2_prep_kernel(const M2Pr
     }
     const int v = v0 + i_t;
     unsigned char* st = wbase + (size_t)(i_t % kPrepDepth) * L.stage;
+    if (lane == 0) {
+      int* hdr = reinterpret_cast<int*>(st + L.hdr);
+      hdr[0] = i_len;
+      hdr[1] = i_hd;
+      hdr[2] = i_ok ? 1 : 0;
+    }
     if (i_ok) {
       const unsigned char* xs = ringx + (size_t)v * W * row;
       if (lane_map) {
@@ -163,6 +171,7 @@ __global__ void __launch_bounds__(32 * kPrepWarps) mamba2_prep_kernel(const M2Pr
   int cb_seq = -1, cb_g = -1;  // (sequence, group) whose C.B_j the cache holds
   int seq_first = v0;          // first head of the current sequence in this range
   int seq = v0 / H, h = v0 - (v0 / H) * H;
+  int g = h / hpg, hg = h - g * hpg;  // group of head h and h's index in it
   const int nv = v1 - v0;
   while (i_t < kPrepDepth - 1 && i_t < nv) issue();
   for (int t = 0; t < nv; ++t) {
@@ -177,14 +186,10 @@ __global__ void __launch_bounds__(32 * kPrepWarps) mamba2_prep_kernel(const M2Pr
     if (seq != cur_seq) {
       if (cur_seq >= 0 && ok && lane == 0)  // leaving a sequence: arrive with its heads
         arrive_and_finish(a.sync + cur_seq, v - seq_first, H, [&] { a.len[cur_seq] = len + 1; });
-      int l = 0, hh = 0;
-      if (lane == 0) {
-        l = a.len[seq];
-        hh = a.head[seq];
-      }
-      len = __shfl_sync(kFull, l, 0);
-      hd = __shfl_sync(kFull, hh, 0);
-      ok = pointers_ok(hd, len, W) && len + 1 <= W;
+      const int* hdr = reinterpret_cast<const int*>(wbase + (size_t)(t % kPrepDepth) * L.stage + L.hdr);
+      len = hdr[0];
+      hd = hdr[1];
+      ok = hdr[2] != 0;
       cur_seq = seq;
       seq_first = v;
       if (h == 0 && lane == 0) {
@@ -195,7 +200,6 @@ __global__ void __launch_bounds__(32 * kPrepWarps) mamba2_prep_kernel(const M2Pr
       }
     }
     if (ok) {
-      const int g = h / hpg;
       const unsigned char* st = wbase + (size_t)(t % kPrepDepth) * L.stage;
       // C.B_j of this (sequence, group), entries 0..len (entry len: the token)
       if (seq != cb_seq || g != cb_g) {
@@ -260,8 +264,10 @@ __global__ void __launch_bounds__(32 * kPrepWarps) mamba2_prep_kernel(const M2Pr
         inc0 += __shfl_sync(kFull, inc1, 0);
       }
       const float total = __shfl_sync(kFull, inc0, 0);
-      const float w0 = dtv0 * __expf_acc(Ah * (inc0 - dtv0)) * cbv0;
-      const float w1 = n > 32 ? dtv1 * __expf_acc(Ah * (inc1 - dtv1)) * cbv1 : 0.f;
+      // exponents lie in [A_h sum dt, 0]; the fast exponential's relative
+      // error (about 1e-6 there) is far inside the output tolerance
+      const float w0 = dtv0 * __expf(Ah * (inc0 - dtv0)) * cbv0;
+      const float w1 = n > 32 ? dtv1 * __expf(Ah * (inc1 - dtv1)) * cbv1 : 0.f;
       // buffer terms: lane owns rows p = 2 lane + {0, 1} (+ 64 k)
       const TI* xr = reinterpret_cast<const TI*>(st + L.xr);
       const TI* xt = reinterpret_cast<const TI*>(st + L.xt);
@@ -293,14 +299,14 @@ __global__ void __launch_bounds__(32 * kPrepWarps) mamba2_prep_kernel(const M2Pr
         }
         if (act) *reinterpret_cast<float2*>(wrow + p) = make_float2(e0, e1);
       }
-      if (lane == 0) wrow[P] = __expf_acc(Ah * total);
+      if (lane == 0) wrow[P] = __expf(Ah * total);
       // append the token: x row and dt of this head, B and C of its group
       const int slot = hd + len < W ? hd + len : hd + len - W;
       uint4* xd = reinterpret_cast<uint4*>(const_cast<unsigned char*>(ringx) +
                                            ((size_t)v * W + slot) * row);
       for (int c = lane; c < cpr; c += 32) xd[c] = reinterpret_cast<const uint4*>(xt)[c];
       if (lane == 0) a.ring_dt[(size_t)v * Wd + slot] = dt_tok;
-      if (h - g * hpg == 0) {
+      if (hg == 0) {
         TI* dB = reinterpret_cast<TI*>(a.ring_B) + (((size_t)seq * W + slot) * G + g) * N;
         for (int c = lane; c < N; c += 32) dB[c] = Btc[c];
         if (a.ring_C) {
@@ -310,8 +316,13 @@ __global__ void __launch_bounds__(32 * kPrepWarps) mamba2_prep_kernel(const M2Pr
       }
       __syncwarp();
     }
+    if (++hg == hpg) {
+      hg = 0;
+      ++g;
+    }
     if (++h == H) {
       h = 0;
+      g = 0;
       ++seq;
     }
   }

@@ -127,6 +127,9 @@ __global__ void __launch_bounds__(kStreamMaxThreads, 1) stream_kernel(const Stre
       return res != 0;
     };
     const int c0 = RD::chunk_of(lane) * kE;  // this lane's vector elements
+    // The work rows come from the preparation grid (this grid may start
+    // before it ends); the producer's state copies do not depend on it.
+    griddep_wait();
     int s = gi;
     uint32_t ph = 0;
     for (int i = gi; u0 + i < u1; i += NG) {
@@ -274,8 +277,19 @@ cudaError_t launch_stream(StreamArgs a, cudaStream_t st) {
   const long long units = (long long)a.batch * a.H * a.nrb;
   if (units >= (1LL << 31)) return cudaErrorInvalidValue;
   const int grid = (int)std::min<long long>(units, dev.sms);
-  kern<<<grid, 32 * (kStreamGroups * a.GU + 1), smem, st>>>(a);
-  return cudaGetLastError();
+  // Launched as a programmatic dependent of the preparation kernel before it
+  // on the stream: blocks start (and stream state rows) as SMs free up.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(32 * (kStreamGroups * a.GU + 1));
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, a);
 }
 
 }  // namespace rs
