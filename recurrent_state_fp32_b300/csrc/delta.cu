@@ -594,103 +594,153 @@ struct DFold {
   int32_t* sync;
 };
 
-// Grid-stride over (sequence, head) tiles of folding sequences. Rows are
-// independent: 4 lanes per row, 8 rows per warp step; lane q of a row owns
-// the float4 chunks q, q+4, q+8, ... (so 4 lanes read 64 contiguous bytes).
+// Rows of `cols` elements (in_dtype) of ring entries 0..n-1 of one head --
+// entry j is ring slot (head + j) mod W of the head's [W][cols] block -- into
+// shared memory as float [n][cols], with 16-byte loads (cols * sizeof(TI)
+// a multiple of 16).
+template <typename TI>
+__device__ __forceinline__ void stage_rows_f32(float* dst, const TI* head_rows, int cols, int n,
+                                               int hd, int W) {
+  constexpr int epc = 16 / (int)sizeof(TI);  // elements per 16-byte chunk
+  const int cpr = cols / epc;
+  for (int idx = threadIdx.x; idx < n * cpr; idx += blockDim.x) {
+    const int j = idx / cpr, c = idx - j * cpr;
+    const int slot = hd + j < W ? hd + j : hd + j - W;
+    const uint4 raw = *reinterpret_cast<const uint4*>(head_rows + (size_t)slot * cols + c * epc);
+    float f[epc];
+    unpack<TI>(raw, f);
+    float4* d = reinterpret_cast<float4*>(dst + (size_t)j * cols + c * epc);
+#pragma unroll
+    for (int e = 0; e < epc / 4; ++e) d[e] = make_float4(f[4 * e], f[4 * e + 1], f[4 * e + 2], f[4 * e + 3]);
+  }
+}
+
+constexpr int kDFoldThreads = 256;
+
+// Consolidate for the delta-rule layers: one block per folding head (a
+// parallel pre-scan of the pointers lists them). The head's n entries (k, v,
+// gates, beta) are staged as float; each row of S evolves independently,
+//   s <- alpha (.) s;  s <- s + beta (v[r] - s . k) k   for j = 0..n-1,
+// so each thread keeps two rows x 32 columns in registers (DK / 32 lanes per
+// row), reads k_j (and a KDA gate row) from shared memory per entry, reduces
+// its partial dot with the row's other lanes, and updates with packed FMAs.
+// Rows are read once and written once (FP32 checkpoint and BF16 read copy).
 template <int DK, typename TI, bool KDA>
-__global__ void __launch_bounds__(kThreads) delta_fold_kernel(const DFold a) {
+__global__ void __launch_bounds__(kDFoldThreads, 2) delta_fold_kernel(const DFold a) {
   extern __shared__ __align__(128) unsigned char smem[];
   __shared__ FoldList fl;
-  constexpr int CH = DK / 16;  // float4 chunks per lane
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int H = a.H, DV = a.DV, W = a.W;
-  float* kbuf = reinterpret_cast<float*>(smem);                  // [W][DK]
-  float* abuf = kbuf + (size_t)W * DK;                           // [W][DK] or [W]
-  float* bbuf = abuf + (size_t)W * (KDA ? DK : 1);               // [W]
-  float* vbuf = bbuf + W;                                        // [W][DV]
+  constexpr int LPR = DK / 32;                 // lanes per row
+  constexpr int SLOTS = kDFoldThreads / LPR;   // row slots per pass
+  const int tid = threadIdx.x, q = tid % LPR, rs = tid / LPR;
+  const int H = a.H, DV = a.DV, W = a.W, Wd = ring_wd(W);
+  float* kbuf = reinterpret_cast<float*>(smem);                   // [W][DK]
+  float* abuf = kbuf + (size_t)W * DK;                            // KDA [W][DK], GDN [W]
+  float* vbuf = abuf + align_up((size_t)W * (KDA ? DK : 1), 4);   // [W][DV]
+  float* bbuf = vbuf + (size_t)W * DV;                            // [W]
   const TI* rk = reinterpret_cast<const TI*>(a.ring_k);
   const TI* rv = reinterpret_cast<const TI*>(a.ring_v);
 
   collect_folds(fl, (long long)a.batch * H, H, a.len, a.head, a.status, W, a.k_next, a.force);
   for (int f = 0; f < fl.count; ++f) {
-    const int t = fl.tile[f], len = fl.len[f], hd = fl.head[f];
-    const int seq = t / H, h = t - seq * H;
-    const int n = len;
-    auto ring_ix = [&](int j) { return ((size_t)seq * H + h) * W + (hd + j) % W; };
-    auto ring_sx = [&](int j) { return ((size_t)seq * H + h) * ring_wd(W) + (hd + j) % W; };
-    for (int idx = tid; idx < n * DK; idx += kThreads) {
-      const int j = idx / DK, c = idx - j * DK;
-      kbuf[idx] = to_f(rk[ring_ix(j) * DK + c]);
-      if (KDA) abuf[idx] = a.ring_alpha[ring_ix(j) * DK + c];
-    }
-    for (int idx = tid; idx < n * DV; idx += kThreads) {
-      const int j = idx / DV, r = idx - j * DV;
-      vbuf[idx] = to_f(rv[ring_ix(j) * DV + r]);
-    }
-    for (int j = tid; j < n; j += kThreads) {
-      bbuf[j] = a.ring_beta[ring_sx(j)];
-      if (!KDA) abuf[j] = a.ring_alpha[ring_sx(j)];
+    const int t = fl.tile[f], n = fl.len[f], hd = fl.head[f];
+    const int seq = t / H;
+    stage_rows_f32<TI>(kbuf, rk + (size_t)t * W * DK, DK, n, hd, W);
+    stage_rows_f32<TI>(vbuf, rv + (size_t)t * W * DV, DV, n, hd, W);
+    if (KDA) stage_rows_f32<float>(abuf, a.ring_alpha + (size_t)t * W * DK, DK, n, hd, W);
+    for (int j = tid; j < n; j += kDFoldThreads) {
+      const int slot = hd + j < W ? hd + j : hd + j - W;
+      bbuf[j] = a.ring_beta[(size_t)t * Wd + slot];
+      if (!KDA) abuf[j] = a.ring_alpha[(size_t)t * Wd + slot];
     }
     __syncthreads();
-    const int q = lane & 3;
-    for (int r = warp * 8 + (lane >> 2); r < DV; r += kWarps * 8) {
-      float4* row = reinterpret_cast<float4*>(a.S + ((size_t)t * DV + r) * DK);
-      float s[CH][4];
+    for (int r0 = rs; r0 < DV; r0 += 2 * SLOTS) {
+      const int r1 = r0 + SLOTS;
+      const bool has1 = r1 < DV;
+      float4* row0 = reinterpret_cast<float4*>(a.S + ((size_t)t * DV + r0) * DK) + q;
+      float4* row1 = reinterpret_cast<float4*>(a.S + ((size_t)t * DV + (has1 ? r1 : r0)) * DK) + q;
+      float2 s0[16], s1[16];
 #pragma unroll
-      for (int m = 0; m < CH; ++m) {
-        const float4 v4 = row[q + 4 * m];
-        s[m][0] = v4.x;
-        s[m][1] = v4.y;
-        s[m][2] = v4.z;
-        s[m][3] = v4.w;
+      for (int m = 0; m < 8; ++m) {
+        const float4 u = row0[LPR * m], w = row1[LPR * m];
+        s0[2 * m] = make_float2(u.x, u.y);
+        s0[2 * m + 1] = make_float2(u.z, u.w);
+        s1[2 * m] = make_float2(w.x, w.y);
+        s1[2 * m + 1] = make_float2(w.z, w.w);
       }
       for (int j = 0; j < n; ++j) {
-        const float* kj = kbuf + j * DK;
-        float d = 0.f;
+        // k_j (and a KDA gate row) are read from shared memory per use: the
+        // lanes of a warp share 4 addresses, so each read is one broadcast
+        const float4* kj = reinterpret_cast<const float4*>(kbuf + (size_t)j * DK) + q;
+        if (KDA) {
+          const float4* aj = reinterpret_cast<const float4*>(abuf + (size_t)j * DK) + q;
 #pragma unroll
-        for (int m = 0; m < CH; ++m) {
-          const float4 k4 = *reinterpret_cast<const float4*>(kj + (q + 4 * m) * 4);
-          if (KDA) {
-            const float4 a4 = *reinterpret_cast<const float4*>(abuf + j * DK + (q + 4 * m) * 4);
-            s[m][0] *= a4.x;
-            s[m][1] *= a4.y;
-            s[m][2] *= a4.z;
-            s[m][3] *= a4.w;
-          } else {
-            const float g = abuf[j];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) s[m][e] *= g;
+          for (int m = 0; m < 8; ++m) {
+            const float4 u = aj[LPR * m];
+            const float2 g0 = make_float2(u.x, u.y), g1 = make_float2(u.z, u.w);
+            s0[2 * m] = __fmul2_rn(s0[2 * m], g0);
+            s0[2 * m + 1] = __fmul2_rn(s0[2 * m + 1], g1);
+            s1[2 * m] = __fmul2_rn(s1[2 * m], g0);
+            s1[2 * m + 1] = __fmul2_rn(s1[2 * m + 1], g1);
           }
-          d = fmaf(s[m][0], k4.x, d);
-          d = fmaf(s[m][1], k4.y, d);
-          d = fmaf(s[m][2], k4.z, d);
-          d = fmaf(s[m][3], k4.w, d);
-        }
-        d += __shfl_xor_sync(kFull, d, 1);
-        d += __shfl_xor_sync(kFull, d, 2);
-        const float c = bbuf[j] * (vbuf[j * DV + r] - d);
+        } else {
+          const float g = abuf[j];
+          const float2 gg = make_float2(g, g);
 #pragma unroll
-        for (int m = 0; m < CH; ++m) {
-          const float4 k4 = *reinterpret_cast<const float4*>(kj + (q + 4 * m) * 4);
-          s[m][0] = fmaf(c, k4.x, s[m][0]);
-          s[m][1] = fmaf(c, k4.y, s[m][1]);
-          s[m][2] = fmaf(c, k4.z, s[m][2]);
-          s[m][3] = fmaf(c, k4.w, s[m][3]);
+          for (int m = 0; m < 16; ++m) {
+            s0[m] = __fmul2_rn(s0[m], gg);
+            s1[m] = __fmul2_rn(s1[m], gg);
+          }
+        }
+        float2 d0 = make_float2(0.f, 0.f), d1 = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int m = 0; m < 8; ++m) {
+          const float4 u = kj[LPR * m];
+          const float2 ka = make_float2(u.x, u.y), kb = make_float2(u.z, u.w);
+          d0 = __ffma2_rn(s0[2 * m], ka, d0);
+          d1 = __ffma2_rn(s1[2 * m], ka, d1);
+          d0 = __ffma2_rn(s0[2 * m + 1], kb, d0);
+          d1 = __ffma2_rn(s1[2 * m + 1], kb, d1);
+        }
+        float dot0 = d0.x + d0.y, dot1 = d1.x + d1.y;
+#pragma unroll
+        for (int o = 1; o < LPR; o <<= 1) {
+          dot0 += __shfl_xor_sync(kFull, dot0, o);
+          dot1 += __shfl_xor_sync(kFull, dot1, o);
+        }
+        const float bj = bbuf[j];
+        const float c0 = bj * (vbuf[(size_t)j * DV + r0] - dot0);
+        const float c1 = has1 ? bj * (vbuf[(size_t)j * DV + r1] - dot1) : 0.f;
+        const float2 cc0 = make_float2(c0, c0), cc1 = make_float2(c1, c1);
+#pragma unroll
+        for (int m = 0; m < 8; ++m) {
+          const float4 u = kj[LPR * m];
+          const float2 ka = make_float2(u.x, u.y), kb = make_float2(u.z, u.w);
+          s0[2 * m] = __ffma2_rn(cc0, ka, s0[2 * m]);
+          s0[2 * m + 1] = __ffma2_rn(cc0, kb, s0[2 * m + 1]);
+          s1[2 * m] = __ffma2_rn(cc1, ka, s1[2 * m]);
+          s1[2 * m + 1] = __ffma2_rn(cc1, kb, s1[2 * m + 1]);
         }
       }
 #pragma unroll
-      for (int m = 0; m < CH; ++m) row[q + 4 * m] = make_float4(s[m][0], s[m][1], s[m][2], s[m][3]);
+      for (int m = 0; m < 8; ++m) {
+        row0[LPR * m] = make_float4(s0[2 * m].x, s0[2 * m].y, s0[2 * m + 1].x, s0[2 * m + 1].y);
+        if (has1) row1[LPR * m] = make_float4(s1[2 * m].x, s1[2 * m].y, s1[2 * m + 1].x, s1[2 * m + 1].y);
+      }
       if (a.Sr) {
-        uint2* rrow = reinterpret_cast<uint2*>(a.Sr + ((size_t)t * DV + r) * DK);
+        uint2* rr0 = reinterpret_cast<uint2*>(a.Sr + ((size_t)t * DV + r0) * DK) + q;
+        uint2* rr1 = reinterpret_cast<uint2*>(a.Sr + ((size_t)t * DV + (has1 ? r1 : r0)) * DK) + q;
 #pragma unroll
-        for (int m = 0; m < CH; ++m)
-          rrow[q + 4 * m] = make_uint2(pack_bf16x2(s[m][0], s[m][1]), pack_bf16x2(s[m][2], s[m][3]));
+        for (int m = 0; m < 8; ++m) {
+          rr0[LPR * m] = make_uint2(pack_bf16x2(s0[2 * m].x, s0[2 * m].y), pack_bf16x2(s0[2 * m + 1].x, s0[2 * m + 1].y));
+          if (has1)
+            rr1[LPR * m] = make_uint2(pack_bf16x2(s1[2 * m].x, s1[2 * m].y), pack_bf16x2(s1[2 * m + 1].x, s1[2 * m + 1].y));
+        }
       }
     }
     __syncthreads();
     if (tid == 0)
       arrive_and_finish(a.sync + seq, 1, H, [&] {
-        a.head[seq] = (hd + len) % W;
+        a.head[seq] = (hd + n) % W;
         a.len[seq] = 0;
       });
   }
@@ -918,10 +968,11 @@ cudaError_t launch_delta_fold(const replayssm_dims& d, const replayssm_state& s,
           reinterpret_cast<bf16*>(s.S_read), s.ring_k, s.ring_v, s.ring_alpha, s.ring_beta,
           s.ring_head, s.ring_len, s.status, s.sync};
   const bool kda = d.kind == REPLAYSSM_KDA;
-  const size_t smem =
-      4 * ((size_t)d.window * d.dk + (size_t)d.window * (kda ? d.dk : 1) + d.window +
-           (size_t)d.window * d.dv);
-  const int grid = fold_grid((long long)d.batch * d.heads);
+  const size_t smem = 4 * ((size_t)d.window * d.dk + align_up((size_t)d.window * (kda ? d.dk : 1), 4) +
+                           (size_t)d.window * d.dv + d.window);
+  const long long heads = (long long)d.batch * d.heads;
+  const int grid = (int)std::max<long long>((heads + kMaxFoldTiles - 1) / kMaxFoldTiles,
+                                            std::min<long long>(heads, (long long)device_info().sms * 2));
   const bool in16 = d.in_dtype == REPLAYSSM_BF16;
   void (*kern)(const DFold);
   if (d.dk == 128)
@@ -932,7 +983,7 @@ cudaError_t launch_delta_fold(const replayssm_dims& d, const replayssm_state& s,
                 : (kda ? delta_fold_kernel<64, float, true> : delta_fold_kernel<64, float, false>);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  kern<<<grid, kThreads, smem, st>>>(a);
+  kern<<<grid, kDFoldThreads, smem, st>>>(a);
   return cudaGetLastError();
 }
 
