@@ -620,7 +620,9 @@ constexpr int kDFoldThreads = 256;
 // Consolidate for the delta-rule layers: one block per folding head (a
 // parallel pre-scan of the pointers lists them). The head's n entries (k, v,
 // gates, beta) are staged as float; each row of S evolves independently,
-//   s <- alpha (.) s;  s <- s + beta (v[r] - s . k) k   for j = 0..n-1,
+//   s <- alpha (.) s;  s <- s + beta (v[r] - s . k) k   for j = 0..n-1
+// (a scalar GDN gate is applied lazily: the row holds s / gam, gam the
+// product of the gates so far, and is rescaled once at the end),
 // so each thread keeps two rows x 32 columns in registers (DK / 32 lanes per
 // row), reads k_j (and a KDA gate row) from shared memory per entry, reduces
 // its partial dot with the row's other lanes, and updates with packed FMAs.
@@ -637,6 +639,7 @@ __global__ void __launch_bounds__(kDFoldThreads, 2) delta_fold_kernel(const DFol
   float* abuf = kbuf + (size_t)W * DK;                            // KDA [W][DK], GDN [W]
   float* vbuf = abuf + align_up((size_t)W * (KDA ? DK : 1), 4);   // [W][DV]
   float* bbuf = vbuf + (size_t)W * DV;                            // [W]
+  float* rbuf = bbuf + W;                                         // GDN [W]: 1 / alpha_j
   const TI* rk = reinterpret_cast<const TI*>(a.ring_k);
   const TI* rv = reinterpret_cast<const TI*>(a.ring_v);
 
@@ -650,7 +653,11 @@ __global__ void __launch_bounds__(kDFoldThreads, 2) delta_fold_kernel(const DFol
     for (int j = tid; j < n; j += kDFoldThreads) {
       const int slot = hd + j < W ? hd + j : hd + j - W;
       bbuf[j] = a.ring_beta[(size_t)t * Wd + slot];
-      if (!KDA) abuf[j] = a.ring_alpha[(size_t)t * Wd + slot];
+      if (!KDA) {
+        const float al = a.ring_alpha[(size_t)t * Wd + slot];
+        abuf[j] = al;
+        rbuf[j] = 1.f / al;
+      }
     }
     __syncthreads();
     for (int r0 = rs; r0 < DV; r0 += 2 * SLOTS) {
@@ -667,6 +674,7 @@ __global__ void __launch_bounds__(kDFoldThreads, 2) delta_fold_kernel(const DFol
         s1[2 * m] = make_float2(w.x, w.y);
         s1[2 * m + 1] = make_float2(w.z, w.w);
       }
+      float gam = 1.f, igam = 1.f;  // GDN: product of the gates so far, and its inverse
       for (int j = 0; j < n; ++j) {
         // k_j (and a KDA gate row) are read from shared memory per use: the
         // lanes of a warp share 4 addresses, so each read is one broadcast
@@ -683,33 +691,51 @@ __global__ void __launch_bounds__(kDFoldThreads, 2) delta_fold_kernel(const DFol
             s1[2 * m + 1] = __fmul2_rn(s1[2 * m + 1], g1);
           }
         } else {
-          const float g = abuf[j];
-          const float2 gg = make_float2(g, g);
+          // scalar gate, applied lazily: the rows hold s / gam
+          gam *= abuf[j];
+          igam *= rbuf[j];
+        }
+        float dot0, dot1;
+        if (KDA) {
+          float2 d0 = make_float2(0.f, 0.f), d1 = make_float2(0.f, 0.f);
 #pragma unroll
-          for (int m = 0; m < 16; ++m) {
-            s0[m] = __fmul2_rn(s0[m], gg);
-            s1[m] = __fmul2_rn(s1[m], gg);
+          for (int m = 0; m < 8; ++m) {
+            const float4 u = kj[LPR * m];
+            const float2 ka = make_float2(u.x, u.y), kb = make_float2(u.z, u.w);
+            d0 = __ffma2_rn(s0[2 * m], ka, d0);
+            d1 = __ffma2_rn(s1[2 * m], ka, d1);
+            d0 = __ffma2_rn(s0[2 * m + 1], kb, d0);
+            d1 = __ffma2_rn(s1[2 * m + 1], kb, d1);
           }
-        }
-        float2 d0 = make_float2(0.f, 0.f), d1 = make_float2(0.f, 0.f);
+          dot0 = d0.x + d0.y;
+          dot1 = d1.x + d1.y;
+        } else {  // two accumulators per row: shorter dependency chains
+          float2 d0 = make_float2(0.f, 0.f), d1 = make_float2(0.f, 0.f);
+          float2 e0 = make_float2(0.f, 0.f), e1 = make_float2(0.f, 0.f);
 #pragma unroll
-        for (int m = 0; m < 8; ++m) {
-          const float4 u = kj[LPR * m];
-          const float2 ka = make_float2(u.x, u.y), kb = make_float2(u.z, u.w);
-          d0 = __ffma2_rn(s0[2 * m], ka, d0);
-          d1 = __ffma2_rn(s1[2 * m], ka, d1);
-          d0 = __ffma2_rn(s0[2 * m + 1], kb, d0);
-          d1 = __ffma2_rn(s1[2 * m + 1], kb, d1);
+          for (int m = 0; m < 8; ++m) {
+            const float4 u = kj[LPR * m];
+            const float2 ka = make_float2(u.x, u.y), kb = make_float2(u.z, u.w);
+            d0 = __ffma2_rn(s0[2 * m], ka, d0);
+            d1 = __ffma2_rn(s1[2 * m], ka, d1);
+            e0 = __ffma2_rn(s0[2 * m + 1], kb, e0);
+            e1 = __ffma2_rn(s1[2 * m + 1], kb, e1);
+          }
+          dot0 = ((d0.x + d0.y) + (e0.x + e0.y)) * gam;
+          dot1 = ((d1.x + d1.y) + (e1.x + e1.y)) * gam;
         }
-        float dot0 = d0.x + d0.y, dot1 = d1.x + d1.y;
 #pragma unroll
         for (int o = 1; o < LPR; o <<= 1) {
           dot0 += __shfl_xor_sync(kFull, dot0, o);
           dot1 += __shfl_xor_sync(kFull, dot1, o);
         }
         const float bj = bbuf[j];
-        const float c0 = bj * (vbuf[(size_t)j * DV + r0] - dot0);
-        const float c1 = has1 ? bj * (vbuf[(size_t)j * DV + r1] - dot1) : 0.f;
+        float c0 = bj * (vbuf[(size_t)j * DV + r0] - dot0);
+        float c1 = has1 ? bj * (vbuf[(size_t)j * DV + r1] - dot1) : 0.f;
+        if (!KDA) {
+          c0 *= igam;
+          c1 *= igam;
+        }
         const float2 cc0 = make_float2(c0, c0), cc1 = make_float2(c1, c1);
 #pragma unroll
         for (int m = 0; m < 8; ++m) {
@@ -719,6 +745,14 @@ __global__ void __launch_bounds__(kDFoldThreads, 2) delta_fold_kernel(const DFol
           s0[2 * m + 1] = __ffma2_rn(cc0, kb, s0[2 * m + 1]);
           s1[2 * m] = __ffma2_rn(cc1, ka, s1[2 * m]);
           s1[2 * m + 1] = __ffma2_rn(cc1, kb, s1[2 * m + 1]);
+        }
+      }
+      if (!KDA) {
+        const float2 gg = make_float2(gam, gam);
+#pragma unroll
+        for (int m = 0; m < 16; ++m) {
+          s0[m] = __fmul2_rn(s0[m], gg);
+          s1[m] = __fmul2_rn(s1[m], gg);
         }
       }
 #pragma unroll
@@ -969,7 +1003,7 @@ cudaError_t launch_delta_fold(const replayssm_dims& d, const replayssm_state& s,
           s.ring_head, s.ring_len, s.status, s.sync};
   const bool kda = d.kind == REPLAYSSM_KDA;
   const size_t smem = 4 * ((size_t)d.window * d.dk + align_up((size_t)d.window * (kda ? d.dk : 1), 4) +
-                           (size_t)d.window * d.dv + d.window);
+                           (size_t)d.window * d.dv + 2 * (size_t)d.window);
   const long long heads = (long long)d.batch * d.heads;
   const int grid = (int)std::max<long long>((heads + kMaxFoldTiles - 1) / kMaxFoldTiles,
                                             std::min<long long>(heads, (long long)device_info().sms * 2));
