@@ -874,13 +874,15 @@ int fused_rows(int DK, int ts, int DV) {
 
 // Fused-kernel configuration: state stages, vector slots, prep warps and
 // their pipeline depth. Among the settings that fit in shared memory with at
-// least kMinStages state stages, the one with most heads in flight in the
+// least min_stages state stages, the one with most heads in flight in the
 // prep warps (NP x depth) wins; ties go to depth 2, then to more stages.
 struct FusedConfig {
   int NS, NSL, NP, depth;
   size_t smem;
 };
-constexpr int kMinStages = 8;
+// Fewest state stages a configuration may have: BF16 tiles stream fine from 4
+// (more prep warps pay off there), FP32 tiles need 8.
+constexpr int min_stages(int ts) { return ts == 2 ? 4 : 8; }
 
 FusedConfig fused_config(int RB, int DK, int DV, int W, int K, int GU, bool kda, int ts, int ti,
                          size_t optin) {
@@ -894,7 +896,7 @@ FusedConfig fused_config(int RB, int DK, int DV, int W, int K, int GU, bool kda,
       if (fixed >= optin) continue;
       const int fit = (int)((optin - fixed) / (L0.stage + 16));
       const int NS = std::min(fit, 12) / kFGroups * kFGroups;
-      if (NS < kMinStages) continue;
+      if (NS < min_stages(ts)) continue;
       const bool better = NP * depth > best.NP * best.depth ||
                           (NP * depth == best.NP * best.depth && NS > best.NS);
       if (better) {
