@@ -39,6 +39,8 @@ WORKLOADS = {
     "mamba2": dict(kind="mamba2", batch=256, heads=128, dk=128, dv=64, window=16, groups=1),
     "gdn": dict(kind="gdn", batch=256, heads=32, dk=128, dv=128, window=16, groups=1),
     "kda": dict(kind="kda", batch=256, heads=32, dk=128, dv=128, window=16, groups=1),
+    # speculative rounds: consolidate(k_next = K) + verify K drafts + accept m
+    "gdn_spec": dict(kind="gdn", batch=512, heads=32, dk=128, dv=128, window=16, groups=1, K=4),
 }
 POOL = 16  # distinct synthetic tokens, cycled through the timed steps
 
@@ -423,6 +425,124 @@ def run_e2e(layer, args, stream, world):
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": K}
 
 
+# ------------------------------------------------------ speculative rounds
+def run_spec(args, rank, local_rank, world):
+    """Speculative decoding rounds on a delta layer: consolidate(k_next = K),
+    verify K drafts from one read of the state, accept m drafts by moving the
+    ring pointer (m drawn U{0..K} per sequence and round). The A/B runs the
+    conventional baseline on the same drafts: verify with a state snapshot per
+    draft, then accept by copying snapshot m - 1 into the state."""
+    import numpy as np
+    import torch
+
+    import synth
+    from recurrent_state_fp32_b300 import api
+
+    device = torch.device("cuda", local_rank)
+    torch.cuda.set_device(device)
+    wl = dict(WORKLOADS[args.workload])
+    if args.batch:
+        wl["batch"] = args.batch
+    b, H, dk, dv, W, K, kind = (wl[x] for x in ("batch", "heads", "dk", "dv", "window", "K", "kind"))
+    dims = api.LayerDims(kind, b, H, dk=dk, dv=dv, window=W, in_dtype="bf16")
+    state = api.LayerState(dims, device=device, read_copy=(args.read == "bf16"), max_drafts=K)
+    gen = torch.Generator(device=device)
+    gen.manual_seed(4)
+    state.S_ckpt.normal_(0.0, 0.1, generator=gen)
+    if state.S_read is not None:
+        api.refresh_read_copy(dims, state)
+    seed, rounds_pool = 4, 8
+    to = lambda a, ty: torch.from_numpy(np.ascontiguousarray(a)).to(device, ty)  # noqa: E731
+    drafts, ms, m_tot = [], [], []
+    for r in range(rounds_pool):
+        dr = synth.spec_draft_inputs(seed, r, b, K, H, dk, dv, kind, "bf16")
+        drafts.append({n: to(v, torch.bfloat16 if n in ("q", "k", "v") else torch.float32)
+                       for n, v in dr.items()})
+        m = synth.accept_counts(seed, r, b, K)
+        ms.append(to(m, torch.int32))
+        m_tot.append(int(m.sum()))
+    o = torch.empty((b, K, H, dv), device=device)
+
+    def round_(i):
+        d = drafts[i % rounds_pool]
+        api.consolidate(dims, state, None, K, False)
+        api.spec_verify(dims, state, K, d["q"], d["k"], d["v"], d["alpha"], d["beta"], 1.0, o)
+        api.accept(dims, state, ms[i % rounds_pool], K)
+
+    Kt, Wm = args.steps, args.warmup
+    for i in range(Wm):
+        round_(i)
+    torch.cuda.synchronize()
+    ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+    a0, a1 = ev(), ev()
+    clocks = ClockSampler(local_rank) if not args.no_extras else None
+    if clocks:
+        clocks.__enter__()
+    barrier(world)
+    torch.cuda.synchronize()
+    a0.record()
+    for i in range(Kt):
+        round_(Wm + i)
+    a1.record()
+    a1.synchronize()
+    barrier(world)
+    if clocks:
+        clocks.__exit__(None, None, None)
+    ms_tot = max_over_ranks(a0.elapsed_time(a1), world)
+    accepted = sum(m_tot[(Wm + i) % rounds_pool] for i in range(Kt)) * world
+    bad = int(state.status.ne(0).sum().item())
+    res = {
+        "metric": "speculative rounds: accepted tokens/s per SSM layer (verified K drafts per "
+                  "sequence from one state read, pointer accept)",
+        "value": round(accepted / (ms_tot / 1e3), 1), "unit": "accepted tokens/s",
+        "n_gpus": world, "steps": Kt, "warmup": Wm, "ms_per_step": round(ms_tot / Kt, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded; no weights or datasets)",
+        "config": {"workload": f"{kind}_spec_b{b}_h{H}_d{dk}_w{W}_k{K}", "batch_per_gpu": b,
+                   "drafts": K, "read_copy": args.read, "inputs": "bf16", "checkpoint": "f32",
+                   "step": "consolidate(k_next=K) + spec_verify(K) + accept(m)",
+                   "l2": "state larger than L2 (no flush)", "parallelism": f"replicas x{world}"},
+        "verified_tokens_per_s": round(b * K * Kt * world / (ms_tot / 1e3), 1),
+        "gpu_launches": Kt * 3, "device_status_ok": bad == 0,
+    }
+    if clocks:
+        res["clocks"] = clocks.summary()
+    if not args.no_extras:
+        # the conventional baseline: snapshots per draft, accept by copy
+        S = state.S_ckpt.clone()
+        snaps = torch.empty((b, K, H, dv, dk), device=device)
+        st = torch.zeros(b, dtype=torch.int32, device=device)
+
+        def conv_round(i):
+            d = drafts[i % rounds_pool]
+            api.conventional_gdn_verify(dims, S, K, d["q"], d["k"], d["v"], d["alpha"],
+                                        d["beta"], 1.0, snaps, o)
+            api.conventional_accept(dims, S, snaps, ms[i % rounds_pool], K, st)
+
+        for i in range(4):
+            conv_round(i)
+        Kc = max(8, Kt // 4)
+        c0, c1 = ev(), ev()
+        torch.cuda.synchronize()
+        c0.record()
+        for i in range(Kc):
+            conv_round(i)
+        c1.record()
+        c1.synchronize()
+        cms = max_over_ranks(c0.elapsed_time(c1), world)
+        acc_c = sum(m_tot[i % rounds_pool] for i in range(Kc)) * world
+        res["ab"] = {"conventional_accepted_tokens_per_s": round(acc_c / (cms / 1e3), 1),
+                     "conventional_ms_per_round": round(cms / Kc, 5), "rounds": Kc,
+                     # verify: read S, write K snapshots; accept: copy one snapshot
+                     # for every sequence with m > 0
+                     "conventional_bytes_per_round":
+                         int(b * H * dv * dk * 4 * (1 + K) +
+                             np.mean([int((mm > 0).sum().item()) for mm in ms]) * H * dv * dk * 8)}
+        del S, snaps
+        torch.cuda.empty_cache()
+    return res
+
+
 # --------------------------------------------------------- oracle timing
 def oracle_sample(wl: dict, heads: int, seed: int = 2):
     """A one-sequence, `heads`-head slice of the workload for the CPU oracle."""
@@ -532,7 +652,10 @@ def main(argv=None):
         import torch.distributed as dist
 
         dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
-    res = run_ours(args, rank, local_rank, world)
+    if "K" in WORKLOADS[args.workload]:
+        res = run_spec(args, rank, local_rank, world)
+    else:
+        res = run_ours(args, rank, local_rank, world)
     if rank == 0:
         print(json.dumps(res), flush=True)
     if world > 1:

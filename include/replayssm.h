@@ -232,6 +232,34 @@ REPLAYSSM_API replayssm_status replayssm_conventional_gdn_step(
     const float* alpha, const float* beta, float scale, float* o, void* stream);
 
 /*
+ * Conventional speculative verify of K drafts with a state snapshot per
+ * draft: the baseline that rollback by a buffer pointer replaces ("NVIDIA
+ * présente ReplaySSM : accélérer le décodage des modèles hybrides Mamba et
+ * GDN", section "D'où vient le problème de l'état": a fixed-size state cannot
+ * be truncated, so each draft's state is kept). GDN/KDA only.
+ * S: f32 [b, H, d_v, d_k], read, not modified. Drafts q, k, v [b, K, H, d]
+ * (in_dtype), alpha [b, K, H] or [b, K, H, d_k], beta [b, K, H] (f32).
+ * Writes snapshots[b, K, H, d_v, d_k] (f32), the state after drafts 0..i,
+ * and o[b, K, H, d_v] = scale * S_i q_i. 1 <= K <= 8.
+ */
+REPLAYSSM_API replayssm_status replayssm_conventional_gdn_verify(
+    const replayssm_dims* dims, const float* S, int32_t K, const void* q, const void* k,
+    const void* v, const float* alpha, const float* beta, float scale, float* snapshots, float* o,
+    void* stream);
+
+/*
+ * Conventional accept after replayssm_conventional_gdn_verify: for each
+ * sequence, S = snapshot m[seq] - 1 (m = 0 leaves S unchanged). m outside
+ * [0, K] sets REPLAYSSM_SEQ_BAD_ACCEPT in status[seq] (status may be NULL)
+ * and leaves S unchanged. Any kind; S and snapshots as above (Mamba-2:
+ * P x N per head). batch <= 65535.
+ */
+REPLAYSSM_API replayssm_status replayssm_conventional_accept(const replayssm_dims* dims, float* S,
+                                                             const float* snapshots,
+                                                             const int32_t* m, int32_t K,
+                                                             int32_t* status, void* stream);
+
+/*
  * Mamba-2 replay decode that allocates nothing and needs no caller scratch.
  * The paper has no counterpart: this is a library convenience.
  *

@@ -12,7 +12,9 @@ from .api import (  # noqa: F401
     ReplaySSMError,
     accept,
     consolidate,
+    conventional_accept,
     conventional_gdn_step,
+    conventional_gdn_verify,
     conventional_mamba2_step,
     gdn_decode,
     mamba2_decode,

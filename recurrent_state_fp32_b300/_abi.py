@@ -52,6 +52,8 @@ SIGNATURES = {
     "replayssm_refresh_read_copy": [_DP, _SP, _P],
     "replayssm_conventional_mamba2_step": [_DP, _P, _P, _P, _P, _P, _P, _P, _P, _P],
     "replayssm_conventional_gdn_step": [_DP, _P, _P, _P, _P, _P, _P, _F, _P, _P],
+    "replayssm_conventional_gdn_verify": [_DP, _P, _I, _P, _P, _P, _P, _P, _F, _P, _P, _P],
+    "replayssm_conventional_accept": [_DP, _P, _P, _P, _I, _P, _P],
     "replayssm_workspace_bytes": [_DP, _I],
     "replayssm_status_string": [_I],
     "replayssm_version": [],

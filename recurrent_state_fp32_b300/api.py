@@ -195,6 +195,19 @@ def conventional_gdn_step(dims, S, q, k, v, alpha, beta, scale, o, stream=None):
           _ptr(v), _ptr(alpha), _ptr(beta), float(scale), _ptr(o), _stream(stream))
 
 
+def conventional_gdn_verify(dims, S, K, q, k, v, alpha, beta, scale, snapshots, o, stream=None):
+    """Baseline speculative verify: K drafts stepped with a state snapshot each."""
+    _call("replayssm_conventional_gdn_verify", ctypes.byref(dims.c()), _ptr(S), int(K), _ptr(q),
+          _ptr(k), _ptr(v), _ptr(alpha), _ptr(beta), float(scale), _ptr(snapshots), _ptr(o),
+          _stream(stream))
+
+
+def conventional_accept(dims, S, snapshots, m, K, status=None, stream=None):
+    """Baseline accept: S = snapshot m - 1 per sequence (m = 0: unchanged)."""
+    _call("replayssm_conventional_accept", ctypes.byref(dims.c()), _ptr(S), _ptr(snapshots),
+          _ptr(m), int(K), _ptr(status), _stream(stream))
+
+
 def workspace_bytes(dims: LayerDims, K: int = 1) -> int:
     """Bytes of scratch a state needs for decode (K = 1) and verify with up to K drafts."""
     return int(_abi.lib.replayssm_workspace_bytes(ctypes.byref(dims.c()), int(K)))

@@ -49,6 +49,25 @@ __global__ void accept_kernel(int batch, int W, int K, const int32_t* __restrict
     len[s] = l + mv;
 }
 
+// Restores the state of the accepted prefix from its snapshot: block x of
+// sequence y copies a slice of snapshot m - 1 into S (m = 0: nothing to do).
+__global__ void conventional_accept_kernel(long long per_seq4, int K, const int32_t* __restrict__ m,
+                                           const float4* __restrict__ snap,
+                                           float4* __restrict__ S, int32_t* __restrict__ status) {
+  const int seq = blockIdx.y;
+  const int mv = m[seq];
+  if (mv < 0 || mv > K) {
+    if (blockIdx.x == 0 && threadIdx.x == 0 && status) status[seq] |= REPLAYSSM_SEQ_BAD_ACCEPT;
+    return;
+  }
+  if (mv == 0) return;
+  const float4* src = snap + ((long long)seq * K + (mv - 1)) * per_seq4;
+  float4* dst = S + (long long)seq * per_seq4;
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < per_seq4;
+       i += (long long)gridDim.x * blockDim.x)
+    dst[i] = src[i];
+}
+
 __global__ void refresh_kernel(const float4* __restrict__ S, uint2* __restrict__ R, long long n4) {
   for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n4;
        i += (long long)gridDim.x * blockDim.x) {
@@ -63,6 +82,16 @@ cudaError_t launch_accept(const replayssm_dims& d, const replayssm_state& s, con
                           int K, cudaStream_t st) {
   accept_kernel<<<(d.batch + 255) / 256, 256, 0, st>>>(d.batch, d.window, K, m, s.ring_len,
                                                        s.status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_conventional_accept(const replayssm_dims& d, float* S, const float* snap,
+                                       const int32_t* m, int K, int32_t* status, cudaStream_t st) {
+  // one snapshot is H * d_v * d_k floats per sequence (a multiple of 4)
+  const long long per_seq4 = (long long)d.heads * d.dv * d.dk / 4;
+  const int bx = (int)std::max<long long>(1, std::min<long long>((per_seq4 + 255) / 256, 64));
+  conventional_accept_kernel<<<dim3(bx, d.batch), 256, 0, st>>>(
+      per_seq4, K, m, reinterpret_cast<const float4*>(snap), reinterpret_cast<float4*>(S), status);
   return cudaGetLastError();
 }
 
@@ -322,6 +351,38 @@ REPLAYSSM_API replayssm_status replayssm_conventional_gdn_step(
   if (dims->batch == 0) return REPLAYSSM_OK;
   return finish(rs::launch_delta_conventional(*dims, S, q, k, v, alpha, beta, scale, o,
                                               static_cast<cudaStream_t>(stream)));
+}
+
+REPLAYSSM_API replayssm_status replayssm_conventional_gdn_verify(
+    const replayssm_dims* dims, const float* S, int32_t K, const void* q, const void* k,
+    const void* v, const float* alpha, const float* beta, float scale, float* snapshots, float* o,
+    void* stream) {
+  RS_TRY(check_dims(dims));
+  if (dims->kind == REPLAYSSM_MAMBA2) return REPLAYSSM_ERR_INVALID_ARG;
+  if (K < 1 || K > 8) return REPLAYSSM_ERR_INVALID_ARG;
+  RS_TRY(check_ptr(S));
+  RS_TRY(check_delta_token(q, k, v, alpha, beta));
+  RS_TRY(check_ptr(snapshots));
+  RS_TRY(check_ptr(o));
+  if (dims->batch == 0) return REPLAYSSM_OK;
+  return finish(rs::launch_delta_conventional_verify(*dims, S, K, q, k, v, alpha, beta, scale,
+                                                     snapshots, o, static_cast<cudaStream_t>(stream)));
+}
+
+REPLAYSSM_API replayssm_status replayssm_conventional_accept(const replayssm_dims* dims, float* S,
+                                                             const float* snapshots,
+                                                             const int32_t* m, int32_t K,
+                                                             int32_t* status, void* stream) {
+  RS_TRY(check_dims(dims));
+  if (K < 1 || K > 8) return REPLAYSSM_ERR_INVALID_ARG;
+  RS_TRY(check_ptr(S));
+  RS_TRY(check_ptr(snapshots));
+  RS_TRY(check_ptr(m));
+  RS_TRY(check_opt(status));
+  if (dims->batch == 0) return REPLAYSSM_OK;
+  if (dims->batch > 65535) return REPLAYSSM_ERR_UNSUPPORTED;
+  return finish(rs::launch_conventional_accept(*dims, S, snapshots, m, K, status,
+                                               static_cast<cudaStream_t>(stream)));
 }
 
 REPLAYSSM_API int64_t replayssm_workspace_bytes(const replayssm_dims* dims, int32_t K) {

@@ -864,6 +864,101 @@ __global__ void __launch_bounds__(kThreads) delta_conventional_kernel(const DCon
   }
 }
 
+struct DConvSpec {
+  int batch, H, DV, K;
+  const float* S;       // [b, H, DV, DK], not modified
+  const void* q;        // drafts [b, K, H, ...]
+  const void* k;
+  const void* v;
+  const float* alpha;
+  const float* beta;
+  float scale;
+  float* snap;          // [b, K, H, DV, DK]: the state after drafts 0..i
+  float* o;             // [b, K, H, DV]
+};
+
+// Conventional speculative verify, the baseline the pointer method replaces:
+// the recurrence runs through the K drafts in order and the state after each
+// draft is written out as a snapshot (from which accept restores the state
+// of the accepted prefix). Same row layout as the conventional step: one warp
+// per 8 rows of one head, 8 lanes per row; the rows stay in registers across
+// the drafts.
+template <int DK, typename TI, bool KDA>
+__global__ void __launch_bounds__(kThreads) delta_conventional_verify_kernel(const DConvSpec a) {
+  constexpr int CH = DK / 32;  // float4 chunks per lane
+  const int lane = threadIdx.x & 31;
+  const long long gw = (long long)blockIdx.x * kWarps + (threadIdx.x >> 5);
+  const int groups = a.DV / 8, H = a.H, K = a.K;
+  if (gw >= (long long)a.batch * H * groups) return;
+  const long long t = gw / groups;  // seq * H + h
+  const long long seq = t / H, h = t - seq * H;
+  const int r0 = (int)(gw - t * groups) * 8;
+  const int sub = lane >> 3, c8 = lane & 7;
+  float4 sv[2][CH];
+#pragma unroll
+  for (int st = 0; st < 2; ++st) {
+    const float4* row = reinterpret_cast<const float4*>(a.S + (t * a.DV + r0 + st * 4 + sub) * DK);
+#pragma unroll
+    for (int m = 0; m < CH; ++m) sv[st][m] = row[c8 + 8 * m];
+  }
+  for (int i = 0; i < K; ++i) {
+    const long long ti = (seq * K + i) * H + h;  // draft i of this head
+    const TI* qi = reinterpret_cast<const TI*>(a.q) + ti * DK;
+    const TI* ki = reinterpret_cast<const TI*>(a.k) + ti * DK;
+    const TI* vi = reinterpret_cast<const TI*>(a.v) + ti * a.DV;
+    float kq[CH][4], qq[CH][4], al[CH][4];
+    float kqdot = 0.f;
+#pragma unroll
+    for (int m = 0; m < CH; ++m)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int c = (c8 + 8 * m) * 4 + e;
+        kq[m][e] = to_f(ki[c]);
+        qq[m][e] = to_f(qi[c]);
+        al[m][e] = KDA ? a.alpha[ti * DK + c] : a.alpha[ti];
+        kqdot = fmaf(kq[m][e], qq[m][e], kqdot);
+      }
+    kqdot += __shfl_xor_sync(kFull, kqdot, 1);
+    kqdot += __shfl_xor_sync(kFull, kqdot, 2);
+    kqdot += __shfl_xor_sync(kFull, kqdot, 4);
+    const float be = a.beta[ti];
+#pragma unroll
+    for (int st = 0; st < 2; ++st) {
+      const int r = r0 + st * 4 + sub;
+      float d1 = 0.f, d2 = 0.f;
+#pragma unroll
+      for (int m = 0; m < CH; ++m) {
+        sv[st][m].x *= al[m][0];
+        sv[st][m].y *= al[m][1];
+        sv[st][m].z *= al[m][2];
+        sv[st][m].w *= al[m][3];
+        d1 = fmaf(sv[st][m].x, kq[m][0], d1);
+        d1 = fmaf(sv[st][m].y, kq[m][1], d1);
+        d1 = fmaf(sv[st][m].z, kq[m][2], d1);
+        d1 = fmaf(sv[st][m].w, kq[m][3], d1);
+        d2 = fmaf(sv[st][m].x, qq[m][0], d2);
+        d2 = fmaf(sv[st][m].y, qq[m][1], d2);
+        d2 = fmaf(sv[st][m].z, qq[m][2], d2);
+        d2 = fmaf(sv[st][m].w, qq[m][3], d2);
+      }
+#pragma unroll
+      for (int o = 1; o <= 4; o <<= 1) {
+        d1 += __shfl_xor_sync(kFull, d1, o);
+        d2 += __shfl_xor_sync(kFull, d2, o);
+      }
+      const float c = be * (to_f(vi[r]) - d1);
+      float4* snap = reinterpret_cast<float4*>(a.snap + (ti * a.DV + r) * DK);
+#pragma unroll
+      for (int m = 0; m < CH; ++m) {
+        sv[st][m] = make_float4(fmaf(c, kq[m][0], sv[st][m].x), fmaf(c, kq[m][1], sv[st][m].y),
+                                fmaf(c, kq[m][2], sv[st][m].z), fmaf(c, kq[m][3], sv[st][m].w));
+        snap[c8 + 8 * m] = sv[st][m];
+      }
+      if (c8 == 0) a.o[ti * a.DV + r] = a.scale * fmaf(c, kqdot, d2);
+    }
+  }
+}
+
 // State rows per unit: about 16 KB (at least 32 rows, dividing DV).
 int fused_rows(int DK, int ts, int DV) {
   int RB = std::max(32, 16384 / (DK * ts) / 32 * 32);
@@ -1020,6 +1115,26 @@ cudaError_t launch_delta_fold(const replayssm_dims& d, const replayssm_state& s,
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   kern<<<grid, kDFoldThreads, smem, st>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_delta_conventional_verify(const replayssm_dims& d, const float* S, int K,
+                                             const void* q, const void* k, const void* v,
+                                             const float* alpha, const float* beta, float scale,
+                                             float* snap, float* o, cudaStream_t st) {
+  DConvSpec a{d.batch, d.heads, d.dv, K, S, q, k, v, alpha, beta, scale, snap, o};
+  const long long warps = (long long)d.batch * d.heads * (d.dv / 8);
+  const unsigned grid = (unsigned)((warps + kWarps - 1) / kWarps);
+  const bool in16 = d.in_dtype == REPLAYSSM_BF16;
+  const bool kda = d.kind == REPLAYSSM_KDA;
+  void (*kern)(const DConvSpec);
+  if (d.dk == 128)
+    kern = in16 ? (kda ? delta_conventional_verify_kernel<128, bf16, true> : delta_conventional_verify_kernel<128, bf16, false>)
+                : (kda ? delta_conventional_verify_kernel<128, float, true> : delta_conventional_verify_kernel<128, float, false>);
+  else
+    kern = in16 ? (kda ? delta_conventional_verify_kernel<64, bf16, true> : delta_conventional_verify_kernel<64, bf16, false>)
+                : (kda ? delta_conventional_verify_kernel<64, float, true> : delta_conventional_verify_kernel<64, float, false>);
+  kern<<<grid, kThreads, 0, st>>>(a);
   return cudaGetLastError();
 }
 

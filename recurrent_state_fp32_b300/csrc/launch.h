@@ -57,6 +57,13 @@ cudaError_t launch_delta_conventional(const replayssm_dims& d, float* S, const v
                                       const void* k, const void* v, const float* alpha,
                                       const float* beta, float scale, float* o, cudaStream_t st);
 
+cudaError_t launch_delta_conventional_verify(const replayssm_dims& d, const float* S, int K,
+                                             const void* q, const void* k, const void* v,
+                                             const float* alpha, const float* beta, float scale,
+                                             float* snap, float* o, cudaStream_t st);
+cudaError_t launch_conventional_accept(const replayssm_dims& d, float* S, const float* snap,
+                                       const int32_t* m, int K, int32_t* status, cudaStream_t st);
+
 cudaError_t launch_accept(const replayssm_dims& d, const replayssm_state& s, const int32_t* m,
                           int K, cudaStream_t st);
 cudaError_t launch_refresh(const replayssm_dims& d, const replayssm_state& s, cudaStream_t st);

@@ -154,3 +154,21 @@ def test_workspace_size():
     assert _abi.lib.replayssm_workspace_bytes(None, 1) == 0
     assert m2_decode(dims(), state(work=None)) == _abi.ERR_INVALID_ARG
     assert m2_decode(dims(), state(work=MISALIGNED)) == _abi.ERR_MISALIGNED
+
+
+def test_conventional_spec_arguments():
+    r = ctypes.byref
+    g = dims(kind=_abi.GDN, dv=128)
+    cv = _abi.lib.replayssm_conventional_gdn_verify
+    assert cv(r(g), FAKE, 0, FAKE, FAKE, FAKE, FAKE, FAKE, 1.0, FAKE, FAKE, None) == _abi.ERR_INVALID_ARG
+    assert cv(r(g), FAKE, 9, FAKE, FAKE, FAKE, FAKE, FAKE, 1.0, FAKE, FAKE, None) == _abi.ERR_INVALID_ARG
+    assert cv(r(dims()), FAKE, 4, FAKE, FAKE, FAKE, FAKE, FAKE, 1.0, FAKE, FAKE, None) == _abi.ERR_INVALID_ARG
+    assert cv(r(g), FAKE, 4, FAKE, FAKE, FAKE, FAKE, FAKE, 1.0, None, FAKE, None) == _abi.ERR_INVALID_ARG
+    assert cv(r(g), MISALIGNED, 4, FAKE, FAKE, FAKE, FAKE, FAKE, 1.0, FAKE, FAKE, None) == _abi.ERR_MISALIGNED
+    g0 = dims(kind=_abi.GDN, batch=0, dv=128)
+    assert cv(r(g0), FAKE, 4, FAKE, FAKE, FAKE, FAKE, FAKE, 1.0, FAKE, FAKE, None) == _abi.OK
+    ca = _abi.lib.replayssm_conventional_accept
+    assert ca(r(g), FAKE, FAKE, None, 4, None, None) == _abi.ERR_INVALID_ARG
+    assert ca(r(g), FAKE, FAKE, FAKE, 0, None, None) == _abi.ERR_INVALID_ARG
+    assert ca(r(g), FAKE, FAKE, FAKE, 4, MISALIGNED, None) == _abi.ERR_MISALIGNED
+    assert ca(r(g0), FAKE, FAKE, FAKE, 4, None, None) == _abi.OK

@@ -72,3 +72,50 @@ def test_full_size_sampled():
                              in_dtype="bf16", seed=4)
     s = Session("gdn", wl, "bf16", seqs=[0, 311, 511], heads=[0, 16, 31])
     run(s, 24, 4, check_every=7)
+
+
+@pytest.mark.parametrize("kind,dk,dv,in_dtype", [("gdn", 128, 128, "bf16"), ("kda", 64, 96, "f32")])
+def test_conventional_snapshot_verify_and_accept(kind, dk, dv, in_dtype):
+    """The baseline spec path: per-draft snapshots and outputs against the oracle's
+    conventional recurrence stepped through the drafts; accept restores snapshot m - 1."""
+    import torch
+
+    from gpu_harness import dev, f32_close, host
+    from oracle import recurrences as rec
+    from recurrent_state_fp32_b300 import api
+
+    b, H, K, seed = 5, 3, 4, 23
+    dims = api.LayerDims(kind, b, H, dk=dk, dv=dv, window=16, in_dtype=in_dtype)
+    S0 = synth.delta_initial_state(seed, b, H, dv, dk)
+    drafts = synth.spec_draft_inputs(seed, 0, b, K, H, dk, dv, kind, in_dtype)
+    vt = torch.bfloat16 if in_dtype == "bf16" else torch.float32
+    d = {n: dev(v, vt if n in ("q", "k", "v") else torch.float32) for n, v in drafts.items()}
+    S = dev(S0)
+    snaps = torch.empty((b, K, H, dv, dk), device="cuda")
+    o = torch.empty((b, K, H, dv), device="cuda")
+    api.conventional_gdn_verify(dims, S, K, d["q"], d["k"], d["v"], d["alpha"], d["beta"], 0.8,
+                                snaps, o)
+    torch.cuda.synchronize()
+    assert np.array_equal(host(S), S0), "verify must not modify S"
+    ref = np.asarray(S0, np.float64)
+    for i in range(K):
+        ref, o_ref = rec.delta_step(ref, drafts["q"][:, i], drafts["k"][:, i], drafts["v"][:, i],
+                                    drafts["alpha"][:, i], drafts["beta"][:, i], scale=0.8)
+        f32_close(host(o[:, i]), o_ref, f"draft {i} output")
+        f32_close(host(snaps[:, i]), ref, f"draft {i} snapshot")
+    m = np.array([0, 1, 2, 4, 3], np.int32)
+    status = torch.zeros(b, dtype=torch.int32, device="cuda")
+    api.conventional_accept(dims, S, snaps, dev(m, torch.int32), K, status)
+    got, sn = host(S), host(snaps)
+    for q in range(b):
+        want = S0[q] if m[q] == 0 else sn[q, m[q] - 1]
+        assert np.array_equal(got[q], want), f"sequence {q}: accept of {m[q]} drafts"
+    assert int(status.abs().sum()) == 0
+    before = host(S)
+    api.conventional_accept(dims, S, snaps, dev(np.array([5, -1, 0, 4, 1], np.int32), torch.int32),
+                            K, status)
+    st = host(status).astype(np.int64)
+    assert st[0] & 2 and st[1] & 2 and not st[2:].any()
+    after = host(S)
+    assert np.array_equal(after[:2], before[:2]), "a refused accept leaves S unchanged"
+    assert np.array_equal(after[3], sn[3, 3]) and np.array_equal(after[4], sn[4, 0])
