@@ -173,9 +173,11 @@ class ReplayOracle:
 
         Draft i sees the committed entries and drafts 0..i. Nothing is
         committed. Sequences with len + K > W are refused (RING_FULL, NaN).
+        Any layer kind: the pointer rollback applies to every SSM layer type
+        the pages name ("NVIDIA y Princeton aceleran…", paragraph 3;
+        "NVIDIA présente ReplaySSM…", "Pourquoi les hybrides sont devenus la
+        norme").
         """
-        if self.kind == "mamba2":
-            raise NotImplementedError("speculative verify is built for the delta kinds")
         ok = self.len + K <= self.W
         self.status[~ok] |= RING_FULL
         outs, states = [], []

@@ -452,6 +452,29 @@ def pin_rollback_equals_accepted_prefix():
         spec.consolidate(1, force=True)
         _close(spec.ckpt, plain.committed, 1e-11, f"{kind} checkpoint after rollback")
         assert np.all(spec.status == 0)
+    # Mamba-2: the same invariant with its own recurrence
+    r = _rng(52)
+    b, H, G, P, N, W, K, R = 3, 4, 2, 3, 5, 16, 4, 12
+    A, D = -r.uniform(1.0, 16.0, H), r.standard_normal(H)
+    h0 = r.standard_normal((b, H, P, N))
+    spec = om.ReplayOracle("mamba2", h0, W, A=A, D=D, groups=G)
+    plain = om.ReplayOracle("mamba2", h0, W, A=A, D=D, groups=G)
+    for rnd in range(R):
+        toks = m2_tokens(r, b, H, G, P, N, K)
+        drafts = {k: np.stack([t[k] for t in toks], axis=1) for k in toks[0]}
+        m = r.integers(0, K + 1, size=b)
+        spec.consolidate(K)
+        o = spec.spec_verify(K, drafts)
+        spec.accept(m, K)
+        for s in range(b):
+            one = om.ReplayOracle("mamba2", plain.committed[s:s + 1], W, A=A, D=D, groups=G)
+            for i in range(m[s]):
+                y = one.decode({k: v[s:s + 1] for k, v in toks[i].items()})
+                _close(o[s, i], y[0], 1e-11, f"mamba2 round {rnd} seq {s} draft {i}")
+            plain.committed[s] = one.committed[0]
+    spec.consolidate(1, force=True)
+    _close(spec.ckpt, plain.committed, 1e-11, "mamba2 checkpoint after rollback")
+    assert np.all(spec.status == 0)
 
 
 def pin_status_and_refusal():
