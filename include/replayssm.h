@@ -190,11 +190,32 @@ REPLAYSSM_API replayssm_status replayssm_consolidate(
  * drafts 0..i, all K outputs from one read of the checkpoint. Draft fields
  * are [b, K, H, ...] (alpha [b, K, H] or [b, K, H, d_k], beta [b, K, H]).
  * Precondition len + K <= W (consolidate with k_next = K first), else
- * RING_FULL and the sequence is untouched. Mamba-2: REPLAYSSM_ERR_UNSUPPORTED.
+ * RING_FULL and the sequence is untouched. Mamba-2 layers use
+ * replayssm_mamba2_spec_verify (here: REPLAYSSM_ERR_UNSUPPORTED).
  */
 REPLAYSSM_API replayssm_status replayssm_spec_verify(
     const replayssm_dims* dims, const replayssm_state* state, int32_t K, const void* q,
     const void* k, const void* v, const float* alpha, const float* beta, float scale, float* o,
+    void* stream);
+
+/*
+ * Speculative verify for Mamba-2 layers (same passages as
+ * replayssm_spec_verify; the pointer rollback applies to every SSM layer
+ * type of "NVIDIA présente ReplaySSM…", "Pourquoi les hybrides sont devenus
+ * la norme"). Writes draft i (i < K) of each sequence into slot
+ * (head + len + i) mod W without committing it and outputs, for the state
+ * after the committed entries and drafts 0..i, all from one read of the
+ * checkpoint:
+ *   y[:, i] = (prod dA) (h_c C_i) + sum_j w_j (C_i . B_j) x_j + D x_i.
+ * Drafts: x [b, K, H, P], B and C [b, K, G, N] (in_dtype), dt [b, K, H] f32;
+ * y [b, K, H, P] f32; A, D f32 [H]. state->work must hold
+ * replayssm_workspace_bytes(dims, K) bytes. 1 <= K <= min(8, W).
+ * Precondition len + K <= W (consolidate with k_next = K first), else
+ * RING_FULL and the sequence is untouched. Accept with replayssm_accept.
+ */
+REPLAYSSM_API replayssm_status replayssm_mamba2_spec_verify(
+    const replayssm_dims* dims, const replayssm_state* state, int32_t K, const float* A,
+    const float* D, const void* x, const void* B, const void* C, const float* dt, float* y,
     void* stream);
 
 /*

@@ -175,6 +175,12 @@ def spec_verify(dims, state, K, q, k, v, alpha, beta, scale, o, stream=None):
           _ptr(beta), float(scale), _ptr(o), _stream(stream))
 
 
+def mamba2_spec_verify(dims, state, K, A, D, x, B, C, dt, y, stream=None):
+    d, s = _refs(dims, state)
+    _call("replayssm_mamba2_spec_verify", d, s, int(K), _ptr(A), _ptr(D), _ptr(x), _ptr(B),
+          _ptr(C), _ptr(dt), _ptr(y), _stream(stream))
+
+
 def accept(dims, state, m, K, stream=None):
     d, s = _refs(dims, state)
     _call("replayssm_accept", d, s, _ptr(m), int(K), _stream(stream))

@@ -301,6 +301,23 @@ REPLAYSSM_API replayssm_status replayssm_spec_verify(
                                         static_cast<cudaStream_t>(stream)));
 }
 
+REPLAYSSM_API replayssm_status replayssm_mamba2_spec_verify(
+    const replayssm_dims* dims, const replayssm_state* state, int32_t K, const float* A,
+    const float* D, const void* x, const void* B, const void* C, const float* dt, float* y,
+    void* stream) {
+  RS_TRY(check_dims(dims));
+  if (dims->kind != REPLAYSSM_MAMBA2) return REPLAYSSM_ERR_INVALID_ARG;
+  if (K < 1 || K > 8 || K > dims->window) return REPLAYSSM_ERR_INVALID_ARG;
+  RS_TRY(check_state(dims, state));
+  RS_TRY(check_ptr(A));
+  RS_TRY(check_ptr(D));
+  RS_TRY(check_mamba2_token(x, B, C, dt));
+  RS_TRY(check_ptr(y));
+  if (dims->batch == 0) return REPLAYSSM_OK;
+  return finish(rs::launch_mamba2_verify(*dims, *state, K, A, D, x, B, C, dt, y,
+                                         static_cast<cudaStream_t>(stream)));
+}
+
 REPLAYSSM_API replayssm_status replayssm_accept(const replayssm_dims* dims,
                                                 const replayssm_state* state, const int32_t* m,
                                                 int32_t K, void* stream) {

@@ -37,6 +37,9 @@ const DeviceInfo& device_info();
 cudaError_t launch_mamba2_decode(const replayssm_dims& d, const replayssm_state& s, const float* A,
                                  const float* D, const void* x, const void* B, const void* C,
                                  const float* dt, float* y, cudaStream_t st);
+cudaError_t launch_mamba2_verify(const replayssm_dims& d, const replayssm_state& s, int K,
+                                 const float* A, const float* D, const void* x, const void* B,
+                                 const void* C, const float* dt, float* y, cudaStream_t st);
 cudaError_t launch_mamba2_fold(const replayssm_dims& d, const replayssm_state& s, const float* A,
                                int k_next, int force, cudaStream_t st);
 cudaError_t launch_mamba2_conventional(const replayssm_dims& d, float* S, const float* A,

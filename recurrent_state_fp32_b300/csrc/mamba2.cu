@@ -331,6 +331,157 @@ __global__ void __launch_bounds__(32 * kPrepWarps) mamba2_prep_kernel(const M2Pr
     arrive_and_finish(a.sync + cur_seq, v1 - seq_first, H, [&] { a.len[cur_seq] = len + 1; });
 }
 
+// -------------------------------------------------------------- verify prep
+
+struct M2VPrep {
+  int batch, H, G, P, W, K;
+  const float* A;
+  const float* D;
+  const void* x;       // drafts [b, K, H, P]
+  const void* B;       // [b, K, G, N]
+  const void* C;       // [b, K, G, N]
+  const float* dt;     // [b, K, H]
+  void* ring_x;
+  void* ring_B;
+  void* ring_C;
+  float* ring_dt;
+  int32_t* head;
+  int32_t* len;
+  int32_t* status;
+  float* work;         // [b, K, H, wrow]: buffer terms [0, P), decay at P
+  int wrow;
+  int32_t* flags;      // [b]
+};
+
+// Preparation of a Mamba-2 speculative verify, one warp per head. Entry
+// j < len is ring slot (head + j) mod W; entry len + i is draft i. For draft
+// i (entries 0..len + i visible), with dA_l = exp(dt_l A_h):
+//   decay_i    = prod_{l <= len+i} dA_l
+//   extra_i[p] = sum_{j <= len+i} dt_j prod_{j < l <= len+i} dA_l (C_i . B_j) x_j[p] + D_h x_i[p]
+// go to work row (seq, i, h). The drafts are appended at slots
+// (head + len + i) mod W; len is unchanged (accept moves it). A sequence
+// without room for K drafts gets a status bit and flags[seq] = 0.
+template <int N, typename TI>
+__global__ void __launch_bounds__(256) mamba2_verify_prep_kernel(const M2VPrep a) {
+  constexpr int kNL = N / 32;
+  const int lane = threadIdx.x & 31;
+  const int H = a.H, G = a.G, P = a.P, W = a.W, K = a.K, hpg = H / G, Wd = ring_wd(W);
+  const long long heads = (long long)a.batch * H;
+  const long long nw = (long long)gridDim.x * (blockDim.x >> 5);
+  const TI* xin = reinterpret_cast<const TI*>(a.x);
+  const TI* Bin = reinterpret_cast<const TI*>(a.B);
+  const TI* Cin = reinterpret_cast<const TI*>(a.C);
+  const TI* rB = reinterpret_cast<const TI*>(a.ring_B);
+  const TI* rx = reinterpret_cast<const TI*>(a.ring_x);
+  griddep_launch_dependents();  // the stream kernel may start streaming state rows
+  for (long long v = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); v < heads; v += nw) {
+    const int seq = (int)(v / H), h = (int)(v - (long long)seq * H), g = h / hpg;
+    int l = 0, hh = 0;
+    if (lane == 0) {
+      l = a.len[seq];
+      hh = a.head[seq];
+    }
+    const int len = __shfl_sync(kFull, l, 0), hd = __shfl_sync(kFull, hh, 0);
+    const bool ok = pointers_ok(hd, len, W) && len + K <= W;
+    if (h == 0 && lane == 0) {
+      a.flags[seq] = ok ? 1 : 0;
+      if (!ok)
+        atomicOr(a.status + seq, pointers_ok(hd, len, W) ? REPLAYSSM_SEQ_RING_FULL
+                                                         : REPLAYSSM_SEQ_BAD_POINTER);
+    }
+    if (!ok) continue;
+    const float Ah = a.A[h], Dh = a.D[h];
+    auto slot_of = [&](int j) { return hd + j < W ? hd + j : hd + j - W; };
+    auto entry_dt = [&](int j) -> float {
+      if (j < len) return a.ring_dt[(size_t)v * Wd + slot_of(j)];
+      if (j < len + K) return a.dt[((size_t)seq * K + (j - len)) * H + h];
+      return 0.f;
+    };
+    auto entry_B = [&](int j) -> const TI* {
+      return j < len ? rB + (((size_t)seq * W + slot_of(j)) * G + g) * N
+                     : Bin + (((size_t)seq * K + (j - len)) * G + g) * N;
+    };
+    auto entry_x = [&](int j) -> const TI* {
+      return j < len ? rx + ((size_t)v * W + slot_of(j)) * P
+                     : xin + (((size_t)seq * K + (j - len)) * H + h) * P;
+    };
+    const float dtv0 = entry_dt(lane), dtv1 = entry_dt(lane + 32);
+    for (int i = 0; i < K; ++i) {
+      const int top = len + i;
+      // C_i . B_j for entries 0..top: lane j holds entries j and j + 32
+      float cf[kNL];
+#pragma unroll
+      for (int q = 0; q < kNL; ++q) cf[q] = to_f(Cin[(((size_t)seq * K + i) * G + g) * N + lane + 32 * q]);
+      float cb0 = 0.f, cb1 = 0.f;
+      for (int j0 = 0; j0 <= top; j0 += 16) {
+        float vv[16];
+#pragma unroll
+        for (int q = 0; q < 16; ++q) {
+          const TI* Bj = entry_B(min(j0 + q, top));
+          float pp = 0.f;
+#pragma unroll
+          for (int k = 0; k < kNL; ++k) pp = fmaf(cf[k], to_f(Bj[lane + 32 * k]), pp);
+          vv[q] = pp;
+        }
+        float tot = reduce_scatter<16>(vv, lane);
+        tot += __shfl_xor_sync(kFull, tot, 16);  // every lane: entry j0 + (lane & 15)
+        const float t0 = __shfl_sync(kFull, tot, (lane - j0) & 15);
+        const float t1 = __shfl_sync(kFull, tot, (lane + 32 - j0) & 15);
+        if (lane >= j0 && lane < j0 + 16) cb0 = t0;
+        if (lane + 32 >= j0 && lane + 32 < j0 + 16) cb1 = t1;
+      }
+      // weights from suffix sums of dt over entries 0..top
+      const float d0 = lane <= top ? dtv0 : 0.f, d1 = lane + 32 <= top ? dtv1 : 0.f;
+      float inc0 = d0, inc1 = d1;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const float t0 = __shfl_down_sync(kFull, inc0, o), t1 = __shfl_down_sync(kFull, inc1, o);
+        if (lane + o < 32) {
+          inc0 += t0;
+          inc1 += t1;
+        }
+      }
+      inc0 += __shfl_sync(kFull, inc1, 0);
+      const float total = __shfl_sync(kFull, inc0, 0);
+      float c0 = lane <= top ? d0 * __expf(Ah * (inc0 - d0)) * cb0 : 0.f;
+      float c1 = lane + 32 <= top ? d1 * __expf(Ah * (inc1 - d1)) * cb1 : 0.f;
+      if (lane == top) c0 += Dh;
+      if (lane + 32 == top) c1 += Dh;
+      float* wrow = a.work + (((size_t)seq * K + i) * H + h) * a.wrow;
+      for (int p0 = 0; p0 < P; p0 += 64) {  // every lane runs every iteration
+        const int p = p0 + 2 * lane;
+        const bool act = p < P;
+        float e0 = 0.f, e1 = 0.f;
+        for (int j = 0; j <= top; ++j) {
+          const float c = __shfl_sync(kFull, j < 32 ? c0 : c1, j & 31);
+          if (act) {
+            const float2 xv = load2<TI>(entry_x(j) + p);
+            e0 = fmaf(c, xv.x, e0);
+            e1 = fmaf(c, xv.y, e1);
+          }
+        }
+        if (act) *reinterpret_cast<float2*>(wrow + p) = make_float2(e0, e1);
+      }
+      if (lane == 0) wrow[P] = __expf(Ah * total);
+    }
+    // append the drafts: x rows and dt of this head, B and C of its group
+    for (int i = 0; i < K; ++i) {
+      const int slot = slot_of(len + i);
+      const size_t xb = (size_t)P * sizeof(TI);
+      block_copy_warp(reinterpret_cast<unsigned char*>(a.ring_x) + ((size_t)v * W + slot) * xb,
+                      reinterpret_cast<const unsigned char*>(xin) + (((size_t)seq * K + i) * H + h) * xb,
+                      (int)xb, lane);
+      if (lane == 0) a.ring_dt[(size_t)v * Wd + slot] = a.dt[((size_t)seq * K + i) * H + h];
+      if (h - g * hpg == 0) {
+        const size_t src = (((size_t)seq * K + i) * G + g) * N, dst = (((size_t)seq * W + slot) * G + g) * N;
+        for (int c = lane; c < N; c += 32) reinterpret_cast<TI*>(a.ring_B)[dst + c] = Bin[src + c];
+        if (a.ring_C)
+          for (int c = lane; c < N; c += 32) reinterpret_cast<TI*>(a.ring_C)[dst + c] = Cin[src + c];
+      }
+    }
+  }
+}
+
 constexpr int kFoldThreads = 256;
 constexpr int kFoldRows = 8;  // contiguous state rows per thread (loads in flight)
 
@@ -628,6 +779,57 @@ cudaError_t launch_mamba2_decode(const replayssm_dims& d, const replayssm_state&
   }
   if (rd16) return in16 ? launch_stream<64, bf16, bf16, 1>(sa, st) : launch_stream<64, bf16, float, 1>(sa, st);
   return in16 ? launch_stream<64, float, bf16, 1>(sa, st) : launch_stream<64, float, float, 1>(sa, st);
+}
+
+cudaError_t launch_mamba2_verify(const replayssm_dims& d, const replayssm_state& s, int K,
+                                 const float* A, const float* D, const void* x, const void* B,
+                                 const void* C, const float* dt, float* y, cudaStream_t st) {
+  const WorkLayout wl(d, K);
+  const bool in16 = d.in_dtype == REPLAYSSM_BF16;
+  M2VPrep p{d.batch, d.heads, d.groups, d.dv, d.window, K, A, D, x, B, C, dt,
+            s.ring_x, s.ring_B, s.ring_C, s.ring_dt, s.ring_head, s.ring_len, s.status,
+            s.work, wl.row, wl.flags(s.work)};
+  const long long heads = (long long)d.batch * d.heads;
+  const int grid = (int)std::min<long long>((heads + 7) / 8, (long long)device_info().sms * 8);
+  if (d.dk == 128) {
+    if (in16) mamba2_verify_prep_kernel<128, bf16><<<grid, 256, 0, st>>>(p);
+    else mamba2_verify_prep_kernel<128, float><<<grid, 256, 0, st>>>(p);
+  } else {
+    if (in16) mamba2_verify_prep_kernel<64, bf16><<<grid, 256, 0, st>>>(p);
+    else mamba2_verify_prep_kernel<64, float><<<grid, 256, 0, st>>>(p);
+  }
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  // Stream: y_i = decay_i * (S C_i) + extra_i, C_i straight from the drafts.
+  StreamArgs sa{};
+  sa.batch = d.batch;
+  sa.H = d.heads;
+  sa.P = d.dv;
+  sa.K = K;
+  sa.S = s.S_read ? (const void*)s.S_read : (const void*)s.S_ckpt;
+  sa.out = y;
+  sa.work = s.work;
+  sa.wrow = wl.row;
+  sa.vec_off = -1;
+  sa.extra_off = 0;
+  sa.scale_off = d.dv;
+  sa.flags = wl.flags(s.work);
+  sa.vin = C;
+  sa.G = d.groups;
+  sa.status = s.status;
+  const bool rd16 = s.S_read != nullptr;
+#define RS_VSTREAM(KM_)                                                                        \
+  if (d.dk == 128) {                                                                           \
+    if (rd16) return in16 ? launch_stream<128, bf16, bf16, KM_>(sa, st) : launch_stream<128, bf16, float, KM_>(sa, st); \
+    return in16 ? launch_stream<128, float, bf16, KM_>(sa, st) : launch_stream<128, float, float, KM_>(sa, st);       \
+  }                                                                                            \
+  if (rd16) return in16 ? launch_stream<64, bf16, bf16, KM_>(sa, st) : launch_stream<64, bf16, float, KM_>(sa, st);   \
+  return in16 ? launch_stream<64, float, bf16, KM_>(sa, st) : launch_stream<64, float, float, KM_>(sa, st);
+  if (K <= 4) {
+    RS_VSTREAM(4)
+  }
+  RS_VSTREAM(8)
+#undef RS_VSTREAM
 }
 
 cudaError_t launch_mamba2_fold(const replayssm_dims& d, const replayssm_state& s, const float* A,

@@ -40,7 +40,7 @@ struct StreamArgs {
   int extra_off;        // additive-term offset in the work row
   int scale_off;        // scale offset in the work row; < 0: scale 1
   const int32_t* flags; // per sequence: nonzero = write outputs
-  const void* vin;      // vector input [b, G, N] when vec_off < 0
+  const void* vin;      // vector input [b, K, G, N] when vec_off < 0
   int G;                // groups of vin (head h uses group h / (H / G))
   int32_t* status;      // timeout reporting
 };
@@ -158,7 +158,7 @@ __global__ void __launch_bounds__(kStreamMaxThreads, 1) stream_kernel(const Stre
           }
         } else {
           const TV* vin = reinterpret_cast<const TV*>(a.vin) +
-                          ((size_t)seq * a.G + h / (H / a.G)) * N + c0;
+                          (((size_t)seq * K + k) * a.G + h / (H / a.G)) * N + c0;
 #pragma unroll
           for (int e = 0; e < kE; ++e) vec[k][e] = to_f(vin[e]);
         }

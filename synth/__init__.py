@@ -14,6 +14,7 @@ from .inputs import (  # noqa: F401
     bf16_round,
     delta_initial_state,
     delta_step_inputs,
+    mamba2_draft_inputs,
     mamba2_initial_state,
     mamba2_params,
     mamba2_step_inputs,

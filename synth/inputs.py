@@ -77,6 +77,7 @@ class Mamba2Workload:
     steps: int = 64
     in_dtype: str = "bf16"
     seed: int = 1
+    K: int = 1  # drafts per speculative round
 
     @property
     def name(self) -> str:
@@ -182,6 +183,22 @@ def spec_draft_inputs(seed: int, rnd: int, batch: int, K: int, heads: int, dk: i
                       kind: str = "gdn", in_dtype: str = "bf16"):
     """K draft tokens per sequence for one speculative round: fields [b, K, H, ...]."""
     return _delta_token(_rng(seed, _DRAFTS, rnd), (batch, K), heads, dk, dv, kind, in_dtype)
+
+
+def mamba2_draft_inputs(seed: int, rnd: int, batch: int, K: int, heads: int, groups: int,
+                        P: int, N: int, dt_bias: np.ndarray, in_dtype: str = "bf16"):
+    """K Mamba-2 draft tokens per sequence for one speculative round:
+    x [b, K, H, P], B and C [b, K, G, N], dt [b, K, H] (same distributions as
+    a decode token)."""
+    r = _rng(seed, _DRAFTS, rnd)
+    x = r.standard_normal((batch, K, heads, P), dtype=np.float32)
+    inv = np.float32(1.0 / np.sqrt(N))
+    B = r.standard_normal((batch, K, groups, N), dtype=np.float32) * inv
+    C = r.standard_normal((batch, K, groups, N), dtype=np.float32) * inv
+    dt_raw = r.standard_normal((batch, K, heads))
+    dt = np.clip(_softplus(dt_raw + dt_bias.astype(np.float64)), 1e-3, 0.1)
+    return {"x": _vec(x, in_dtype), "B": _vec(B, in_dtype), "C": _vec(C, in_dtype),
+            "dt": dt.astype(np.float32)}
 
 
 def accept_counts(seed: int, rnd: int, batch: int, K: int) -> np.ndarray:

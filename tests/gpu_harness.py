@@ -153,13 +153,23 @@ class Session:
 
     def verify(self, r, K):
         wl = self.wl
-        d = synth.spec_draft_inputs(wl.seed, r, wl.batch, K, wl.heads, wl.dk, wl.dv, self.kind,
-                                    wl.in_dtype)
-        g = self._to_dev(d)
-        o = torch.full((wl.batch, K, wl.heads, wl.dv), float("nan"), device=DEV)
-        api.spec_verify(self.dims, self.state, K, g["q"], g["k"], g["v"], g["alpha"], g["beta"],
-                        self.scale, o)
-        sub = {k: np.take(v[self.seqs], self.heads, axis=2) for k, v in d.items()}
+        if self.kind == "mamba2":
+            d = synth.mamba2_draft_inputs(wl.seed, r, wl.batch, K, wl.heads, wl.groups, wl.P,
+                                          wl.N, self.dt_bias, wl.in_dtype)
+            g = self._to_dev(d)
+            o = torch.full((wl.batch, K, wl.heads, wl.P), float("nan"), device=DEV)
+            api.mamba2_spec_verify(self.dims, self.state, K, self.dA, self.dD, g["x"], g["B"],
+                                   g["C"], g["dt"], o)
+            sub = {k: v[self.seqs] if k in ("B", "C") else np.take(v[self.seqs], self.heads, axis=2)
+                   for k, v in d.items()}
+        else:
+            d = synth.spec_draft_inputs(wl.seed, r, wl.batch, K, wl.heads, wl.dk, wl.dv,
+                                        self.kind, wl.in_dtype)
+            g = self._to_dev(d)
+            o = torch.full((wl.batch, K, wl.heads, wl.dv), float("nan"), device=DEV)
+            api.spec_verify(self.dims, self.state, K, g["q"], g["k"], g["v"], g["alpha"],
+                            g["beta"], self.scale, o)
+            sub = {k: np.take(v[self.seqs], self.heads, axis=2) for k, v in d.items()}
         ref = self.oracle.spec_verify(K, sub)
         got = host(o)[self.seqs][:, :, self.heads]
         self.compare_out(got, ref, f"verify round {r}")

@@ -172,3 +172,20 @@ def test_conventional_spec_arguments():
     assert ca(r(g), FAKE, FAKE, FAKE, 0, None, None) == _abi.ERR_INVALID_ARG
     assert ca(r(g), FAKE, FAKE, FAKE, 4, MISALIGNED, None) == _abi.ERR_MISALIGNED
     assert ca(r(g0), FAKE, FAKE, FAKE, 4, None, None) == _abi.OK
+
+
+def test_mamba2_spec_arguments():
+    r = ctypes.byref
+    mv = _abi.lib.replayssm_mamba2_spec_verify
+    m = dims()
+    assert mv(r(dims(kind=_abi.GDN, dv=128)), r(state()), 4, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE,
+              None) == _abi.ERR_INVALID_ARG
+    assert mv(r(m), r(state()), 0, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None) == _abi.ERR_INVALID_ARG
+    assert mv(r(m), r(state()), 9, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None) == _abi.ERR_INVALID_ARG
+    assert mv(r(dims(window=3)), r(state()), 4, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE,
+              None) == _abi.ERR_INVALID_ARG
+    assert mv(r(m), r(state()), 4, None, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None) == _abi.ERR_INVALID_ARG
+    assert mv(r(m), r(state()), 4, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, MISALIGNED,
+              None) == _abi.ERR_MISALIGNED
+    assert mv(r(dims(batch=0)), r(state()), 4, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE,
+              None) == _abi.OK

@@ -119,3 +119,33 @@ def test_conventional_snapshot_verify_and_accept(kind, dk, dv, in_dtype):
     after = host(S)
     assert np.array_equal(after[:2], before[:2]), "a refused accept leaves S unchanged"
     assert np.array_equal(after[3], sn[3, 3]) and np.array_equal(after[4], sn[4, 0])
+
+
+@pytest.mark.parametrize("read", ["f32", "bf16"])
+def test_mamba2_spec(read):
+    """Mamba-2 verify (K drafts from one state read) + pointer accept, with folds."""
+    wl = synth.Mamba2Workload(batch=4, heads=8, P=64, N=128, window=16, K=4, in_dtype="bf16",
+                              seed=31)
+    run(Session("mamba2", wl, read), 20, 4)
+
+
+def test_mamba2_spec_ragged():
+    """P = 96, N = 64, two B/C groups, W = 7, K = 3, FP32 inputs and read path."""
+    wl = synth.Mamba2Workload(batch=3, heads=6, P=96, N=64, groups=2, window=7, K=3,
+                              in_dtype="f32", seed=32)
+    run(Session("mamba2", wl, "f32"), 14, 3, check_every=1)
+
+
+def test_mamba2_spec_then_plain_decode():
+    wl = synth.Mamba2Workload(batch=3, heads=4, P=64, N=128, window=16, K=4, seed=33)
+    s = Session("mamba2", wl, "bf16")
+    for r in range(8):
+        s.consolidate(4)
+        s.verify(r, 4)
+        s.accept(synth.accept_counts(wl.seed, r, wl.batch, 4), 4)
+        s.consolidate(1)
+        s.decode(r)
+        s.check_pointers(f"round {r}")
+        s.check_ring(f"round {r}")
+    s.consolidate(1, force=True)
+    s.check_checkpoint("end")
