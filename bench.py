@@ -44,6 +44,15 @@ WORKLOADS = {
 }
 POOL = 16  # distinct synthetic tokens, cycled through the timed steps
 
+# DRAM bytes (read + write) of one decode call at batch 64 from single-launch
+# ncu captures (profiles/mamba2_stream_kernel_b64.md + mamba2_prep_kernel_b64.md,
+# profiles/gdn_fused_kernel_b64.md; ring length 8); traffic grows in proportion
+# to the batch, so it is scaled by batch / 64. Only for the captured kernels.
+TRAFFIC_B64 = {
+    ("mamba2", "bf16"): 136.526592e6 + 3.470848e6 + 10.205184e6,
+    ("gdn", "bf16"): 77.418752e6 + 1.333760e6,
+}
+
 
 def parse(argv=None):
     p = argparse.ArgumentParser(description=__doc__.split("\n")[0])
@@ -350,7 +359,10 @@ def run_ours(args, rank, local_rank, world):
         "roofline": {
             "kernel": layer.decode_kernels(), "bound": "hbm", "achieved": round(achieved, 1),
             "peak": peak, "peak_source": peak_kind, "unit": "GB/s",
-            "frac": round(achieved / peak, 4), "traffic": None,
+            "frac": round(achieved / peak, 4),
+            "traffic": (round(TRAFFIC_B64[(wl["kind"], args.read)] * wl["batch"] / 64)
+                        if (wl["kind"], args.read) in TRAFFIC_B64 and wl["heads"] ==
+                        WORKLOADS[wl["kind"]]["heads"] else None),
             "bytes_per_launch": int(dec_bytes / K),
             "avg_launch_us": round(1e3 * sum(dec_ms) / K, 3),
         },
