@@ -45,9 +45,9 @@ WORKLOADS = {
 POOL = 16  # distinct synthetic tokens, cycled through the timed steps
 
 # DRAM bytes (read + write) of one decode call at batch 64 from single-launch
-# ncu captures (profiles/mamba2_stream_kernel_b64.md + mamba2_prep_kernel_b64.md,
-# profiles/gdn_fused_kernel_b64.md; ring length 8); traffic grows in proportion
-# to the batch, so it is scaled by batch / 64. Only for the captured kernels.
+# ncu captures of the same kernels (Mamba-2: stream + prep kernels; GDN: the
+# fused kernel; ring length 8); traffic grows in proportion to the batch, so
+# it is scaled by batch / 64. Only for the captured kernels.
 TRAFFIC_B64 = {
     ("mamba2", "bf16"): 136.526592e6 + 3.470848e6 + 10.205184e6,
     ("gdn", "bf16"): 77.418752e6 + 1.333760e6,
