@@ -319,6 +319,34 @@ REPLAYSSM_API replayssm_status replayssm_mamba2_decode_noalloc(
 #define REPLAYSSM_NOALLOC_SCRATCH_BYTES (16u << 20)
 
 /*
+ * Copies whole sequences between two layer states of the same dims: for each
+ * i < n, sequence src_idx[i] of src is written to sequence dst_idx[i] of dst
+ * (checkpoint, read copy, every ring field, ring head and len, status), so a
+ * sequence resumes from (S_c, ring, pointer) without replaying its history
+ * -- the state operations prefix caching and continuous batching need (the
+ * pages' serving context, "NVIDIA présente ReplaySSM…", "D'où vient le
+ * problème de l'état"). src and dst may be the same state (disjoint index
+ * sets). Optional fields (S_read, ring_C / ring_q) must be set on both sides
+ * or on neither. src_idx, dst_idx: device int32 [n], n <= 65535; pairs with
+ * an index outside [0, batch) are skipped. Nothing may be in flight on
+ * either state (the arrival counters are not copied and must be zero).
+ */
+REPLAYSSM_API replayssm_status replayssm_copy_sequences(const replayssm_dims* dims,
+                                                       const replayssm_state* src,
+                                                       const int32_t* src_idx,
+                                                       const replayssm_state* dst,
+                                                       const int32_t* dst_idx, int32_t n,
+                                                       void* stream);
+
+/*
+ * Self-test of the kernels' bounded waits (no counterpart on the pages): one
+ * warp waits on a barrier that nothing completes; after the wait limit (about
+ * one second) it ORs REPLAYSSM_SEQ_TIMEOUT into status[0] and returns, and
+ * the context stays usable. status: device int32, 16-byte aligned.
+ */
+REPLAYSSM_API replayssm_status replayssm_selftest_wait_timeout(int32_t* status, void* stream);
+
+/*
  * Size in bytes of state->work for decode calls (K = 1) and verify calls
  * with up to K drafts on the given sizes (0 if dims is invalid).
  */

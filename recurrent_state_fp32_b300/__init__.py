@@ -16,6 +16,7 @@ from .api import (  # noqa: F401
     conventional_gdn_step,
     conventional_gdn_verify,
     conventional_mamba2_step,
+    copy_sequences,
     gdn_decode,
     mamba2_decode,
     mamba2_decode_noalloc,

@@ -55,6 +55,8 @@ SIGNATURES = {
     "replayssm_conventional_gdn_step": [_DP, _P, _P, _P, _P, _P, _P, _F, _P, _P],
     "replayssm_conventional_gdn_verify": [_DP, _P, _I, _P, _P, _P, _P, _P, _F, _P, _P, _P],
     "replayssm_conventional_accept": [_DP, _P, _P, _P, _I, _P, _P],
+    "replayssm_copy_sequences": [_DP, _SP, _P, _SP, _P, _I, _P],
+    "replayssm_selftest_wait_timeout": [_P, _P],
     "replayssm_workspace_bytes": [_DP, _I],
     "replayssm_status_string": [_I],
     "replayssm_version": [],

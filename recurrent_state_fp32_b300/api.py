@@ -214,6 +214,13 @@ def conventional_accept(dims, S, snapshots, m, K, status=None, stream=None):
           _ptr(m), int(K), _ptr(status), _stream(stream))
 
 
+def copy_sequences(dims, src, src_idx, dst, dst_idx, stream=None):
+    """Copy whole sequences (checkpoint, read copy, ring, pointers) between states."""
+    n = int(src_idx.numel())
+    _call("replayssm_copy_sequences", ctypes.byref(dims.c()), ctypes.byref(src.c()),
+          _ptr(src_idx), ctypes.byref(dst.c()), _ptr(dst_idx), n, _stream(stream))
+
+
 def workspace_bytes(dims: LayerDims, K: int = 1) -> int:
     """Bytes of scratch a state needs for decode (K = 1) and verify with up to K drafts."""
     return int(_abi.lib.replayssm_workspace_bytes(ctypes.byref(dims.c()), int(K)))

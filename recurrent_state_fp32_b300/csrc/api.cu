@@ -68,6 +68,49 @@ __global__ void conventional_accept_kernel(long long per_seq4, int K, const int3
     dst[i] = src[i];
 }
 
+// Copies n_bytes (a multiple of 16) per sequence from sequence src_idx[i] of
+// src to sequence dst_idx[i] of dst (blockIdx.y = i); pairs with an index
+// outside [0, batch) are skipped.
+__global__ void copy_rows_kernel(const unsigned char* __restrict__ src, unsigned char* __restrict__ dst,
+                                 long long n_bytes, const int32_t* __restrict__ src_idx,
+                                 const int32_t* __restrict__ dst_idx, int batch) {
+  const int si = src_idx[blockIdx.y], di = dst_idx[blockIdx.y];
+  if (si < 0 || si >= batch || di < 0 || di >= batch) return;
+  const uint4* s4 = reinterpret_cast<const uint4*>(src + (long long)si * n_bytes);
+  uint4* d4 = reinterpret_cast<uint4*>(dst + (long long)di * n_bytes);
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n_bytes / 16;
+       i += (long long)gridDim.x * blockDim.x)
+    d4[i] = s4[i];
+}
+
+// Per-sequence ring pointers and status of pair i (one thread per pair).
+__global__ void copy_pointers_kernel(const int32_t* __restrict__ sh, const int32_t* __restrict__ sl,
+                                     const int32_t* __restrict__ ss, int32_t* __restrict__ dh,
+                                     int32_t* __restrict__ dl, int32_t* __restrict__ ds,
+                                     const int32_t* __restrict__ src_idx,
+                                     const int32_t* __restrict__ dst_idx, int n, int batch) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n) return;
+  const int si = src_idx[i], di = dst_idx[i];
+  if (si < 0 || si >= batch || di < 0 || di >= batch) return;
+  dh[di] = sh[si];
+  dl[di] = sl[si];
+  ds[di] = ss[si];
+}
+
+// Waits on an mbarrier that nothing arrives at, with the kernels' bounded
+// wait: after the limit it records REPLAYSSM_SEQ_TIMEOUT and returns.
+__global__ void wait_timeout_kernel(int32_t* status) {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  const bool done = mbar_wait_warp(&bar, 0);
+  if (threadIdx.x == 0 && !done) atomicOr(status, REPLAYSSM_SEQ_TIMEOUT);
+}
+
 __global__ void refresh_kernel(const float4* __restrict__ S, uint2* __restrict__ R, long long n4) {
   for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n4;
        i += (long long)gridDim.x * blockDim.x) {
@@ -92,6 +135,24 @@ cudaError_t launch_conventional_accept(const replayssm_dims& d, float* S, const 
   const int bx = (int)std::max<long long>(1, std::min<long long>((per_seq4 + 255) / 256, 64));
   conventional_accept_kernel<<<dim3(bx, d.batch), 256, 0, st>>>(
       per_seq4, K, m, reinterpret_cast<const float4*>(snap), reinterpret_cast<float4*>(S), status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_copy_rows(const void* src, void* dst, long long n_bytes, const int32_t* src_idx,
+                             const int32_t* dst_idx, int n, int batch, cudaStream_t st) {
+  const int bx = (int)std::max<long long>(1, std::min<long long>((n_bytes / 16 + 255) / 256, 64));
+  copy_rows_kernel<<<dim3(bx, n), 256, 0, st>>>(static_cast<const unsigned char*>(src),
+                                                 static_cast<unsigned char*>(dst), n_bytes, src_idx,
+                                                 dst_idx, batch);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_copy_pointers(const replayssm_state* src, const replayssm_state* dst,
+                                 const int32_t* src_idx, const int32_t* dst_idx, int n, int batch,
+                                 cudaStream_t st) {
+  copy_pointers_kernel<<<(n + 255) / 256, 256, 0, st>>>(src->ring_head, src->ring_len, src->status,
+                                                        dst->ring_head, dst->ring_len, dst->status,
+                                                        src_idx, dst_idx, n, batch);
   return cudaGetLastError();
 }
 
@@ -400,6 +461,60 @@ REPLAYSSM_API replayssm_status replayssm_conventional_accept(const replayssm_dim
   if (dims->batch > 65535) return REPLAYSSM_ERR_UNSUPPORTED;
   return finish(rs::launch_conventional_accept(*dims, S, snapshots, m, K, status,
                                                static_cast<cudaStream_t>(stream)));
+}
+
+REPLAYSSM_API replayssm_status replayssm_copy_sequences(const replayssm_dims* dims,
+                                                       const replayssm_state* src,
+                                                       const int32_t* src_idx,
+                                                       const replayssm_state* dst,
+                                                       const int32_t* dst_idx, int32_t n,
+                                                       void* stream) {
+  RS_TRY(check_dims(dims));
+  RS_TRY(check_state(dims, src));
+  RS_TRY(check_state(dims, dst));
+  if (n < 0 || n > 65535) return REPLAYSSM_ERR_INVALID_ARG;
+  if (n == 0 || dims->batch == 0) return REPLAYSSM_OK;
+  RS_TRY(check_ptr(src_idx));
+  RS_TRY(check_ptr(dst_idx));
+  // optional fields must be present on both sides or on neither
+  if (!src->S_read != !dst->S_read) return REPLAYSSM_ERR_INVALID_ARG;
+  const bool m2 = dims->kind == REPLAYSSM_MAMBA2;
+  if (m2 && !src->ring_C != !dst->ring_C) return REPLAYSSM_ERR_INVALID_ARG;
+  if (!m2 && !src->ring_q != !dst->ring_q) return REPLAYSSM_ERR_INVALID_ARG;
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const long long H = dims->heads, W = dims->window, Wd = (W + 3) / 4 * 4;
+  const long long ti = dims->in_dtype == REPLAYSSM_BF16 ? 2 : 4;
+  const long long elems = H * dims->dv * dims->dk;
+  const int b = dims->batch;
+  cudaError_t e;
+#define RS_COPY(SRC, DST, BYTES)                                                           \
+  do {                                                                                     \
+    e = rs::launch_copy_rows(SRC, DST, BYTES, src_idx, dst_idx, n, b, st);                \
+    if (e != cudaSuccess) return REPLAYSSM_ERR_CUDA;                                       \
+  } while (0)
+  RS_COPY(src->S_ckpt, dst->S_ckpt, elems * 4);
+  if (src->S_read) RS_COPY(src->S_read, dst->S_read, elems * 2);
+  if (m2) {
+    RS_COPY(src->ring_x, dst->ring_x, H * W * dims->dv * ti);
+    RS_COPY(src->ring_B, dst->ring_B, W * dims->groups * dims->dk * ti);
+    if (src->ring_C) RS_COPY(src->ring_C, dst->ring_C, W * dims->groups * dims->dk * ti);
+    RS_COPY(src->ring_dt, dst->ring_dt, H * Wd * 4);
+  } else {
+    if (src->ring_q) RS_COPY(src->ring_q, dst->ring_q, H * W * dims->dk * ti);
+    RS_COPY(src->ring_k, dst->ring_k, H * W * dims->dk * ti);
+    RS_COPY(src->ring_v, dst->ring_v, H * W * dims->dv * ti);
+    RS_COPY(src->ring_alpha, dst->ring_alpha,
+            dims->kind == REPLAYSSM_KDA ? H * W * dims->dk * 4 : H * Wd * 4);
+    RS_COPY(src->ring_beta, dst->ring_beta, H * Wd * 4);
+  }
+#undef RS_COPY
+  return finish(rs::launch_copy_pointers(src, dst, src_idx, dst_idx, n, b, st));
+}
+
+REPLAYSSM_API replayssm_status replayssm_selftest_wait_timeout(int32_t* status, void* stream) {
+  RS_TRY(check_ptr(status));
+  rs::wait_timeout_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(status);
+  return finish(cudaGetLastError());
 }
 
 REPLAYSSM_API int64_t replayssm_workspace_bytes(const replayssm_dims* dims, int32_t K) {

@@ -69,6 +69,11 @@ cudaError_t launch_conventional_accept(const replayssm_dims& d, float* S, const 
 
 cudaError_t launch_accept(const replayssm_dims& d, const replayssm_state& s, const int32_t* m,
                           int K, cudaStream_t st);
+cudaError_t launch_copy_rows(const void* src, void* dst, long long n_bytes, const int32_t* src_idx,
+                             const int32_t* dst_idx, int n, int batch, cudaStream_t st);
+cudaError_t launch_copy_pointers(const replayssm_state* src, const replayssm_state* dst,
+                                 const int32_t* src_idx, const int32_t* dst_idx, int n, int batch,
+                                 cudaStream_t st);
 cudaError_t launch_refresh(const replayssm_dims& d, const replayssm_state& s, cudaStream_t st);
 
 // Grid for the fold kernels: every block examines at most kFoldTilesPerBlock

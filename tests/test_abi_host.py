@@ -189,3 +189,19 @@ def test_mamba2_spec_arguments():
               None) == _abi.ERR_MISALIGNED
     assert mv(r(dims(batch=0)), r(state()), 4, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE,
               None) == _abi.OK
+
+
+def test_selftest_arguments():
+    assert _abi.lib.replayssm_selftest_wait_timeout(None, None) == _abi.ERR_INVALID_ARG
+    assert _abi.lib.replayssm_selftest_wait_timeout(MISALIGNED, None) == _abi.ERR_MISALIGNED
+
+
+def test_copy_sequences_arguments():
+    r = ctypes.byref
+    cs = _abi.lib.replayssm_copy_sequences
+    g = dims(kind=_abi.GDN, dv=128)
+    assert cs(r(g), r(state()), FAKE, r(state()), FAKE, -1, None) == _abi.ERR_INVALID_ARG
+    assert cs(r(g), r(state()), FAKE, r(state()), FAKE, 0, None) == _abi.OK
+    assert cs(r(g), r(state()), None, r(state()), FAKE, 2, None) == _abi.ERR_INVALID_ARG
+    assert cs(r(g), r(state(S_read=None)), FAKE, r(state()), FAKE, 2, None) == _abi.ERR_INVALID_ARG
+    assert cs(r(g), r(state()), FAKE, r(state(ring_k=None)), FAKE, 2, None) == _abi.ERR_INVALID_ARG

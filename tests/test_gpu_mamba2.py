@@ -119,3 +119,19 @@ def test_conventional_step(N, P):
         ref, yr = rec.mamba2_step(ref, tok["x"], tok["B"], tok["C"], tok["dt"], A, D)
         f32_close(host(y), yr, f"conventional y step {t}")
     f32_close(host(S), ref, "conventional state")
+
+
+def test_bounded_wait_reports_timeout_and_context_survives():
+    """A wait that nothing completes ends after its limit with TIMEOUT set, and the
+    same context then decodes normally."""
+    import ctypes
+
+    from recurrent_state_fp32_b300 import _abi
+
+    st = torch.zeros(4, dtype=torch.int32, device="cuda")
+    rc = _abi.lib.replayssm_selftest_wait_timeout(ctypes.c_void_p(st.data_ptr()), None)
+    assert rc == _abi.OK
+    torch.cuda.synchronize()
+    assert int(st[0]) == _abi.SEQ_TIMEOUT
+    wl = synth.Mamba2Workload(batch=2, heads=4, P=64, N=128, window=4, steps=6, seed=12)
+    run(Session("mamba2", wl, "f32"), wl.steps)
