@@ -8,7 +8,12 @@ inputs, FP32 checkpoint plus BF16 read copy. One step = consolidate(k_next = 1)
 plain decoding. Prints one JSON line.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--workload mamba2|gdn|kda] [--read bf16|f32]
+                  [--workload mamba2|gdn|kda|gdn_spec] [--read bf16|f32] [--stagger]
+
+By default every sequence starts at the same ring phase, so all of them fold
+on the same step (every W-th). --stagger starts sequence s at phase s mod W,
+as sequences that joined a continuous batch at different steps are: then
+1/W of the batch folds on every step.
 
 Timing: device time with CUDA events on the launching stream, W untimed
 warm-up steps first, a barrier and a synchronize on both sides of the K timed
@@ -63,11 +68,42 @@ def parse(argv=None):
     p.add_argument("--workload", choices=sorted(WORKLOADS), default="mamba2")
     p.add_argument("--read", choices=["bf16", "f32"], default="bf16")
     p.add_argument("--batch", type=int, default=None, help="override the batch size")
+    p.add_argument("--stagger", action="store_true",
+                   help="start sequence s at ring phase s mod W (continuous batching)")
     p.add_argument("--no-extras", action="store_true",
                    help="time the main loop only (no A/B, e2e, CPU baseline, clocks)")
     p.add_argument("--cpu-seconds", type=float, default=12.0,
                    help="budget of the CPU-oracle baseline sample")
     return p.parse_args(argv)
+
+
+# ------------------------------------------------------------------ config
+def decode_config(wl: dict, read: str, world: int, stagger: bool) -> dict:
+    k, W = wl["kind"], wl["window"]
+    rows, cols = ("p", "n") if k == "mamba2" else ("dv", "dk")
+    return {
+        "workload": f"{k}_decode_b{wl['batch']}_h{wl['heads']}_{rows}{wl['dv']}_"
+                    f"{cols}{wl['dk']}_w{W}" + ("_staggered" if stagger else ""),
+        "batch_per_gpu": wl["batch"], "heads": wl["heads"], "dk_or_N": wl["dk"],
+        "dv_or_P": wl["dv"], "window": W, "read_copy": read, "inputs": "bf16",
+        "checkpoint": "f32", "step": "consolidate(k_next=1) + replay decode",
+        "ring_phases": ("staggered: sequence s starts at phase s mod W" if stagger else
+                        "lockstep: every sequence at the same phase"),
+        "l2": "state larger than L2 (no flush)", "parallelism": f"replicas x{world}",
+    }
+
+
+def spec_config(wl: dict, read: str, world: int) -> dict:
+    k, b, H, dk, W, K = (wl[x] for x in ("kind", "batch", "heads", "dk", "window", "K"))
+    return {"workload": f"{k}_spec_b{b}_h{H}_d{dk}_w{W}_k{K}", "batch_per_gpu": b,
+            "drafts": K, "read_copy": read, "inputs": "bf16", "checkpoint": "f32",
+            "step": "consolidate(k_next=K) + spec_verify(K) + accept(m)",
+            "l2": "state larger than L2 (no flush)", "parallelism": f"replicas x{world}"}
+
+
+SPEC_METRIC = ("speculative rounds: accepted tokens/s per SSM layer (verified K drafts per "
+               "sequence from one state read, pointer accept)")
+SPEC_UNIT = "accepted tokens/s"
 
 
 # ------------------------------------------------------------- distributed
@@ -268,10 +304,40 @@ class Layer:
         out = self.out.numel() * 4
         return self.state_elems() * ts + 2 * self.token_bytes() + n_prior * self.ring_entry_bytes() + out
 
-    def fold_bytes(self, n):
-        """Algorithmic bytes of one consolidate that folds n entries for every sequence."""
+    def fold_bytes(self, n, frac=1.0):
+        """Algorithmic bytes of one consolidate that folds a fraction frac of the
+        sequences, n entries each (on average)."""
         rd = 2 if self.state.S_read is not None else 0
-        return self.state_elems() * (4 + 4 + rd) + n * self.ring_entry_bytes()
+        return frac * (self.state_elems() * (4 + 4 + rd) + n * self.ring_entry_bytes())
+
+    def account(self, lens, steps):
+        """Algorithmic bytes (decode, consolidate) of `steps` steps of
+        consolidate(k_next = 1) + decode from per-sequence ring lengths `lens`.
+        Both byte counts are linear in the entries, so batch means suffice."""
+        lens = self.np.array(lens, dtype=self.np.int64)
+        W, b = self.wl["window"], len(lens)
+        dec = fold = 0.0
+        for _ in range(steps):
+            f = lens + 1 > W
+            if f.any():
+                fold += self.fold_bytes(lens[f].mean(), f.sum() / b)
+                lens[f] = 0
+            dec += self.decode_bytes(lens.mean())
+            lens += 1
+        return dec, fold
+
+    def stagger(self):
+        """Puts sequence s at ring phase s mod W: W lockstep steps, before the
+        j-th of which the sequences with s mod W == j restart from their
+        checkpoint (ring length 0, as a sequence that joins the batch with its
+        prefill state does). Afterwards their lengths are W, W - 1, ..., 1."""
+        torch = self.torch
+        W = self.wl["window"]
+        phase = torch.arange(self.wl["batch"], device=self.device) % W
+        for j in range(W):
+            self.state.ring_len[phase == j] = 0
+            self.consolidate()
+            self.decode(self.pool[j % POOL])
 
     def conventional_bytes(self):
         return self.state_elems() * 8 + self.token_bytes() + self.out.numel() * 4
@@ -294,9 +360,10 @@ def run_ours(args, rank, local_rank, world):
     for i in range(Wm):
         layer.consolidate()
         layer.decode(layer.pool[i % POOL])
+    if args.stagger:
+        layer.stagger()
     torch.cuda.synchronize()
-    # ring length before timed step i (all sequences move in lockstep)
-    len0 = int(layer.state.ring_len[0].item())
+    lens0 = layer.state.ring_len.cpu().numpy()
 
     ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
     start, end = ev(), ev()
@@ -327,13 +394,7 @@ def run_ours(args, rank, local_rank, world):
               f"{sorted(set(layer.state.status.tolist()))}", file=sys.stderr)
 
     # algorithmic bytes of the timed region
-    dec_bytes, fold_bytes, ln = 0, 0, len0
-    for i in range(K):
-        if ln + 1 > W:
-            fold_bytes += layer.fold_bytes(ln)
-            ln = 0
-        dec_bytes += layer.decode_bytes(ln)
-        ln += 1
+    dec_bytes, fold_bytes = layer.account(lens0, K)
     peak, peak_kind = measured_peaks()
     dec_s = sum(dec_ms) / 1e3
     achieved = dec_bytes / dec_s / 1e9
@@ -346,15 +407,7 @@ def run_ours(args, rank, local_rank, world):
         "steps": K, "warmup": Wm, "ms_per_step": round(ms / K, 5),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f32", "data": "synthetic (seeded; no weights or datasets)",
-        "config": {
-            "workload": f"{wl['kind']}_decode_b{wl['batch']}_h{wl['heads']}_"
-                        f"{'p' if wl['kind'] == 'mamba2' else 'dv'}{wl['dv']}_"
-                        f"{'n' if wl['kind'] == 'mamba2' else 'dk'}{wl['dk']}_w{W}",
-            "batch_per_gpu": wl["batch"], "heads": wl["heads"], "dk_or_N": wl["dk"],
-            "dv_or_P": wl["dv"], "window": W, "read_copy": args.read, "inputs": "bf16",
-            "checkpoint": "f32", "step": "consolidate(k_next=1) + replay decode",
-            "l2": "state larger than L2 (no flush)", "parallelism": f"replicas x{world}",
-        },
+        "config": decode_config(wl, args.read, world, args.stagger),
         "step_hbm_gbs": round(step_gbs, 1),
         "roofline": {
             "kernel": layer.decode_kernels(), "bound": "hbm", "achieved": round(achieved, 1),
@@ -504,16 +557,12 @@ def run_spec(args, rank, local_rank, world):
     accepted = sum(m_tot[(Wm + i) % rounds_pool] for i in range(Kt)) * world
     bad = int(state.status.ne(0).sum().item())
     res = {
-        "metric": "speculative rounds: accepted tokens/s per SSM layer (verified K drafts per "
-                  "sequence from one state read, pointer accept)",
-        "value": round(accepted / (ms_tot / 1e3), 1), "unit": "accepted tokens/s",
+        "metric": SPEC_METRIC,
+        "value": round(accepted / (ms_tot / 1e3), 1), "unit": SPEC_UNIT,
         "n_gpus": world, "steps": Kt, "warmup": Wm, "ms_per_step": round(ms_tot / Kt, 5),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic (seeded; no weights or datasets)",
-        "config": {"workload": f"{kind}_spec_b{b}_h{H}_d{dk}_w{W}_k{K}", "batch_per_gpu": b,
-                   "drafts": K, "read_copy": args.read, "inputs": "bf16", "checkpoint": "f32",
-                   "step": "consolidate(k_next=K) + spec_verify(K) + accept(m)",
-                   "l2": "state larger than L2 (no flush)", "parallelism": f"replicas x{world}"},
+        "config": spec_config(wl, args.read, world),
         "verified_tokens_per_s": round(b * K * Kt * world / (ms_tot / 1e3), 1),
         "gpu_launches": Kt * 3, "device_status_ok": bad == 0,
     }
@@ -617,36 +666,65 @@ def cpu_baseline(wl: dict, seconds: float):
 
 def run_reference(args, rank, world):
     """The CPU oracle as the reference arm: K timed steps (after W warm-up), each
-    a bounded sample of the workload (one sequence, a slice of its heads)."""
+    a bounded sample of the workload (one sequence, a slice of its heads). For
+    a speculative workload a step is one round: consolidate(k_next = K),
+    verify K drafts, accept the same m as the GPU arm draws."""
     if rank != 0:
         return None
     wl = dict(WORKLOADS[args.workload])
+    if args.batch:
+        wl["batch"] = args.batch
     heads = max(1, wl["heads"] // 16)
-    orc, toks, _ = oracle_sample(wl, heads)
+    frac = heads / wl["heads"]
+    spec = "K" in wl
+    if spec:
+        import synth
+
+        K, seed = wl["K"], 4
+        orc, _, np = oracle_sample(wl, heads, seed=seed)
+        H, dk, dv, kind = wl["heads"], wl["dk"], wl["dv"], wl["kind"]
+        rounds = []
+        for r in range(8):
+            d = synth.spec_draft_inputs(seed, r, 1, K, H, dk, dv, kind, "bf16")
+            m = synth.accept_counts(seed, r, wl["batch"], K)[:1]
+            rounds.append(({n: v[:, :, :heads] for n, v in d.items()}, m))
+
+        def step(i):
+            d, m = rounds[i % len(rounds)]
+            orc.consolidate(K)
+            orc.spec_verify(K, d)
+            orc.accept(m, K)
+            return int(m[0])
+    else:
+        orc, toks, _ = oracle_sample(wl, heads)
+
+        def step(i):
+            orc.consolidate(1)
+            orc.decode(toks[i % POOL])
+            return 1
     with _single_thread():
         for i in range(args.warmup):
-            orc.consolidate(1)
-            orc.decode(toks[i % POOL])
+            step(i)
         t0 = time.perf_counter()
-        for i in range(args.steps):
-            orc.consolidate(1)
-            orc.decode(toks[i % POOL])
+        tokens = sum(step(args.warmup + i) for i in range(args.steps))
         dt = time.perf_counter() - t0
-    frac = heads / wl["heads"]
-    value = args.steps * frac / dt
-    sample = (f"1 sequence x {heads} of {wl['heads']} heads per step ({frac:.4f} of a "
-              f"layer token), float64 numpy oracle, single thread")
+    value = tokens * frac / dt
+    what = "speculative round" if spec else "step"
+    sample = (f"1 sequence x {heads} of {wl['heads']} heads per {what} ({frac:.4f} of a "
+              f"layer's work for that sequence), float64 numpy oracle, single thread")
+    unit = SPEC_UNIT if spec else UNIT
     return {
-        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT,
+        "impl": "reference", "metric": SPEC_METRIC if spec else METRIC,
+        "value": round(value, 4), "unit": unit,
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(1e3 * dt / args.steps, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded; no weights or datasets)",
-        "config": {"workload": f"{wl['kind']}_decode_b{wl['batch']}_h{wl['heads']}_w{wl['window']}",
-                   "sample": sample},
-        "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
+        "config": dict(spec_config(wl, args.read, world) if spec else
+                       decode_config(wl, args.read, world, args.stagger), sample=sample),
+        "cpu_baseline": {"value": round(value, 4), "unit": unit, "cores": 1, "kind": "oracle",
                          "sample": sample},
-        "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
+        "e2e": {"value": round(value, 4), "unit": unit, "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
 

@@ -124,6 +124,21 @@ class ReplayOracle:
             return self.ckpt.copy()
         raise ValueError(precision)
 
+    def restart(self, seqs, S0) -> None:
+        """New sequences take over the slots ``seqs`` (continuous batching).
+
+        Each gets its own checkpoint S0[i] (also its committed state) and the
+        initial pointers and status, zero; the ring bytes stay as they are and
+        are overwritten as the new sequence appends. S0: [len(seqs),H,rows,cols].
+        """
+        seqs = np.asarray(seqs, np.int64)
+        S0 = np.asarray(S0, dtype=np.float64)
+        self.committed[seqs] = S0
+        self.ckpt[seqs] = S0
+        self.head[seqs] = 0
+        self.len[seqs] = 0
+        self.status[seqs] = 0
+
     # ---------------------------------------------------------- the calls
     def consolidate(self, k_next: int = 1, force: bool = False) -> np.ndarray:
         """Fold where len + k_next > W (or force and len > 0); returns the fold mask."""

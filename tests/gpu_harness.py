@@ -121,6 +121,30 @@ class Session:
         return {k: dev(v, self.vt if self._vec(k) else torch.float32) for k, v in tok.items()}
 
     # ---------------------------------------------------------------- calls
+    def join(self, slots, seed):
+        """New sequences take over ``slots``: a fresh seeded checkpoint, ring
+        pointers and status zero (the per-sequence initialisation the state
+        layout documents); the ring bytes stay. Sampled slots restart in the
+        oracle too."""
+        wl, st = self.wl, self.state
+        slots = np.asarray(slots, np.int64)
+        if self.kind == "mamba2":
+            S = synth.mamba2_initial_state(seed, len(slots), wl.heads, wl.P, wl.N)
+        else:
+            S = synth.delta_initial_state(seed, len(slots), wl.heads, wl.dv, wl.dk)
+        idx = torch.from_numpy(slots).to(DEV)
+        st.S_ckpt[idx] = dev(S)
+        for name in ("ring_head", "ring_len", "status"):
+            getattr(st, name)[idx] = 0
+        if st.S_read is not None:
+            api.refresh_read_copy(self.dims, st)
+        pos = {int(s): i for i, s in enumerate(self.seqs)}
+        mine = [(pos[int(s)], i) for i, s in enumerate(slots) if int(s) in pos]
+        if mine:
+            o_idx, s_idx = (np.array(v) for v in zip(*mine))
+            S32 = S.astype(np.float32)[s_idx][:, self.heads]
+            self.oracle.restart(o_idx, S32)
+
     def consolidate(self, k_next=1, force=False):
         api.consolidate(self.dims, self.state, self.dA if self.kind == "mamba2" else None,
                         k_next, force)

@@ -422,6 +422,43 @@ def pin_replay_reads_checkpoint_and_ring():
             _close(orc.replay_output(tok, "f64"), y, 1e-11, f"{kind} replay step {t}")
 
 
+def pin_restart_is_a_fresh_sequence():
+    """A slot taken over by a new sequence from the zero state mid-stream: its
+    first output is the single-token closed form, the replay formula keeps
+    agreeing with decode through later folds, and the other slot runs exactly
+    as it would without the restart."""
+    for kind in ("mamba2", "gdn", "kda"):
+        r = _rng(47)
+        b, H, rows, cols, W, T, t_join = 2, 2, 4, 6, 5, 17, 7
+        S0 = r.standard_normal((b, H, rows, cols))
+        if kind == "mamba2":
+            A, D = m2_params(r, H)
+            toks = m2_tokens(r, b, H, 1, rows, cols, T)
+            mk = lambda: om.ReplayOracle(kind, S0, W, A=A, D=D)  # noqa: E731
+        else:
+            toks = delta_tokens(r, b, H, cols, rows, T, kind == "kda")
+            mk = lambda: om.ReplayOracle(kind, S0, W, scale=0.7)  # noqa: E731
+        orc, plain = mk(), mk()
+        for t, tok in enumerate(toks):
+            if t == t_join:
+                orc.restart([1], np.zeros((1, H, rows, cols)))
+            orc.consolidate(1)
+            plain.consolidate(1)
+            y = orc.decode(tok)
+            y_plain = plain.decode(tok)
+            _close(y[0], y_plain[0], 0.0, f"{kind} untouched slot, step {t}")
+            _close(orc.replay_output(tok, "f64"), y, 1e-11, f"{kind} replay step {t}")
+            if t == t_join:
+                if kind == "mamba2":
+                    cb = np.sum(tok["C"][1, 0] * tok["B"][1, 0])
+                    want = (tok["dt"][1] * cb + D)[:, None] * tok["x"][1]
+                else:
+                    kq = np.sum(tok["k"][1] * tok["q"][1], axis=-1)
+                    want = 0.7 * (tok["beta"][1] * kq)[:, None] * tok["v"][1]
+                _close(y[1], want, 1e-13, f"{kind} first token after the restart")
+        assert orc.len[1] == (T - t_join - 1) % W + 1, f"{kind} restarted slot length"
+
+
 def pin_rollback_equals_accepted_prefix():
     """Verify K drafts then accept m equals decoding only the m accepted tokens.
 

@@ -141,6 +141,21 @@ def write_next_slot(self, mask, slot, tok):
     return _orig_write(self, mask, (slot + 1) % self.W, tok)
 
 
+def restart_keeps_checkpoint(self, seqs, S0):
+    seqs = np.asarray(seqs, np.int64)
+    self.committed[seqs] = np.asarray(S0, np.float64)
+    self.head[seqs] = 0
+    self.len[seqs] = 0
+    self.status[seqs] = 0
+
+
+def restart_keeps_length(self, seqs, S0):
+    seqs = np.asarray(seqs, np.int64)
+    self.committed[seqs] = np.asarray(S0, np.float64)
+    self.ckpt[seqs] = np.asarray(S0, np.float64)
+    self.status[seqs] = 0
+
+
 MUTANTS = [
     (rec, "mamba2_step", m2_no_skip),
     (rec, "mamba2_step", m2_old_state_output),
@@ -159,6 +174,8 @@ MUTANTS = [
     (om.ReplayOracle, "consolidate", consolidate_off_by_one),
     (om.ReplayOracle, "consolidate", consolidate_keeps_head),
     (om.ReplayOracle, "_write", write_next_slot),
+    (om.ReplayOracle, "restart", restart_keeps_checkpoint),
+    (om.ReplayOracle, "restart", restart_keeps_length),
 ]
 
 
