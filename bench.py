@@ -9,7 +9,11 @@ plain decoding. Prints one JSON line.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                   [--workload mamba2|gdn|kda|gdn_spec] [--read bf16|f32] [--stagger]
+                  [--step fused|split]
 
+A Mamba-2 step is one fused call (replayssm_mamba2_fold_decode: a full ring
+is folded while its state rows stream past) unless --step split asks for
+the two calls consolidate + decode; the delta kinds always take two calls.
 By default every sequence starts at the same ring phase, so all of them fold
 on the same step (every W-th). --stagger starts sequence s at phase s mod W,
 as sequences that joined a continuous batch at different steps are: then
@@ -68,6 +72,8 @@ def parse(argv=None):
     p.add_argument("--workload", choices=sorted(WORKLOADS), default="mamba2")
     p.add_argument("--read", choices=["bf16", "f32"], default="bf16")
     p.add_argument("--batch", type=int, default=None, help="override the batch size")
+    p.add_argument("--step", choices=["fused", "split"], default="fused",
+                   help="Mamba-2: one fused fold + decode call per step, or two calls")
     p.add_argument("--stagger", action="store_true",
                    help="start sequence s at ring phase s mod W (continuous batching)")
     p.add_argument("--no-extras", action="store_true",
@@ -78,7 +84,7 @@ def parse(argv=None):
 
 
 # ------------------------------------------------------------------ config
-def decode_config(wl: dict, read: str, world: int, stagger: bool) -> dict:
+def decode_config(wl: dict, read: str, world: int, stagger: bool, fused: bool = False) -> dict:
     k, W = wl["kind"], wl["window"]
     rows, cols = ("p", "n") if k == "mamba2" else ("dv", "dk")
     return {
@@ -86,7 +92,9 @@ def decode_config(wl: dict, read: str, world: int, stagger: bool) -> dict:
                     f"{cols}{wl['dk']}_w{W}" + ("_staggered" if stagger else ""),
         "batch_per_gpu": wl["batch"], "heads": wl["heads"], "dk_or_N": wl["dk"],
         "dv_or_P": wl["dv"], "window": W, "read_copy": read, "inputs": "bf16",
-        "checkpoint": "f32", "step": "consolidate(k_next=1) + replay decode",
+        "checkpoint": "f32",
+        "step": ("fold_decode: consolidate(k_next=1) + replay decode fused in one call"
+                 if fused else "consolidate(k_next=1) + replay decode"),
         "ring_phases": ("staggered: sequence s starts at phase s mod W" if stagger else
                         "lockstep: every sequence at the same phase"),
         "l2": "state larger than L2 (no flush)", "parallelism": f"replicas x{world}",
@@ -204,7 +212,7 @@ class ClockSampler:
 class Layer:
     """One SSM layer's state, token pool and step functions on one GPU."""
 
-    def __init__(self, wl: dict, read: str, device, seed: int = 2):
+    def __init__(self, wl: dict, read: str, device, seed: int = 2, fused: bool = False):
         import numpy as np
         import torch
 
@@ -244,6 +252,7 @@ class Layer:
         self.out = torch.empty((b, H, dv), device=device)
         self.names = names
         self.vec = vec
+        self.fused = fused and k == "mamba2"
 
     # one decode step on device-resident inputs
     def consolidate(self, stream=None):
@@ -258,6 +267,15 @@ class Layer:
             a.gdn_decode(self.dims, self.state, tok["q"], tok["k"], tok["v"], tok["alpha"],
                          tok["beta"], 1.0, self.out, stream)
 
+    def step(self, tok, stream=None):
+        """One whole step: the fused call, or consolidate then decode."""
+        if self.fused:
+            self.api.mamba2_fold_decode(self.dims, self.state, self.A, self.D, tok["x"], tok["B"],
+                                        tok["C"], tok["dt"], self.out, stream)
+        else:
+            self.consolidate(stream)
+            self.decode(tok, stream)
+
     def conventional(self, S, tok, stream=None):
         a = self.api
         if self.wl["kind"] == "mamba2":
@@ -267,11 +285,16 @@ class Layer:
             a.conventional_gdn_step(self.dims, S, tok["q"], tok["k"], tok["v"], tok["alpha"],
                                     tok["beta"], 1.0, self.out, stream)
 
-    def decode_launches(self):
-        """Kernels one decode call launches (consolidate launches one more)."""
-        return 2 if self.wl["kind"] == "mamba2" else 1
+    def step_launches(self):
+        """Kernels of one step: the fused call's two, or consolidate's one
+        plus the decode's (two for Mamba-2, one for the delta kinds)."""
+        if self.fused:
+            return 2
+        return 1 + (2 if self.wl["kind"] == "mamba2" else 1)
 
     def decode_kernels(self):
+        if self.fused:
+            return "mamba2_prep_kernel + mamba2_step_stream_kernel (one fused call)"
         if self.wl["kind"] == "mamba2":
             return "mamba2_prep_kernel + stream_kernel (one decode call)"
         return "delta_fused_kernel (one decode call)"
@@ -316,12 +339,15 @@ class Layer:
         Both byte counts are linear in the entries, so batch means suffice."""
         lens = self.np.array(lens, dtype=self.np.int64)
         W, b = self.wl["window"], len(lens)
+        ts = 2 if self.state.S_read is not None else 4
         dec = fold = 0.0
         for _ in range(steps):
             f = lens + 1 > W
             if f.any():
                 fold += self.fold_bytes(lens[f].mean(), f.sum() / b)
                 lens[f] = 0
+                if self.fused:  # a folded sequence's output comes from its new rows
+                    dec -= f.sum() / b * self.state_elems() * ts
             dec += self.decode_bytes(lens.mean())
             lens += 1
         return dec, fold
@@ -336,8 +362,7 @@ class Layer:
         phase = torch.arange(self.wl["batch"], device=self.device) % W
         for j in range(W):
             self.state.ring_len[phase == j] = 0
-            self.consolidate()
-            self.decode(self.pool[j % POOL])
+            self.step(self.pool[j % POOL])
 
     def conventional_bytes(self):
         return self.state_elems() * 8 + self.token_bytes() + self.out.numel() * 4
@@ -352,14 +377,13 @@ def run_ours(args, rank, local_rank, world):
     if args.batch:
         wl["batch"] = args.batch
     W = wl["window"]
-    layer = Layer(wl, args.read, device)
+    layer = Layer(wl, args.read, device, fused=args.step == "fused")
     stream = torch.cuda.current_stream(device)
     K, Wm = args.steps, args.warmup
 
     # warm-up
     for i in range(Wm):
-        layer.consolidate()
-        layer.decode(layer.pool[i % POOL])
+        layer.step(layer.pool[i % POOL])
     if args.stagger:
         layer.stagger()
     torch.cuda.synchronize()
@@ -376,9 +400,14 @@ def run_ours(args, rank, local_rank, world):
     torch.cuda.synchronize()
     start.record(stream)
     for i in range(K):
-        layer.consolidate()
-        d0[i].record(stream)
-        layer.decode(layer.pool[i % POOL])
+        # events around the decode call (the fused call also holds the folds)
+        if layer.fused:
+            d0[i].record(stream)
+            layer.step(layer.pool[i % POOL])
+        else:
+            layer.consolidate()
+            d0[i].record(stream)
+            layer.decode(layer.pool[i % POOL])
         d1[i].record(stream)
     end.record(stream)
     end.synchronize()
@@ -397,7 +426,8 @@ def run_ours(args, rank, local_rank, world):
     dec_bytes, fold_bytes = layer.account(lens0, K)
     peak, peak_kind = measured_peaks()
     dec_s = sum(dec_ms) / 1e3
-    achieved = dec_bytes / dec_s / 1e9
+    call_bytes = dec_bytes + (fold_bytes if layer.fused else 0)
+    achieved = call_bytes / dec_s / 1e9
     tokens = wl["batch"] * K * world
     value = tokens / (ms / 1e3)
     step_gbs = (dec_bytes + fold_bytes) / (ms / 1e3) / 1e9
@@ -407,7 +437,7 @@ def run_ours(args, rank, local_rank, world):
         "steps": K, "warmup": Wm, "ms_per_step": round(ms / K, 5),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f32", "data": "synthetic (seeded; no weights or datasets)",
-        "config": decode_config(wl, args.read, world, args.stagger),
+        "config": decode_config(wl, args.read, world, args.stagger, layer.fused),
         "step_hbm_gbs": round(step_gbs, 1),
         "roofline": {
             "kernel": layer.decode_kernels(), "bound": "hbm", "achieved": round(achieved, 1),
@@ -415,11 +445,11 @@ def run_ours(args, rank, local_rank, world):
             "frac": round(achieved / peak, 4),
             "traffic": (round(TRAFFIC_B64[(wl["kind"], args.read)] * wl["batch"] / 64)
                         if (wl["kind"], args.read) in TRAFFIC_B64 and wl["heads"] ==
-                        WORKLOADS[wl["kind"]]["heads"] else None),
-            "bytes_per_launch": int(dec_bytes / K),
+                        WORKLOADS[wl["kind"]]["heads"] and not layer.fused else None),
+            "bytes_per_launch": int(call_bytes / K),
             "avg_launch_us": round(1e3 * sum(dec_ms) / K, 3),
         },
-        "gpu_launches": K * (1 + layer.decode_launches()),
+        "gpu_launches": K * layer.step_launches(),
         "device_status_ok": bad == 0,
     }
     if clocks:
@@ -472,8 +502,7 @@ def run_e2e(layer, args, stream, world):
     def step(i):
         for n, t in host[i % POOL].items():
             stage[n].copy_(t, non_blocking=True)
-        layer.consolidate()
-        layer.decode(stage)
+        layer.step(stage)
         y_host.copy_(layer.out, non_blocking=True)
 
     for i in range(8):
@@ -721,7 +750,9 @@ def run_reference(args, rank, world):
         "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded; no weights or datasets)",
         "config": dict(spec_config(wl, args.read, world) if spec else
-                       decode_config(wl, args.read, world, args.stagger), sample=sample),
+                       decode_config(wl, args.read, world, args.stagger,
+                                     args.step == "fused" and wl["kind"] == "mamba2"),
+                       sample=sample),
         "cpu_baseline": {"value": round(value, 4), "unit": unit, "cores": 1, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": round(value, 4), "unit": unit, "h2d_bytes_per_step": 0,

@@ -111,9 +111,10 @@ typedef struct replayssm_dims {
  * update after every block of that sequence has read it; each call leaves it
  * at zero. `work` is scratch for the per-head values a decode or verify call
  * derives from the ring before it streams the state (the buffer terms, the
- * decay or the swept query); it must hold replayssm_workspace_bytes(dims, K)
- * bytes for the largest K used with this state, needs no initialisation and
- * is overwritten by every decode and verify call.
+ * decay, the swept query or the fold weights); it must hold
+ * replayssm_workspace_bytes(dims, K) bytes for the largest K used with this
+ * state, needs no initialisation and is overwritten by every decode and
+ * verify call.
  */
 typedef struct replayssm_state {
   float* S_ckpt;      /* f32 checkpoint, never rounded */
@@ -179,6 +180,29 @@ REPLAYSSM_API replayssm_status replayssm_gdn_decode(
 REPLAYSSM_API replayssm_status replayssm_consolidate(
     const replayssm_dims* dims, const replayssm_state* state, const float* A, int32_t k_next,
     int32_t force, void* stream);
+
+/*
+ * One plain decode step of a Mamba-2 layer with the consolidation it needs,
+ * in one call: the result (outputs, S_ckpt, S_read, ring, pointers, status)
+ * is that of replayssm_consolidate(dims, state, A, 1, 0) followed by
+ * replayssm_mamba2_decode with the same arguments, up to float rounding
+ * order. A sequence whose ring is full is folded as its state rows stream
+ * past (the fold only when the buffer fills: "NVIDIA y Princeton aceleran
+ * modelos híbridos…", paragraph 2): S_ckpt is read once and written once,
+ * with S_read, and the output is computed from the new rows as the read
+ * copy holds them. Every other sequence is decoded from S_read as by
+ * replayssm_mamba2_decode. Arguments and layouts as for
+ * replayssm_mamba2_decode; state->work must hold
+ * replayssm_workspace_bytes(dims, 1) bytes and state->sync must be zero
+ * (each call leaves it zero). With W > 16, or with a read copy whose row
+ * block (about 16 KB of rows, at most P) is not a multiple of 64 rows -- P
+ * of 32 or 96, say -- the call runs the fold and the decode as two launches
+ * with the same result. Sequences with out-of-range pointers get
+ * REPLAYSSM_SEQ_BAD_POINTER and are untouched.
+ */
+REPLAYSSM_API replayssm_status replayssm_mamba2_fold_decode(
+    const replayssm_dims* dims, const replayssm_state* state, const float* A, const float* D,
+    const void* x, const void* B, const void* C, const float* dt, float* y, void* stream);
 
 /*
  * Speculative verify for the delta kinds ("ReplaySSM: o ganho aparece…",
@@ -347,8 +371,9 @@ REPLAYSSM_API replayssm_status replayssm_copy_sequences(const replayssm_dims* di
 REPLAYSSM_API replayssm_status replayssm_selftest_wait_timeout(int32_t* status, void* stream);
 
 /*
- * Size in bytes of state->work for decode calls (K = 1) and verify calls
- * with up to K drafts on the given sizes (0 if dims is invalid).
+ * Size in bytes of state->work for decode calls (K = 1; for Mamba-2 this
+ * includes replayssm_mamba2_fold_decode's per-head fold terms) and verify
+ * calls with up to K drafts on the given sizes (0 if dims is invalid).
  */
 REPLAYSSM_API int64_t replayssm_workspace_bytes(const replayssm_dims* dims, int32_t K);
 

@@ -20,6 +20,7 @@ from .api import (  # noqa: F401
     gdn_decode,
     mamba2_decode,
     mamba2_decode_noalloc,
+    mamba2_fold_decode,
     mamba2_spec_verify,
     refresh_read_copy,
     spec_verify,

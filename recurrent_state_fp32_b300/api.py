@@ -158,6 +158,14 @@ def mamba2_decode_noalloc(dims, state, A, D, x, B, C, dt, y, stream=None):
           _ptr(dt), _ptr(y), _stream(stream))
 
 
+def mamba2_fold_decode(dims, state, A, D, x, B, C, dt, y, stream=None):
+    """consolidate(k_next=1) then mamba2_decode in one call: a full ring is
+    folded while its state rows stream past."""
+    d, s = _refs(dims, state)
+    _call("replayssm_mamba2_fold_decode", d, s, _ptr(A), _ptr(D), _ptr(x), _ptr(B), _ptr(C),
+          _ptr(dt), _ptr(y), _stream(stream))
+
+
 def gdn_decode(dims, state, q, k, v, alpha, beta, scale, o, stream=None):
     d, s = _refs(dims, state)
     _call("replayssm_gdn_decode", d, s, _ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(beta),

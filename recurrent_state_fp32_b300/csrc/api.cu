@@ -345,6 +345,21 @@ REPLAYSSM_API replayssm_status replayssm_consolidate(const replayssm_dims* dims,
   return finish(rs::launch_delta_fold(*dims, *state, k_next, force, st));
 }
 
+REPLAYSSM_API replayssm_status replayssm_mamba2_fold_decode(
+    const replayssm_dims* dims, const replayssm_state* state, const float* A, const float* D,
+    const void* x, const void* B, const void* C, const float* dt, float* y, void* stream) {
+  RS_TRY(check_dims(dims));
+  if (dims->kind != REPLAYSSM_MAMBA2) return REPLAYSSM_ERR_INVALID_ARG;
+  RS_TRY(check_state(dims, state));
+  RS_TRY(check_ptr(A));
+  RS_TRY(check_ptr(D));
+  RS_TRY(check_mamba2_token(x, B, C, dt));
+  RS_TRY(check_ptr(y));
+  if (dims->batch == 0) return REPLAYSSM_OK;
+  return finish(rs::launch_mamba2_fold_decode(*dims, *state, A, D, x, B, C, dt, y,
+                                              static_cast<cudaStream_t>(stream)));
+}
+
 REPLAYSSM_API replayssm_status replayssm_spec_verify(
     const replayssm_dims* dims, const replayssm_state* state, int32_t K, const void* q,
     const void* k, const void* v, const float* alpha, const float* beta, float scale, float* o,
@@ -519,7 +534,9 @@ REPLAYSSM_API replayssm_status replayssm_selftest_wait_timeout(int32_t* status, 
 
 REPLAYSSM_API int64_t replayssm_workspace_bytes(const replayssm_dims* dims, int32_t K) {
   if (check_dims(dims) != REPLAYSSM_OK || K < 0) return 0;
-  return rs::WorkLayout(*dims, K < 1 ? 1 : K).bytes();
+  const long long b = rs::WorkLayout(*dims, K < 1 ? 1 : K).bytes();
+  if (dims->kind != REPLAYSSM_MAMBA2) return b;
+  return std::max<long long>(b, rs::StepLayout(*dims).bytes());
 }
 
 REPLAYSSM_API replayssm_status replayssm_mamba2_decode_noalloc(

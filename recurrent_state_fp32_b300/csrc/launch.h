@@ -27,6 +27,30 @@ struct WorkLayout {
   int32_t* flags(float* work) const { return reinterpret_cast<int32_t*>(work + rows * row); }
 };
 
+// Entries a fused fold + decode step folds at most (W <= kStepMaxW).
+constexpr int kStepMaxW = 16;
+
+// Layout of state.work for the fused Mamba-2 fold + decode step: one row of
+// `row` floats per (sequence, head) -- buffer terms [0, P), decode decay at
+// P, fold decay at P + 1 -- then, per (sequence, head), the fold
+// coefficients c_j[p] = w_j x_j[p] as [P][kStepMaxW] floats, then per
+// (sequence, group) the folded B rows as [kStepMaxW][N] floats, then one
+// int32 per sequence.
+struct StepLayout {
+  int row;
+  long long rows, batch, pack0, bf0, flag0;  // float offsets
+  explicit StepLayout(const replayssm_dims& d) {
+    row = (d.dv + 2 + 3) & ~3;
+    batch = d.batch;
+    rows = batch * d.heads;
+    pack0 = rows * row;
+    bf0 = pack0 + rows * d.dv * kStepMaxW;
+    flag0 = bf0 + batch * d.groups * kStepMaxW * d.dk;
+  }
+  long long bytes() const { return flag0 * 4 + ((batch * 4 + 15) & ~15LL); }
+  int32_t* flags(float* work) const { return reinterpret_cast<int32_t*>(work + flag0); }
+};
+
 // Device facts cached per device (SM count, opt-in shared memory per block).
 struct DeviceInfo {
   int sms;
@@ -42,6 +66,11 @@ cudaError_t launch_mamba2_verify(const replayssm_dims& d, const replayssm_state&
                                  const void* C, const float* dt, float* y, cudaStream_t st);
 cudaError_t launch_mamba2_fold(const replayssm_dims& d, const replayssm_state& s, const float* A,
                                int k_next, int force, cudaStream_t st);
+// consolidate(k_next = 1) then decode, as one prep and one stream launch
+cudaError_t launch_mamba2_fold_decode(const replayssm_dims& d, const replayssm_state& s,
+                                      const float* A, const float* D, const void* x,
+                                      const void* B, const void* C, const float* dt, float* y,
+                                      cudaStream_t st);
 cudaError_t launch_mamba2_conventional(const replayssm_dims& d, float* S, const float* A,
                                        const float* D, const void* x, const void* B, const void* C,
                                        const float* dt, float* y, cudaStream_t st);

@@ -14,6 +14,7 @@
 
 #include "common.cuh"
 #include "launch.h"
+#include "mamba2_step.cuh"
 #include "stream.cuh"
 
 namespace rs {
@@ -43,6 +44,10 @@ struct M2Prep {
   float* work;     // [b, H, wrow]: buffer terms [0, P), decay at P
   int wrow;
   int32_t* flags;  // [b]
+  // fused fold + decode only: fold decay at P + 1 of each work row, the fold
+  // coefficients [b, H, P, kStepMaxW] and the folded B rows [b, G, kStepMaxW, N]
+  float* pack;
+  float* bfold;
 };
 
 // Shared memory of one prep warp (byte offsets): kPrepDepth head stages
@@ -79,7 +84,17 @@ struct M2PrepSmem {
 // last arrival bumps len. A sequence whose ring is full (or whose pointers
 // are out of range) gets a status bit and flags[seq] = 0 and is untouched.
 // PT is the head dimension P when known at compile time (0: runtime P).
-template <int N, int PT, typename TI>
+//
+// STEP: preparation of the fused fold + decode step. A sequence whose ring
+// is full (len + 1 > W) is first folded: its n = len entries leave the ring
+// (head += n, len = 0) and the token is decoded after them, so the decode
+// terms above use only the token. The fold itself runs in the stream kernel;
+// this warp gives it, from the n entries (n <= kStepMaxW), the fold decay
+// exp(A_h sum_j dt_j) and the coefficients c_j[p] = w_j x_j[p] of every row,
+// and the head's group gets its B_j as floats (read before the token takes
+// the slot of entry 0). The ring pointers are left alone (the stream kernel
+// moves them), so no arrival happens here.
+template <int N, int PT, typename TI, bool STEP>
 __global__ void __launch_bounds__(32 * kPrepWarps) mamba2_prep_kernel(const M2Prep a) {
   extern __shared__ __align__(128) unsigned char smem[];
   constexpr int kNL = N / 32;
@@ -113,6 +128,7 @@ __global__ void __launch_bounds__(32 * kPrepWarps) mamba2_prep_kernel(const M2Pr
   int i_seq = v0 / H, i_h = v0 - (v0 / H) * H;
   int i_len = 0, i_hd = 0;
   bool i_ok = false;
+  int i_nf = 0;       // STEP: entries folded before the token (0: no fold)
   int i_loaded = -1;  // sequence whose pointers the issue side holds
   int i_t = 0;        // next head (offset from v0) to fetch
   auto issue = [&]() {
@@ -124,7 +140,13 @@ __global__ void __launch_bounds__(32 * kPrepWarps) mamba2_prep_kernel(const M2Pr
       }
       i_len = __shfl_sync(kFull, l, 0);
       i_hd = __shfl_sync(kFull, hh, 0);
-      i_ok = pointers_ok(i_hd, i_len, W) && i_len + 1 <= W;
+      i_ok = pointers_ok(i_hd, i_len, W) && (STEP || i_len + 1 <= W);
+      i_nf = 0;
+      if (STEP && i_ok && i_len + 1 > W) {  // fold first: pointers after the fold
+        i_nf = i_len;
+        i_hd = (i_hd + i_len) % W;
+        i_len = 0;
+      }
       i_loaded = i_seq;
     }
     const int v = v0 + i_t;
@@ -133,7 +155,18 @@ __global__ void __launch_bounds__(32 * kPrepWarps) mamba2_prep_kernel(const M2Pr
       int* hdr = reinterpret_cast<int*>(st + L.hdr);
       hdr[0] = i_len;
       hdr[1] = i_hd;
-      hdr[2] = i_ok ? 1 : 0;
+      hdr[2] = (i_ok ? 1 : 0) | (i_nf << 8);
+    }
+    if (STEP && i_nf > 0) {
+      // the x rows of the folded entries, oldest first, in the entry rows
+      // (the decode after the fold uses none of them)
+      const int hd0 = (i_hd - i_nf + W) % W;
+      const unsigned char* xs = ringx + (size_t)v * W * row;
+      for (int idx = lane; idx < i_nf * cpr; idx += 32) {
+        const int j = idx / cpr, c = idx - j * cpr;
+        const int slot = hd0 + j < W ? hd0 + j : hd0 + j - W;
+        cp_async16(st + L.xr + j * row + c * 16, xs + slot * row + c * 16);
+      }
     }
     if (i_ok) {
       const unsigned char* xs = ringx + (size_t)v * W * row;
@@ -166,7 +199,7 @@ __global__ void __launch_bounds__(32 * kPrepWarps) mamba2_prep_kernel(const M2Pr
   };
 
   // ---- compute side
-  int cur_seq = -1, len = 0, hd = 0;
+  int cur_seq = -1, len = 0, hd = 0, nf = 0;
   bool ok = false;
   int cb_seq = -1, cb_g = -1;  // (sequence, group) whose C.B_j the cache holds
   int seq_first = v0;          // first head of the current sequence in this range
@@ -184,12 +217,13 @@ __global__ void __launch_bounds__(32 * kPrepWarps) mamba2_prep_kernel(const M2Pr
     __syncwarp();
     const int v = v0 + t;
     if (seq != cur_seq) {
-      if (cur_seq >= 0 && ok && lane == 0)  // leaving a sequence: arrive with its heads
+      if (!STEP && cur_seq >= 0 && ok && lane == 0)  // leaving a sequence: arrive with its heads
         arrive_and_finish(a.sync + cur_seq, v - seq_first, H, [&] { a.len[cur_seq] = len + 1; });
       const int* hdr = reinterpret_cast<const int*>(wbase + (size_t)(t % kPrepDepth) * L.stage + L.hdr);
       len = hdr[0];
       hd = hdr[1];
-      ok = hdr[2] != 0;
+      ok = (hdr[2] & 1) != 0;
+      nf = hdr[2] >> 8;
       cur_seq = seq;
       seq_first = v;
       if (h == 0 && lane == 0) {
@@ -300,6 +334,53 @@ __global__ void __launch_bounds__(32 * kPrepWarps) mamba2_prep_kernel(const M2Pr
         if (act) *reinterpret_cast<float2*>(wrow + p) = make_float2(e0, e1);
       }
       if (lane == 0) wrow[P] = __expf(Ah * total);
+      if constexpr (STEP) {
+        if (nf > 0) {
+          // fold over entries 0..nf-1 (oldest at slot hd0): weights
+          // w_j = dt_j exp(A_h sum_{i>j} dt_i) (lane j) and decay exp(A_h sum_i dt_i)
+          const int hd0 = (hd - nf + W) % W;
+          const float fj = lane < nf ? dtr[hd0 + lane < W ? hd0 + lane : hd0 + lane - W] : 0.f;
+          float sfx = fj;  // inclusive suffix sum
+#pragma unroll
+          for (int o = 1; o < 32; o <<= 1) {
+            const float u = __shfl_down_sync(kFull, sfx, o);
+            if (lane + o < 32) sfx += u;
+          }
+          const float wj = fj * expf(Ah * (sfx - fj));
+          if (lane == 0) wrow[P + 1] = expf(Ah * sfx);
+          // coefficients of rows p = 2 lane + {0, 1} (+ 64 k): [P][kStepMaxW]
+          float* pk = a.pack + (size_t)v * P * kStepMaxW;
+          for (int p0 = 0; p0 < P; p0 += 64) {  // every lane runs every iteration
+            const int p = p0 + 2 * lane;
+            const bool act = p < P;
+            float c0[kStepMaxW], c1[kStepMaxW];
+#pragma unroll
+            for (int j = 0; j < kStepMaxW; ++j) {
+              const float w = __shfl_sync(kFull, wj, j);
+              const float2 xv = act && j < nf ? load2<TI>(xr + j * P + p) : make_float2(0.f, 0.f);
+              c0[j] = w * xv.x;
+              c1[j] = w * xv.y;
+            }
+            if (act) {
+              float4* d0 = reinterpret_cast<float4*>(pk + (size_t)p * kStepMaxW);
+#pragma unroll
+              for (int j = 0; j < kStepMaxW; j += 4) {
+                d0[j / 4] = make_float4(c0[j], c0[j + 1], c0[j + 2], c0[j + 3]);
+                d0[kStepMaxW / 4 + j / 4] = make_float4(c1[j], c1[j + 1], c1[j + 2], c1[j + 3]);
+              }
+            }
+          }
+          // the group's B rows, before the token takes the slot of entry 0
+          if (hg == 0) {
+            float* Bs = a.bfold + ((size_t)seq * G + g) * kStepMaxW * N;
+            for (int j = 0; j < nf; ++j) {
+              const int slot = hd0 + j < W ? hd0 + j : hd0 + j - W;
+              const TI* Bo = rB + (((size_t)seq * W + slot) * G + g) * N;
+              for (int c = lane; c < N; c += 32) Bs[(size_t)j * N + c] = to_f(Bo[c]);
+            }
+          }
+        }
+      }
       // append the token: x row and dt of this head, B and C of its group
       const int slot = hd + len < W ? hd + len : hd + len - W;
       uint4* xd = reinterpret_cast<uint4*>(const_cast<unsigned char*>(ringx) +
@@ -327,7 +408,7 @@ __global__ void __launch_bounds__(32 * kPrepWarps) mamba2_prep_kernel(const M2Pr
     }
   }
   cp_async_wait_all();
-  if (cur_seq >= 0 && ok && lane == 0)
+  if (!STEP && cur_seq >= 0 && ok && lane == 0)
     arrive_and_finish(a.sync + cur_seq, v1 - seq_first, H, [&] { a.len[cur_seq] = len + 1; });
 }
 
@@ -720,15 +801,13 @@ __global__ void __launch_bounds__(kThreads) mamba2_conventional_kernel(const M2C
 
 }  // namespace
 
-cudaError_t launch_mamba2_decode(const replayssm_dims& d, const replayssm_state& s, const float* A,
-                                 const float* D, const void* x, const void* B, const void* C,
-                                 const float* dt, float* y, cudaStream_t st) {
-  const WorkLayout wl(d, 1);
+namespace {
+
+// Launches the preparation kernel (plain decode, or the fused step when STEP).
+template <bool STEP>
+cudaError_t launch_prep(const replayssm_dims& d, const M2Prep& p, cudaStream_t st) {
   const bool in16 = d.in_dtype == REPLAYSSM_BF16;
   const int ti = in16 ? 2 : 4;
-  M2Prep p{d.batch, d.heads, d.groups, d.dv, d.window, A, D, x, B, C, dt,
-           s.ring_x, s.ring_B, s.ring_C, s.ring_dt, s.ring_head, s.ring_len, s.status, s.sync,
-           s.work, wl.row, wl.flags(s.work)};
   const M2PrepSmem L(d.dv, d.dk, d.window, ti);
   const size_t smem = L.warp_bytes * kPrepWarps;
   const long long heads = (long long)d.batch * d.heads;
@@ -739,7 +818,7 @@ cudaError_t launch_mamba2_decode(const replayssm_dims& d, const replayssm_state&
   cudaError_t e;
 #define RS_PREP(N_, PT_, TI_)                                                                   \
   {                                                                                            \
-    auto k = mamba2_prep_kernel<N_, PT_, TI_>;                                                 \
+    auto k = mamba2_prep_kernel<N_, PT_, TI_, STEP>;                                           \
     e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);       \
     if (e != cudaSuccess) return e;                                                            \
     k<<<(unsigned)grid, 32 * kPrepWarps, smem, st>>>(p);                                       \
@@ -753,7 +832,20 @@ cudaError_t launch_mamba2_decode(const replayssm_dims& d, const replayssm_state&
   }
 #undef RS_PREP_P
 #undef RS_PREP
-  e = cudaGetLastError();
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_mamba2_decode(const replayssm_dims& d, const replayssm_state& s, const float* A,
+                                 const float* D, const void* x, const void* B, const void* C,
+                                 const float* dt, float* y, cudaStream_t st) {
+  const WorkLayout wl(d, 1);
+  const bool in16 = d.in_dtype == REPLAYSSM_BF16;
+  M2Prep p{d.batch, d.heads, d.groups, d.dv, d.window, A, D, x, B, C, dt,
+           s.ring_x, s.ring_B, s.ring_C, s.ring_dt, s.ring_head, s.ring_len, s.status, s.sync,
+           s.work, wl.row, wl.flags(s.work), 0, nullptr};
+  cudaError_t e = launch_prep<false>(d, p, st);
   if (e != cudaSuccess) return e;
   // Stream: y = decay * (S C) + extra, C straight from the token input.
   StreamArgs sa{};
@@ -873,6 +965,105 @@ cudaError_t launch_mamba2_conventional(const replayssm_dims& d, float* S, const 
     else mamba2_conventional_kernel<64, float><<<grid, kThreads, 0, st>>>(a);
   }
   return cudaGetLastError();
+}
+
+namespace {
+
+template <int N, typename TS, typename TV>
+cudaError_t launch_step_stream(const StepArgs& a, size_t smem, int grid, int threads,
+                               cudaStream_t st) {
+  auto kern = mamba2_step_stream_kernel<N, TS, TV>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  // a programmatic dependent of the preparation kernel, as in the plain decode
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(threads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, a);
+}
+
+}  // namespace
+
+cudaError_t launch_mamba2_fold_decode(const replayssm_dims& d, const replayssm_state& s,
+                                      const float* A, const float* D, const void* x,
+                                      const void* B, const void* C, const float* dt, float* y,
+                                      cudaStream_t st) {
+  const bool rd16 = s.S_read != nullptr, in16 = d.in_dtype == REPLAYSSM_BF16;
+  const int ts = rd16 ? 2 : 4, FS = 4 / ts;
+  // the plain decode's tile: about 16 KB of state rows per unit
+  int RB = std::max(32, (int)(16384 / (d.dk * ts)) / 32 * 32);
+  RB = std::min(RB, d.dv);
+  while (d.dv % RB) RB -= 32;
+  const int GU = RB % 64 == 0 ? 2 : 1;
+  // Each consumer warp takes 32 rows of a unit, and a fold unit's FP32 rows
+  // give each warp whole stages (or share one); the entries must fit the
+  // registers. Otherwise: fold, then decode.
+  if (d.window > kStepMaxW || RB / GU != 32 || (FS > 1 && GU != FS)) {
+    cudaError_t e = launch_mamba2_fold(d, s, A, 1, 0, st);
+    if (e != cudaSuccess) return e;
+    return launch_mamba2_decode(d, s, A, D, x, B, C, dt, y, st);
+  }
+  const StepLayout sl(d);
+  M2Prep p{d.batch, d.heads, d.groups, d.dv, d.window, A, D, x, B, C, dt,
+           s.ring_x, s.ring_B, s.ring_C, s.ring_dt, s.ring_head, s.ring_len, s.status, s.sync,
+           s.work, sl.row, sl.flags(s.work), s.work + sl.pack0, s.work + sl.bf0};
+  cudaError_t e = launch_prep<true>(d, p, st);
+  if (e != cudaSuccess) return e;
+
+  const DeviceInfo& dev = device_info();
+  const int nrb = d.dv / RB;
+  const long long units = (long long)d.batch * d.heads * nrb;
+  if (units >= (1LL << 31)) return cudaErrorInvalidValue;
+  const int grid = (int)std::min<long long>(units, dev.sms);
+  const int nloc_max = (int)((units + grid - 1) / grid);  // units of the largest block
+  const int threads = 32 * (kStreamGroups * GU + 1);
+  const StepSmem fixed(RB, d.dk, ts, 0, nloc_max);
+  const size_t per_stage = fixed.stage + fixed.side + 16;
+  if ((size_t)dev.smem_optin < fixed.total + 2048 + 4 * per_stage) return cudaErrorInvalidConfiguration;
+  const int NS = (int)std::min<size_t>((dev.smem_optin - fixed.total - 2048) / per_stage, 12);
+  const size_t smem = StepSmem(RB, d.dk, ts, NS, nloc_max).total;
+
+  StepArgs a{};
+  a.batch = d.batch;
+  a.H = d.heads;
+  a.G = d.groups;
+  a.P = d.dv;
+  a.W = d.window;
+  a.RB = RB;
+  a.nrb = nrb;
+  a.NS = NS;
+  a.GU = GU;
+  a.nloc_max = nloc_max;
+  a.S = rd16 ? (const void*)s.S_read : (const void*)s.S_ckpt;
+  a.S_ckpt = s.S_ckpt;
+  a.S_read = reinterpret_cast<bf16*>(s.S_read);
+  a.out = y;
+  a.work = s.work;
+  a.wrow = sl.row;
+  a.pack = s.work + sl.pack0;
+  a.bfold = s.work + sl.bf0;
+  a.C = C;
+  a.head = s.ring_head;
+  a.len = s.ring_len;
+  a.status = s.status;
+  a.sync = s.sync;
+  if (d.dk == 128) {
+    if (rd16) return in16 ? launch_step_stream<128, bf16, bf16>(a, smem, grid, threads, st)
+                          : launch_step_stream<128, bf16, float>(a, smem, grid, threads, st);
+    return in16 ? launch_step_stream<128, float, bf16>(a, smem, grid, threads, st)
+                : launch_step_stream<128, float, float>(a, smem, grid, threads, st);
+  }
+  if (rd16) return in16 ? launch_step_stream<64, bf16, bf16>(a, smem, grid, threads, st)
+                        : launch_step_stream<64, bf16, float>(a, smem, grid, threads, st);
+  return in16 ? launch_step_stream<64, float, bf16>(a, smem, grid, threads, st)
+              : launch_step_stream<64, float, float>(a, smem, grid, threads, st);
 }
 
 }  // namespace rs

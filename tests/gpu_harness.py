@@ -167,6 +167,21 @@ class Session:
             self.compare_out(got, ref, f"step {t}")
         return y, ref
 
+    def fold_decode(self, t, check=True):
+        """One Mamba-2 step through the fused call; the oracle takes the same
+        step as consolidate(k_next=1) followed by decode."""
+        tok = self.token(t)
+        g = self._to_dev(tok)
+        y = torch.full((self.wl.batch, self.wl.heads, self.wl.P), float("nan"), device=DEV)
+        api.mamba2_fold_decode(self.dims, self.state, self.dA, self.dD, g["x"], g["B"], g["C"],
+                               g["dt"], y)
+        fold = self.oracle.consolidate(1)
+        ref = self.oracle.decode(self._sub(tok))
+        if check:
+            got = host(y)[self.seqs][:, self.heads]
+            self.compare_out(got, ref, f"fused step {t}")
+        return y, ref, fold
+
     def compare_out(self, got, ref, what):
         ok = ~np.isnan(ref).any(axis=-1)
         assert np.array_equal(np.isnan(got).any(axis=-1), ~ok), f"{what}: refused rows differ"

@@ -143,10 +143,35 @@ def test_delta_state_requires_its_ring(missing):
                                          None) == _abi.ERR_INVALID_ARG
 
 
+def test_fold_decode_arguments():
+    """The fused fold + decode entry point validates like the plain decode."""
+    r = ctypes.byref
+
+    def call(d, s, A=FAKE, y=FAKE):
+        return _abi.lib.replayssm_mamba2_fold_decode(
+            r(d) if d is not None else None, r(s) if s is not None else None,
+            A, FAKE, FAKE, FAKE, FAKE, FAKE, y, None)
+
+    assert call(None, state()) == _abi.ERR_INVALID_ARG
+    assert call(dims(), None) == _abi.ERR_INVALID_ARG
+    assert call(dims(kind=_abi.GDN), state()) == _abi.ERR_INVALID_ARG
+    assert call(dims(), state(), A=None) == _abi.ERR_INVALID_ARG
+    assert call(dims(), state(), y=None) == _abi.ERR_INVALID_ARG
+    assert call(dims(), state(ring_len=None)) == _abi.ERR_INVALID_ARG
+    assert call(dims(), state(S_ckpt=FAKE + 4)) == _abi.ERR_MISALIGNED
+    assert call(dims(dk=96), state()) == _abi.ERR_UNSUPPORTED
+    assert call(dims(batch=0), state()) == _abi.OK
+
+
 def test_workspace_size():
     r = ctypes.byref
-    m = dims(batch=2, heads=4, dk=128, dv=64)            # Mamba-2: P + 1 floats, padded to 4
-    assert _abi.lib.replayssm_workspace_bytes(r(m), 1) == 2 * 4 * 68 * 4 + 16
+    # Mamba-2: the fused fold + decode step's rows (P + 2 floats padded to 4),
+    # 16 fold coefficients per state row and 16 B rows per (sequence, group);
+    # verify rows for K = 4
+    m = dims(batch=2, heads=4, dk=128, dv=64)
+    step = 2 * 4 * 68 * 4 + 2 * 4 * 64 * 16 * 4 + 2 * 16 * 128 * 4 + 16
+    assert _abi.lib.replayssm_workspace_bytes(r(m), 1) == step
+    assert _abi.lib.replayssm_workspace_bytes(r(m), 4) == max(4 * 2 * 4 * 68 * 4 + 16, step)
     g = dims(kind=_abi.GDN, batch=3, heads=2, dk=128, dv=96)
     assert _abi.lib.replayssm_workspace_bytes(r(g), 1) == 3 * 2 * 224 * 4 + 16
     assert _abi.lib.replayssm_workspace_bytes(r(g), 4) == 3 * 4 * 2 * 224 * 4 + 16
