@@ -32,19 +32,19 @@ constexpr int kStepMaxW = 16;
 
 // Layout of state.work for the fused Mamba-2 fold + decode step: one row of
 // `row` floats per (sequence, head) -- buffer terms [0, P), decode decay at
-// P, fold decay at P + 1 -- then, per (sequence, head), the fold
-// coefficients c_j[p] = w_j x_j[p] as [P][kStepMaxW] floats, then per
+// P, fold decay at P + 1, fold weights at [P + 2, P + 2 + kStepMaxW), the x
+// row of the entry the token overwrites at [xo, xo + P) -- then per
 // (sequence, group) the folded B rows as [kStepMaxW][N] floats, then one
 // int32 per sequence.
 struct StepLayout {
-  int row;
-  long long rows, batch, pack0, bf0, flag0;  // float offsets
+  int row, xo;
+  long long rows, batch, bf0, flag0;  // float offsets
   explicit StepLayout(const replayssm_dims& d) {
-    row = (d.dv + 2 + 3) & ~3;
+    xo = (d.dv + 2 + kStepMaxW + 3) & ~3;
+    row = (xo + d.dv + 3) & ~3;
     batch = d.batch;
     rows = batch * d.heads;
-    pack0 = rows * row;
-    bf0 = pack0 + rows * d.dv * kStepMaxW;
+    bf0 = rows * row;
     flag0 = bf0 + batch * d.groups * kStepMaxW * d.dk;
   }
   long long bytes() const { return flag0 * 4 + ((batch * 4 + 15) & ~15LL); }

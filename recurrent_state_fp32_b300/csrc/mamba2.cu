@@ -44,9 +44,10 @@ struct M2Prep {
   float* work;     // [b, H, wrow]: buffer terms [0, P), decay at P
   int wrow;
   int32_t* flags;  // [b]
-  // fused fold + decode only: fold decay at P + 1 of each work row, the fold
-  // coefficients [b, H, P, kStepMaxW] and the folded B rows [b, G, kStepMaxW, N]
-  float* pack;
+  // fused fold + decode only: fold decay at P + 1, fold weights at
+  // [P + 2, P + 2 + kStepMaxW) and entry 0's x row at [xo, xo + P) of each
+  // work row; folded B rows [b, G, kStepMaxW, N]
+  int xo;
   float* bfold;
 };
 
@@ -90,10 +91,10 @@ struct M2PrepSmem {
 // (head += n, len = 0) and the token is decoded after them, so the decode
 // terms above use only the token. The fold itself runs in the stream kernel;
 // this warp gives it, from the n entries (n <= kStepMaxW), the fold decay
-// exp(A_h sum_j dt_j) and the coefficients c_j[p] = w_j x_j[p] of every row,
-// and the head's group gets its B_j as floats (read before the token takes
-// the slot of entry 0). The ring pointers are left alone (the stream kernel
-// moves them), so no arrival happens here.
+// exp(A_h sum_j dt_j), the weights w_j (zero past n) and the x row of entry
+// 0, whose slot the token takes, and the head's group gets its B_j as
+// floats (read before the append). The ring pointers are left alone (the
+// stream kernel moves them), so no arrival happens here.
 template <int N, int PT, typename TI, bool STEP>
 __global__ void __launch_bounds__(32 * kPrepWarps) mamba2_prep_kernel(const M2Prep a) {
   extern __shared__ __align__(128) unsigned char smem[];
@@ -158,15 +159,10 @@ __global__ void __launch_bounds__(32 * kPrepWarps) mamba2_prep_kernel(const M2Pr
       hdr[2] = (i_ok ? 1 : 0) | (i_nf << 8);
     }
     if (STEP && i_nf > 0) {
-      // the x rows of the folded entries, oldest first, in the entry rows
-      // (the decode after the fold uses none of them)
-      const int hd0 = (i_hd - i_nf + W) % W;
-      const unsigned char* xs = ringx + (size_t)v * W * row;
-      for (int idx = lane; idx < i_nf * cpr; idx += 32) {
-        const int j = idx / cpr, c = idx - j * cpr;
-        const int slot = hd0 + j < W ? hd0 + j : hd0 + j - W;
-        cp_async16(st + L.xr + j * row + c * 16, xs + slot * row + c * 16);
-      }
+      // the x row of entry 0 of the fold, at row 0 of the (unused) entry rows
+      const int slot0 = (i_hd - i_nf + W) % W;
+      const unsigned char* xs = ringx + ((size_t)v * W + slot0) * row;
+      for (int c = lane; c < cpr; c += 32) cp_async16(st + L.xr + c * 16, xs + c * 16);
     }
     if (i_ok) {
       const unsigned char* xs = ringx + (size_t)v * W * row;
@@ -346,31 +342,10 @@ __global__ void __launch_bounds__(32 * kPrepWarps) mamba2_prep_kernel(const M2Pr
             const float u = __shfl_down_sync(kFull, sfx, o);
             if (lane + o < 32) sfx += u;
           }
-          const float wj = fj * expf(Ah * (sfx - fj));
+          if (lane < kStepMaxW) wrow[P + 2 + lane] = fj * expf(Ah * (sfx - fj));
           if (lane == 0) wrow[P + 1] = expf(Ah * sfx);
-          // coefficients of rows p = 2 lane + {0, 1} (+ 64 k): [P][kStepMaxW]
-          float* pk = a.pack + (size_t)v * P * kStepMaxW;
-          for (int p0 = 0; p0 < P; p0 += 64) {  // every lane runs every iteration
-            const int p = p0 + 2 * lane;
-            const bool act = p < P;
-            float c0[kStepMaxW], c1[kStepMaxW];
-#pragma unroll
-            for (int j = 0; j < kStepMaxW; ++j) {
-              const float w = __shfl_sync(kFull, wj, j);
-              const float2 xv = act && j < nf ? load2<TI>(xr + j * P + p) : make_float2(0.f, 0.f);
-              c0[j] = w * xv.x;
-              c1[j] = w * xv.y;
-            }
-            if (act) {
-              float4* d0 = reinterpret_cast<float4*>(pk + (size_t)p * kStepMaxW);
-#pragma unroll
-              for (int j = 0; j < kStepMaxW; j += 4) {
-                d0[j / 4] = make_float4(c0[j], c0[j + 1], c0[j + 2], c0[j + 3]);
-                d0[kStepMaxW / 4 + j / 4] = make_float4(c1[j], c1[j + 1], c1[j + 2], c1[j + 3]);
-              }
-            }
-          }
-          // the group's B rows, before the token takes the slot of entry 0
+          for (int p = lane; p < P; p += 32) wrow[a.xo + p] = to_f(xr[p]);
+          // the group's B rows as floats
           if (hg == 0) {
             float* Bs = a.bfold + ((size_t)seq * G + g) * kStepMaxW * N;
             for (int j = 0; j < nf; ++j) {
@@ -1002,21 +977,6 @@ cudaError_t launch_mamba2_fold_decode(const replayssm_dims& d, const replayssm_s
   RB = std::min(RB, d.dv);
   while (d.dv % RB) RB -= 32;
   const int GU = RB % 64 == 0 ? 2 : 1;
-  // Each consumer warp takes 32 rows of a unit, and a fold unit's FP32 rows
-  // give each warp whole stages (or share one); the entries must fit the
-  // registers. Otherwise: fold, then decode.
-  if (d.window > kStepMaxW || RB / GU != 32 || (FS > 1 && GU != FS)) {
-    cudaError_t e = launch_mamba2_fold(d, s, A, 1, 0, st);
-    if (e != cudaSuccess) return e;
-    return launch_mamba2_decode(d, s, A, D, x, B, C, dt, y, st);
-  }
-  const StepLayout sl(d);
-  M2Prep p{d.batch, d.heads, d.groups, d.dv, d.window, A, D, x, B, C, dt,
-           s.ring_x, s.ring_B, s.ring_C, s.ring_dt, s.ring_head, s.ring_len, s.status, s.sync,
-           s.work, sl.row, sl.flags(s.work), s.work + sl.pack0, s.work + sl.bf0};
-  cudaError_t e = launch_prep<true>(d, p, st);
-  if (e != cudaSuccess) return e;
-
   const DeviceInfo& dev = device_info();
   const int nrb = d.dv / RB;
   const long long units = (long long)d.batch * d.heads * nrb;
@@ -1024,11 +984,31 @@ cudaError_t launch_mamba2_fold_decode(const replayssm_dims& d, const replayssm_s
   const int grid = (int)std::min<long long>(units, dev.sms);
   const int nloc_max = (int)((units + grid - 1) / grid);  // units of the largest block
   const int threads = 32 * (kStreamGroups * GU + 1);
-  const StepSmem fixed(RB, d.dk, ts, 0, nloc_max);
+  const int xblk = d.window * d.dv * (in16 ? 2 : 4);  // a head's ring x block
+  const StepSmem fixed(RB, d.dk, ts, 0, nloc_max, xblk);
   const size_t per_stage = fixed.stage + fixed.side + 16;
-  if ((size_t)dev.smem_optin < fixed.total + 2048 + 4 * per_stage) return cudaErrorInvalidConfiguration;
-  const int NS = (int)std::min<size_t>((dev.smem_optin - fixed.total - 2048) / per_stage, 12);
-  const size_t smem = StepSmem(RB, d.dk, ts, NS, nloc_max).total;
+  // stages: a multiple of the consumer groups (each owns NS / 4 of them),
+  // at most 12, and each group's share holds a fold unit's FS stages
+  const size_t room = (size_t)dev.smem_optin > fixed.total + 2048
+                          ? ((size_t)dev.smem_optin - fixed.total - 2048) / per_stage : 0;
+  const int NS = (int)std::min<size_t>(room, 12) / kStreamGroups * kStreamGroups;
+  // Each consumer warp takes 32 rows of a unit, and a fold unit's FP32 rows
+  // give each warp whole stages (or share one); the entries must fit the
+  // registers. Otherwise: fold, then decode.
+  if (d.window > kStepMaxW || RB / GU != 32 || (FS > 1 && GU != FS) ||
+      NS < kStreamGroups * FS) {
+    cudaError_t e = launch_mamba2_fold(d, s, A, 1, 0, st);
+    if (e != cudaSuccess) return e;
+    return launch_mamba2_decode(d, s, A, D, x, B, C, dt, y, st);
+  }
+  const size_t smem = StepSmem(RB, d.dk, ts, NS, nloc_max, xblk).total;
+
+  const StepLayout sl(d);
+  M2Prep p{d.batch, d.heads, d.groups, d.dv, d.window, A, D, x, B, C, dt,
+           s.ring_x, s.ring_B, s.ring_C, s.ring_dt, s.ring_head, s.ring_len, s.status, s.sync,
+           s.work, sl.row, sl.flags(s.work), sl.xo, s.work + sl.bf0};
+  cudaError_t e = launch_prep<true>(d, p, st);
+  if (e != cudaSuccess) return e;
 
   StepArgs a{};
   a.batch = d.batch;
@@ -1047,9 +1027,11 @@ cudaError_t launch_mamba2_fold_decode(const replayssm_dims& d, const replayssm_s
   a.out = y;
   a.work = s.work;
   a.wrow = sl.row;
-  a.pack = s.work + sl.pack0;
+  a.xblk = xblk;
+  a.xo = sl.xo;
   a.bfold = s.work + sl.bf0;
   a.C = C;
+  a.ring_x = s.ring_x;
   a.head = s.ring_head;
   a.len = s.ring_len;
   a.status = s.status;

@@ -29,11 +29,12 @@
 // units are done, and the last arrival moves the pointers (fold:
 // head += len, len = 1; else len += 1).
 //
-// Stages are used in unit order (a fold unit takes FS consecutive ones); at
-// block start one warp numbers them, so each unit's entry holds its first
-// stage and that fill's mbarrier parity. The producer streams
-// read-copy rows before the preparation grid ends, but waits for it before
-// the first fold unit (whose coefficients that grid writes).
+// Each consumer group owns R = NS / 4 of the stages and uses them in turn
+// for its units (a fold unit takes FS consecutive ones), so a group only
+// waits for a stage's next fill after it has consumed the previous one and
+// the mbarrier parity of a wait cannot alias an older phase. The producer
+// fills the stages of unit i's group in unit order. It streams state rows
+// before the preparation grid ends; consumers wait for it.
 #pragma once
 
 #include "common.cuh"
@@ -43,29 +44,33 @@
 namespace rs {
 
 struct StepArgs {
-  int batch, H, G, P, W, RB, nrb, NS, GU, nloc_max;
+  int batch, H, G, P, W, RB, nrb, NS, GU, nloc_max, xblk;
   const void* S;        // decode rows: the read copy, or the checkpoint without one
   float* S_ckpt;        // FP32 checkpoint [b, H, P, N]
   bf16* S_read;         // BF16 read copy or null
   float* out;           // y [b, H, P]
   const float* work;    // rows of wrow floats per (sequence, head), StepLayout
   int wrow;
-  const float* pack;    // fold coefficients [b, H, P, kStepMaxW]
+  int xo;               // entry 0's x row in the work row
   const float* bfold;   // folded B rows [b, G, kStepMaxW, N]
-  const void* C;        // [b, G, N]
+  const void* C;        // token input C [b, G, N]
+  const void* ring_x;   // [b, H, W, P]
   int32_t* head;
   int32_t* len;
   int32_t* status;
   int32_t* sync;
 };
 
-// Shared memory: NS stages, NS coefficient side buffers, full and empty
-// barriers, and the kind of each of the block's units.
+// Shared memory: NS stages, NS side buffers, full and empty barriers, and
+// the entry of each of the block's units. A fold unit's first side buffer
+// receives the head's ring x block (W x P inputs); then the side buffer of
+// each of its stages holds the fold coefficients of that stage's FP32 rows.
 struct StepSmem {
   size_t stage, side, sides, bars, table, total;
-  __host__ __device__ StepSmem(int RB, int N, int ts, int NS, int nloc_max) {
+  __host__ __device__ StepSmem(int RB, int N, int ts, int NS, int nloc_max, int xblk) {
     stage = stream_stage_bytes(RB, N, ts);
-    side = (size_t)(RB / (4 / ts)) * kStepMaxW * 4;  // coefficients of a stage's FP32 rows
+    const size_t coefs = (size_t)(RB / (4 / ts)) * kStepMaxW * 4;  // a stage's rows
+    side = align_up((size_t)xblk > coefs ? (size_t)xblk : coefs, 16);
     sides = (size_t)NS * stage;
     bars = sides + (size_t)NS * side;
     table = bars + 2 * (size_t)NS * 8;
@@ -120,7 +125,8 @@ __global__ void __launch_bounds__(kStreamMaxThreads, 1) mamba2_step_stream_kerne
   const int CW = (int)(blockDim.x / 32) - 1;  // consumer warps; the producer is warp CW
   const int GU = a.GU, NG = CW / GU, NS = a.NS, H = a.H, P = a.P, RB = a.RB, nrb = a.nrb;
   const int W = a.W;
-  const StepSmem L(RB, N, sizeof(TS), NS, a.nloc_max);
+  const StepSmem L(RB, N, sizeof(TS), NS, a.nloc_max, a.xblk);
+  const int R = NS / kStreamGroups;  // stages of each consumer group
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bars);
   uint64_t* empty = full + NS;
   int* table = reinterpret_cast<int*>(smem + L.table);
@@ -132,7 +138,7 @@ __global__ void __launch_bounds__(kStreamMaxThreads, 1) mamba2_step_stream_kerne
   // local unit i is unit b0 + i * G0
   const int nloc = units > b0 ? (int)((units - b0 + G0 - 1) / G0) : 0;
   const uint32_t tile_bytes = (uint32_t)((size_t)RB * N * sizeof(TS));
-  const uint32_t side_bytes = (uint32_t)L.side;
+  const uint32_t xblk = (uint32_t)a.xblk;
 
   if (tid == 0) {
     for (int s = 0; s < NS; ++s) {
@@ -142,10 +148,8 @@ __global__ void __launch_bounds__(kStreamMaxThreads, 1) mamba2_step_stream_kerne
     fence_mbar_init();
     abort_flag = 0;
   }
-  // Each local unit's entry: bit 0 pointers valid, bit 1 fold, its first
-  // stage in bits 2..6 and that fill's mbarrier parity in bit 7, len in bits
-  // 8..15, head in bits 16..23. The kinds first, then one warp numbers the
-  // stages in unit order (a fold unit takes FS of them).
+  // Each local unit's entry: bit 0 pointers valid, bit 1 fold, len in bits
+  // 8..15, head in bits 16..23.
   for (int i = tid; i < nloc; i += blockDim.x) {
     const int seq = (b0 + i * G0) / per_seq;
     const int l = a.len[seq], hd = a.head[seq];
@@ -154,65 +158,75 @@ __global__ void __launch_bounds__(kStreamMaxThreads, 1) mamba2_step_stream_kerne
     table[i] = (ok ? 1 : 0) | (fold ? 2 : 0) | (ok ? (l << 8) | (hd << 16) : 0);
   }
   __syncthreads();
-  if (warp == 0) {
-    int base = 0;  // stages of the units before this chunk of 32
-    for (int i0 = 0; i0 < nloc; i0 += 32) {
-      const int i = i0 + lane;
-      const int e = i < nloc ? table[i] : 0;
-      const int n = i < nloc ? ((e & 2) ? FS : 1) : 0;
-      int incl = n;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int t = __shfl_up_sync(kFull, incl, o);
-        if (lane >= o) incl += t;
-      }
-      const int c = base + incl - n;  // stages before unit i
-      if (i < nloc) table[i] = e | ((c % NS) << 2) | (((c / NS) & 1) << 7);
-      base += __shfl_sync(kFull, incl, 31);
-    }
-  }
-  __syncthreads();
 
   if (warp == CW) {
     // ------------------------------------------------------------ producer
     const uint64_t pol = l2_evict_first_policy();
     const TS* Sg = reinterpret_cast<const TS*>(a.S);
-    int s = 0;           // stage of the next fill
-    uint32_t ph = 0;     // parity of that fill (the previous fill of the stage: ph ^ 1)
-    bool reuse = false;  // the stages are being refilled
-    bool stop = false, prep_done = false;
-    for (int i = 0; i < nloc && !stop; ++i) {
-      const int u = b0 + i * G0;
-      const int hg = nrb == 1 ? u : u / nrb, rb = u - hg * nrb;
-      const bool fold = (table[i] & 2) != 0;
-      if (fold && !prep_done) {  // the coefficients come from the preparation grid
-        griddep_wait();
-        prep_done = true;
-      }
-      const int nst = fold ? FS : 1;
-      for (int f = 0; f < nst; ++f) {
-        if (reuse && !mbar_wait_warp(&empty[s], ph ^ 1)) {
-          if (lane == 0) abort_flag = 1;
-          stop = true;
-          break;
-        }
+    // Per consumer group (unit i belongs to group i mod 4): its next unit,
+    // the stages of that unit already issued, its position in its R stages,
+    // the parity of that fill and whether its stages are being refilled. The
+    // groups are served in turn, each whenever its next stage is free, so a
+    // group busy with a fold unit does not hold back the others.
+    int nxt[kStreamGroups], fdone[kStreamGroups] = {}, t[kStreamGroups] = {};
+    uint32_t ph[kStreamGroups] = {};
+    bool reuse[kStreamGroups] = {};
+#pragma unroll
+    for (int gq = 0; gq < kStreamGroups; ++gq) nxt[gq] = gq;
+    int left = nloc;     // units not yet fully issued
+    uint64_t idle0 = 0;  // start of the current stretch without progress
+    while (left > 0) {
+      bool progress = false;
+#pragma unroll
+      for (int gq = 0; gq < kStreamGroups; ++gq) {
+        const int i = nxt[gq];
+        if (i >= nloc) continue;
+        const int s = gq * R + t[gq];
+        const bool room = !reuse[gq] || __shfl_sync(kFull, (int)mbar_try_wait(&empty[s], ph[gq] ^ 1), 0);
+        if (!room) continue;
+        const int u = b0 + i * G0;
+        const int hg = nrb == 1 ? u : u / nrb, rb = u - hg * nrb;
+        const bool fold = (table[i] & 2) != 0;
+        const int f = fdone[gq];
         if (lane == 0) {
           const size_t row = (size_t)hg * P + (size_t)rb * RB;
           if (fold) {
+            // FP32 rows; beside the first stage, the head's ring x block
+            // (the token may or may not have reached entry 0's slot yet:
+            // consumers take entry 0 from the saved row)
             const size_t r0 = row + (size_t)f * (RB / FS);
-            mbar_arrive_expect_tx(&full[s], tile_bytes + side_bytes);
+            mbar_arrive_expect_tx(&full[s], tile_bytes + (f == 0 ? xblk : 0));
             bulk_g2s(smem + (size_t)s * L.stage, a.S_ckpt + r0 * N, tile_bytes, &full[s], pol);
-            bulk_g2s(smem + L.sides + (size_t)s * L.side, a.pack + r0 * kStepMaxW, side_bytes,
-                     &full[s]);
+            if (f == 0)
+              bulk_g2s(smem + L.sides + (size_t)s * L.side,
+                       static_cast<const unsigned char*>(a.ring_x) + (size_t)hg * xblk, xblk,
+                       &full[s]);
           } else {
             mbar_arrive_expect_tx(&full[s], tile_bytes);
             bulk_g2s(smem + (size_t)s * L.stage, Sg + row * N, tile_bytes, &full[s], pol);
           }
         }
-        if (++s == NS) {
-          s = 0;
-          ph ^= 1;
-          reuse = true;
+        if (++t[gq] == R) {
+          t[gq] = 0;
+          ph[gq] ^= 1;
+          reuse[gq] = true;
+        }
+        if (++fdone[gq] == (fold ? FS : 1)) {
+          fdone[gq] = 0;
+          nxt[gq] += kStreamGroups;
+          --left;
+        }
+        progress = true;
+      }
+      if (progress) {
+        idle0 = 0;
+      } else {  // bounded: no stage freed for the wait limit ends the block's work
+        const uint64_t now = global_ns();
+        if (idle0 == 0) {
+          idle0 = now;
+        } else if (now - idle0 > kWaitLimitNs) {
+          if (lane == 0) abort_flag = 1;
+          break;
         }
       }
     }
@@ -237,6 +251,8 @@ __global__ void __launch_bounds__(kStreamMaxThreads, 1) mamba2_step_stream_kerne
     // Work rows and folded B rows come from the preparation grid (this grid
     // may start before it ends).
     griddep_wait();
+    int tg = 0;         // this group's position in its R stages
+    uint32_t phg = 0;   // and the parity of that stage's fill
     for (int i = gi; i < nloc; i += NG) {
       const int u = b0 + i * G0;
       const int hg = nrb == 1 ? u : u / nrb, rb = u - hg * nrb;
@@ -244,8 +260,19 @@ __global__ void __launch_bounds__(kStreamMaxThreads, 1) mamba2_step_stream_kerne
       const int g = h / (H / a.G);
       const int code = table[i];
       const bool ok = (code & 1) != 0, fold = (code & 2) != 0;
-      const int s0 = (code >> 2) & 31;            // the unit's first stage
-      const uint32_t ph0 = (code >> 7) & 1;       // and the parity of its fill
+      // the unit's stages in the group's ring: the first, and for a
+      // two-stage fold unit the next one (wrapping flips the parity)
+      const int s0 = gi * R + tg;
+      const uint32_t ph0 = phg;
+      const bool wrap1 = tg + 1 == R;
+      const int s1 = gi * R + (wrap1 ? 0 : tg + 1);
+      const uint32_t ph1 = wrap1 ? phg ^ 1 : phg;
+      for (int f = 0; f < (fold ? FS : 1); ++f) {
+        if (++tg == R) {
+          tg = 0;
+          phg ^= 1;
+        }
+      }
       const int row0 = rb * RB + part * RBp;  // first row of this warp within the head
       const float* w0 = a.work + (size_t)hg * a.wrow;
       float* yrow = a.out + (size_t)hg * P + row0;
@@ -279,7 +306,7 @@ __global__ void __launch_bounds__(kStreamMaxThreads, 1) mamba2_step_stream_kerne
         if (ok) yrow[RD::row_of(lane)] = fmaf(scale, d, extra);
       } else {
         // ---------------------------------------------------- fold unit
-        const int nf = (code >> 8) & 0xff;
+        const int nf = (code >> 8) & 0xff, hd0 = (code >> 16) & 0xff;
         const float fdec = w0[P + 1];
         // B_j of the head's group, this lane's columns (zero past the n entries)
         const float* Bs = a.bfold + ((size_t)seq * a.G + g) * kStepMaxW * N + cf;
@@ -292,22 +319,50 @@ __global__ void __launch_bounds__(kStreamMaxThreads, 1) mamba2_step_stream_kerne
         load_vec<TV, 4>(Cin + ((size_t)seq * a.G + g) * N + cf, c4);
         const int r = fold_row<RF::kLpr, RF::kRpi, kCS>(lane);
         const float extra = w0[row0 + r];
-        // this warp's stage: the unit's first, or for the second half of a
-        // two-stage unit the next one (wrapping flips the parity)
+        const float x0 = w0[a.xo + row0 + lane];  // entry 0 of this lane's row
+        // this warp's stage: the unit's first, or the second of a two-stage
+        // unit; the first also holds the ring x block, so every warp waits for it
         const bool second = FS > 1 && part == 1;
-        const bool wrap = second && s0 + 1 == NS;
-        const int s = second ? (wrap ? 0 : s0 + 1) : s0;
-        const bool landed = !aborted && mbar_wait_warp(&full[s], wrap ? ph0 ^ 1 : ph0);
+        const int s = second ? s1 : s0;
+        bool landed = !aborted && mbar_wait_warp(&full[s0], ph0);
+        if (second && landed) landed = mbar_wait_warp(&full[s1], ph1);
         if (!aborted && !landed && lane == 0) {
           abort_flag = 1;
           atomicOr(a.status + seq, REPLAYSSM_SEQ_TIMEOUT);
         }
         if (group_any(!landed)) break;
-        // this warp's 32 FP32 rows and their coefficients
-        const int off = FS > 1 ? 0 : part * RBp;
+        // coefficients c_j = w_j x_j of row row0 + lane: entry 0 from the
+        // saved row (the token has taken its slot), entry j > 0 from slot
+        // hd0 + j of the copied ring x block (slots this call does not write)
+        const int off = FS > 1 ? 0 : part * RBp;  // this warp's rows in its stage
+        float* coef = reinterpret_cast<float*>(smem + L.sides + (size_t)s * L.side) +
+                      (size_t)off * kStepMaxW;
+        {
+          const TV* xs = reinterpret_cast<const TV*>(smem + L.sides + (size_t)s0 * L.side);
+          float cj[kStepMaxW];
+#pragma unroll
+          for (int j = 0; j < kStepMaxW; ++j) {
+            float xv = x0;
+            if (j > 0 && j < nf) {
+              const int slot = hd0 + j < W ? hd0 + j : hd0 + j - W;
+              xv = to_f(xs[(size_t)slot * P + row0 + lane]);
+            }
+            cj[j] = j < nf ? w0[P + 2 + j] * xv : 0.f;
+          }
+          // every warp of the unit has read the x block before any
+          // coefficients overwrite it
+          if (GU == 1) {
+            __syncwarp();
+          } else {
+            asm volatile("bar.sync %0, %1;" ::"r"(1 + gi), "r"(32 * GU) : "memory");
+          }
+          float4* dst = reinterpret_cast<float4*>(coef + lane * kStepMaxW);
+#pragma unroll
+          for (int j = 0; j < kStepMaxW; j += 4) dst[j / 4] = make_float4(cj[j], cj[j + 1], cj[j + 2], cj[j + 3]);
+          __syncwarp();
+        }
+        // this warp's 32 FP32 rows
         const float* tile = reinterpret_cast<const float*>(smem + (size_t)s * L.stage) + (size_t)off * N;
-        const float* coef = reinterpret_cast<const float*>(smem + L.sides + (size_t)s * L.side) +
-                            (size_t)off * kStepMaxW;
         // rows in chunks of kCS per lane; lane l ends with the total of row r
         float mine = 0.f;
 #pragma unroll 1
@@ -347,8 +402,10 @@ __global__ void __launch_bounds__(kStreamMaxThreads, 1) mamba2_step_stream_kerne
         }
         yrow[r] = fmaf(scale, mine, extra);
         __syncwarp();
-        if (lane == 0)
-          for (int f = 0; f < FS; ++f) mbar_arrive(&empty[s0 + f < NS ? s0 + f : s0 + f - NS]);
+        if (lane == 0) {
+          mbar_arrive(&empty[s0]);
+          if (FS > 1) mbar_arrive(&empty[s1]);
+        }
       }
     }
   }
