@@ -979,13 +979,38 @@ struct FusedConfig {
 // (more prep warps pay off there), FP32 tiles need 8.
 constexpr int min_stages(int ts) { return ts == 2 ? 4 : 8; }
 
+// Vector slots for NP prep warps: at least NP + 4, a multiple of NP, and
+// with NSL x nrb a multiple of the consumer groups; 0 if no count up to
+// kFMaxSlots has both. Prep warp w takes heads w, w + NP, ..., so with NP
+// dividing NSL every fill of a slot comes from the same warp, in order.
+// Consumer group g takes the heads whose units fall on it (unit = head x nrb
+// + row block), so with NSL x nrb a multiple of the groups its heads repeat
+// every NSL heads and it consumes every fill of each slot it uses. Neither
+// side then waits on a slot whose previous fill it has not seen, so a parity
+// wait can never take an older phase for the one it wants.
+int vector_slots(int NP, int nrb) {
+  auto gcd = [](int x, int y) {
+    while (y) {
+      const int t = x % y;
+      x = y;
+      y = t;
+    }
+    return x;
+  };
+  const int m = kFGroups / gcd(nrb, kFGroups);
+  const int step = NP / gcd(NP, m) * m;  // lcm(NP, m)
+  const int nsl = (NP + 4 + step - 1) / step * step;
+  return nsl <= kFMaxSlots ? nsl : 0;
+}
+
 FusedConfig fused_config(int RB, int DK, int DV, int W, int K, int GU, bool kda, int ts, int ti,
                          size_t optin) {
   FusedConfig best{0, 0, 0, 0, 0};
   const int np_max = kFWarps - 1 - kFGroups * GU;
   for (int depth = 2; depth >= 1; --depth) {
     for (int NP = np_max; NP >= 1; --NP) {
-      const int NSL = std::min(kFMaxSlots, NP + 4);
+      const int NSL = vector_slots(NP, DV / RB);
+      if (NSL == 0) continue;
       const DFusedSmem L0(RB, DK, DV, W, K, 0, NSL, NP, depth, kda, ts, ti);
       const size_t fixed = L0.total + 1024;
       if (fixed >= optin) continue;
@@ -1002,7 +1027,7 @@ FusedConfig fused_config(int RB, int DK, int DV, int W, int K, int GU, bool kda,
     }
   }
   if (best.NP == 0) {  // tight: the fewest stages that still run
-    const int NSL = 5;
+    const int NSL = vector_slots(1, DV / RB);
     const DFusedSmem L0(RB, DK, DV, W, K, 0, NSL, 1, 1, kda, ts, ti);
     const size_t fixed = L0.total + 1024;
     if (fixed < optin) {
@@ -1077,7 +1102,8 @@ cudaError_t launch_delta(const replayssm_dims& d, const replayssm_state& s, int 
 size_t delta_fused_smem(const replayssm_dims& d, int K, bool read16) {
   // the smallest fused block that runs (one prep warp, one stage per group)
   const int ti = d.in_dtype == REPLAYSSM_BF16 ? 2 : 4, ts = read16 ? 2 : 4;
-  return DFusedSmem(fused_rows(d.dk, ts, d.dv), d.dk, d.dv, d.window, K, kFGroups, 5, 1, 1,
+  const int RB = fused_rows(d.dk, ts, d.dv);
+  return DFusedSmem(RB, d.dk, d.dv, d.window, K, kFGroups, vector_slots(1, d.dv / RB), 1, 1,
                     d.kind == REPLAYSSM_KDA, ts, ti).total + 1024;
 }
 
