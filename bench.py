@@ -61,6 +61,23 @@ TRAFFIC_B64 = {
     ("mamba2", "bf16"): 136.526592e6 + 3.470848e6 + 10.205184e6,
     ("gdn", "bf16"): 77.418752e6 + 1.333760e6,
 }
+# The same for one fused Mamba-2 fold + decode call (prep + step stream
+# kernels), averaged over 16 consecutive calls of which one folds every
+# sequence: a sixteenth of the batch folds per call on average, in lockstep
+# or with staggered ring phases alike.
+TRAFFIC_B64_FUSED = {
+    ("mamba2", "bf16"): 178.543408e6,
+}
+
+
+def traffic_per_call(wl: dict, read: str, fused: bool):
+    """DRAM bytes of one decode call at this batch, from the batch-64 captures
+    (None for kernels or shapes without one)."""
+    table = TRAFFIC_B64_FUSED if fused else TRAFFIC_B64
+    key = (wl["kind"], read)
+    if key not in table or wl["heads"] != WORKLOADS[wl["kind"]]["heads"]:
+        return None
+    return round(table[key] * wl["batch"] / 64)
 
 
 def parse(argv=None):
@@ -443,9 +460,7 @@ def run_ours(args, rank, local_rank, world):
             "kernel": layer.decode_kernels(), "bound": "hbm", "achieved": round(achieved, 1),
             "peak": peak, "peak_source": peak_kind, "unit": "GB/s",
             "frac": round(achieved / peak, 4),
-            "traffic": (round(TRAFFIC_B64[(wl["kind"], args.read)] * wl["batch"] / 64)
-                        if (wl["kind"], args.read) in TRAFFIC_B64 and wl["heads"] ==
-                        WORKLOADS[wl["kind"]]["heads"] and not layer.fused else None),
+            "traffic": traffic_per_call(wl, args.read, layer.fused),
             "bytes_per_launch": int(call_bytes / K),
             "avg_launch_us": round(1e3 * sum(dec_ms) / K, 3),
         },
