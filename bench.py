@@ -59,7 +59,7 @@ POOL = 16  # distinct synthetic tokens, cycled through the timed steps
 # it is scaled by batch / 64. Only for the captured kernels.
 TRAFFIC_B64 = {
     ("mamba2", "bf16"): 136.526592e6 + 3.470848e6 + 10.205184e6,
-    ("gdn", "bf16"): 77.418752e6 + 1.333760e6,
+    ("gdn", "bf16"): 77.416192e6 + 1.435392e6,
 }
 # The same for one fused Mamba-2 fold + decode call (prep + step stream
 # kernels), averaged over 16 consecutive calls of which one folds every
