@@ -18,12 +18,15 @@ const DeviceInfo& device_info() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 0;
   std::call_once(once[dev], [dev] {
-    int sms = 0, optin = 0;
+    int sms = 0, optin = 0, per_sm = 0;
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) sms = 148;
     if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
         cudaSuccess)
       optin = 227 * 1024;
-    info[dev] = DeviceInfo{sms, optin};
+    if (cudaDeviceGetAttribute(&per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) !=
+        cudaSuccess)
+      per_sm = 228 * 1024;
+    info[dev] = DeviceInfo{sms, optin, per_sm};
   });
   return info[dev];
 }

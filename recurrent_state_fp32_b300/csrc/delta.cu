@@ -617,16 +617,153 @@ __device__ __forceinline__ void stage_rows_f32(float* dst, const TI* head_rows, 
 
 constexpr int kDFoldThreads = 256;
 
-// Consolidate for the delta-rule layers: one block per folding head (a
-// parallel pre-scan of the pointers lists them). The head's n entries (k, v,
-// gates, beta) are staged as float; each row of S evolves independently,
-//   s <- alpha (.) s;  s <- s + beta (v[r] - s . k) k   for j = 0..n-1
-// (a scalar GDN gate is applied lazily: the row holds s / gam, gam the
-// product of the gates so far, and is rescaled once at the end),
-// so each thread keeps two rows x 32 columns in registers (DK / 32 lanes per
-// row), reads k_j (and a KDA gate row) from shared memory per entry, reduces
-// its partial dot with the row's other lanes, and updates with packed FMAs.
-// Rows are read once and written once (FP32 checkpoint and BF16 read copy).
+// The n-entry fold of two rows of one head held in registers: rows r0 and
+// r1 (r1 only when has1), each spread over DK / 32 lanes, lane q holding the
+// float4 chunks q, q + DK / 32, ... of the row. Each row evolves
+// independently,
+//   s <- alpha (.) s;  s <- s + beta (v[r] - s . k) k   for j = 0..n-1,
+// with the entries (float, entry order) in shared memory. A scalar GDN gate
+// is applied lazily: the row holds s / gam, gam the product of the gates so
+// far, and is rescaled once at the end. k_j (and a KDA gate row) are read
+// from shared memory per use: the lanes of a warp share DK / 32 addresses,
+// so each read is one broadcast.
+template <int DK, bool KDA>
+__device__ __forceinline__ void fold_row_pair(float2 (&s0)[16], float2 (&s1)[16], bool has1,
+                                              int r0, int r1, int n, int DV, int q,
+                                              const float* kbuf, const float* abuf,
+                                              const float* vbuf, const float* bbuf,
+                                              const float* rbuf) {
+  constexpr int LPR = DK / 32;
+  float gam = 1.f, igam = 1.f;  // GDN: product of the gates so far, and its inverse
+  for (int j = 0; j < n; ++j) {
+    const float4* kj = reinterpret_cast<const float4*>(kbuf + (size_t)j * DK) + q;
+    if (KDA) {
+      const float4* aj = reinterpret_cast<const float4*>(abuf + (size_t)j * DK) + q;
+#pragma unroll
+      for (int m = 0; m < 8; ++m) {
+        const float4 u = aj[LPR * m];
+        const float2 g0 = make_float2(u.x, u.y), g1 = make_float2(u.z, u.w);
+        s0[2 * m] = __fmul2_rn(s0[2 * m], g0);
+        s0[2 * m + 1] = __fmul2_rn(s0[2 * m + 1], g1);
+        s1[2 * m] = __fmul2_rn(s1[2 * m], g0);
+        s1[2 * m + 1] = __fmul2_rn(s1[2 * m + 1], g1);
+      }
+    } else {
+      gam *= abuf[j];
+      igam *= rbuf[j];
+    }
+    float dot0, dot1;
+    if (KDA) {
+      float2 d0 = make_float2(0.f, 0.f), d1 = make_float2(0.f, 0.f);
+#pragma unroll
+      for (int m = 0; m < 8; ++m) {
+        const float4 u = kj[LPR * m];
+        const float2 ka = make_float2(u.x, u.y), kb = make_float2(u.z, u.w);
+        d0 = __ffma2_rn(s0[2 * m], ka, d0);
+        d1 = __ffma2_rn(s1[2 * m], ka, d1);
+        d0 = __ffma2_rn(s0[2 * m + 1], kb, d0);
+        d1 = __ffma2_rn(s1[2 * m + 1], kb, d1);
+      }
+      dot0 = d0.x + d0.y;
+      dot1 = d1.x + d1.y;
+    } else {  // two accumulators per row: shorter dependency chains
+      float2 d0 = make_float2(0.f, 0.f), d1 = make_float2(0.f, 0.f);
+      float2 e0 = make_float2(0.f, 0.f), e1 = make_float2(0.f, 0.f);
+#pragma unroll
+      for (int m = 0; m < 8; ++m) {
+        const float4 u = kj[LPR * m];
+        const float2 ka = make_float2(u.x, u.y), kb = make_float2(u.z, u.w);
+        d0 = __ffma2_rn(s0[2 * m], ka, d0);
+        d1 = __ffma2_rn(s1[2 * m], ka, d1);
+        e0 = __ffma2_rn(s0[2 * m + 1], kb, e0);
+        e1 = __ffma2_rn(s1[2 * m + 1], kb, e1);
+      }
+      dot0 = ((d0.x + d0.y) + (e0.x + e0.y)) * gam;
+      dot1 = ((d1.x + d1.y) + (e1.x + e1.y)) * gam;
+    }
+#pragma unroll
+    for (int o = 1; o < LPR; o <<= 1) {
+      dot0 += __shfl_xor_sync(kFull, dot0, o);
+      dot1 += __shfl_xor_sync(kFull, dot1, o);
+    }
+    const float bj = bbuf[j];
+    float c0 = bj * (vbuf[(size_t)j * DV + r0] - dot0);
+    float c1 = has1 ? bj * (vbuf[(size_t)j * DV + r1] - dot1) : 0.f;
+    if (!KDA) {
+      c0 *= igam;
+      c1 *= igam;
+    }
+    const float2 cc0 = make_float2(c0, c0), cc1 = make_float2(c1, c1);
+#pragma unroll
+    for (int m = 0; m < 8; ++m) {
+      const float4 u = kj[LPR * m];
+      const float2 ka = make_float2(u.x, u.y), kb = make_float2(u.z, u.w);
+      s0[2 * m] = __ffma2_rn(cc0, ka, s0[2 * m]);
+      s0[2 * m + 1] = __ffma2_rn(cc0, kb, s0[2 * m + 1]);
+      s1[2 * m] = __ffma2_rn(cc1, ka, s1[2 * m]);
+      s1[2 * m + 1] = __ffma2_rn(cc1, kb, s1[2 * m + 1]);
+    }
+  }
+  if (!KDA) {
+    const float2 gg = make_float2(gam, gam);
+#pragma unroll
+    for (int m = 0; m < 16; ++m) {
+      s0[m] = __fmul2_rn(s0[m], gg);
+      s1[m] = __fmul2_rn(s1[m], gg);
+    }
+  }
+}
+
+// Two rows in the layout of fold_row_pair from a row-major [rows][DK] FP32
+// block (global or shared memory); the second row only when has1.
+template <int DK>
+__device__ __forceinline__ void load_row_pair(const float* row0, const float* row1, bool has1,
+                                              int q, float2 (&s0)[16], float2 (&s1)[16]) {
+  constexpr int LPR = DK / 32;
+  const float4* p0 = reinterpret_cast<const float4*>(row0) + q;
+  const float4* p1 = reinterpret_cast<const float4*>(has1 ? row1 : row0) + q;
+#pragma unroll
+  for (int m = 0; m < 8; ++m) {
+    const float4 u = p0[LPR * m], w = p1[LPR * m];
+    s0[2 * m] = make_float2(u.x, u.y);
+    s0[2 * m + 1] = make_float2(u.z, u.w);
+    s1[2 * m] = make_float2(w.x, w.y);
+    s1[2 * m + 1] = make_float2(w.z, w.w);
+  }
+}
+
+// The folded rows back to the FP32 checkpoint (rows g0 and g1 of S, g1 only
+// when has1) and, when Sr is set, to the BF16 read copy (round to nearest even).
+template <int DK>
+__device__ __forceinline__ void store_row_pair(float* S, bf16* Sr, size_t g0, size_t g1, bool has1,
+                                               int q, const float2 (&s0)[16],
+                                               const float2 (&s1)[16]) {
+  constexpr int LPR = DK / 32;
+  float4* row0 = reinterpret_cast<float4*>(S + g0 * DK) + q;
+  float4* row1 = reinterpret_cast<float4*>(S + g1 * DK) + q;
+#pragma unroll
+  for (int m = 0; m < 8; ++m) {
+    row0[LPR * m] = make_float4(s0[2 * m].x, s0[2 * m].y, s0[2 * m + 1].x, s0[2 * m + 1].y);
+    if (has1) row1[LPR * m] = make_float4(s1[2 * m].x, s1[2 * m].y, s1[2 * m + 1].x, s1[2 * m + 1].y);
+  }
+  if (Sr) {
+    uint2* rr0 = reinterpret_cast<uint2*>(Sr + g0 * DK) + q;
+    uint2* rr1 = reinterpret_cast<uint2*>(Sr + g1 * DK) + q;
+#pragma unroll
+    for (int m = 0; m < 8; ++m) {
+      rr0[LPR * m] = make_uint2(pack_bf16x2(s0[2 * m].x, s0[2 * m].y), pack_bf16x2(s0[2 * m + 1].x, s0[2 * m + 1].y));
+      if (has1)
+        rr1[LPR * m] = make_uint2(pack_bf16x2(s1[2 * m].x, s1[2 * m].y), pack_bf16x2(s1[2 * m + 1].x, s1[2 * m + 1].y));
+    }
+  }
+}
+
+// Consolidate for the delta-rule layers, synchronous form: one block per
+// folding head (a parallel pre-scan of the pointers lists them). The head's
+// n entries (k, v, gates, beta) are staged as float, then each thread folds
+// two rows x DK / 32 columns in registers (fold_row_pair). Rows are read
+// once and written once (FP32 checkpoint and BF16 read copy). Used where the
+// prefetching form below does not fit two blocks per SM.
 template <int DK, typename TI, bool KDA>
 __global__ void __launch_bounds__(kDFoldThreads, 2) delta_fold_kernel(const DFold a) {
   extern __shared__ __align__(128) unsigned char smem[];
@@ -663,113 +800,11 @@ __global__ void __launch_bounds__(kDFoldThreads, 2) delta_fold_kernel(const DFol
     for (int r0 = rs; r0 < DV; r0 += 2 * SLOTS) {
       const int r1 = r0 + SLOTS;
       const bool has1 = r1 < DV;
-      float4* row0 = reinterpret_cast<float4*>(a.S + ((size_t)t * DV + r0) * DK) + q;
-      float4* row1 = reinterpret_cast<float4*>(a.S + ((size_t)t * DV + (has1 ? r1 : r0)) * DK) + q;
+      const size_t g0 = (size_t)t * DV + r0, g1 = (size_t)t * DV + (has1 ? r1 : r0);
       float2 s0[16], s1[16];
-#pragma unroll
-      for (int m = 0; m < 8; ++m) {
-        const float4 u = row0[LPR * m], w = row1[LPR * m];
-        s0[2 * m] = make_float2(u.x, u.y);
-        s0[2 * m + 1] = make_float2(u.z, u.w);
-        s1[2 * m] = make_float2(w.x, w.y);
-        s1[2 * m + 1] = make_float2(w.z, w.w);
-      }
-      float gam = 1.f, igam = 1.f;  // GDN: product of the gates so far, and its inverse
-      for (int j = 0; j < n; ++j) {
-        // k_j (and a KDA gate row) are read from shared memory per use: the
-        // lanes of a warp share 4 addresses, so each read is one broadcast
-        const float4* kj = reinterpret_cast<const float4*>(kbuf + (size_t)j * DK) + q;
-        if (KDA) {
-          const float4* aj = reinterpret_cast<const float4*>(abuf + (size_t)j * DK) + q;
-#pragma unroll
-          for (int m = 0; m < 8; ++m) {
-            const float4 u = aj[LPR * m];
-            const float2 g0 = make_float2(u.x, u.y), g1 = make_float2(u.z, u.w);
-            s0[2 * m] = __fmul2_rn(s0[2 * m], g0);
-            s0[2 * m + 1] = __fmul2_rn(s0[2 * m + 1], g1);
-            s1[2 * m] = __fmul2_rn(s1[2 * m], g0);
-            s1[2 * m + 1] = __fmul2_rn(s1[2 * m + 1], g1);
-          }
-        } else {
-          // scalar gate, applied lazily: the rows hold s / gam
-          gam *= abuf[j];
-          igam *= rbuf[j];
-        }
-        float dot0, dot1;
-        if (KDA) {
-          float2 d0 = make_float2(0.f, 0.f), d1 = make_float2(0.f, 0.f);
-#pragma unroll
-          for (int m = 0; m < 8; ++m) {
-            const float4 u = kj[LPR * m];
-            const float2 ka = make_float2(u.x, u.y), kb = make_float2(u.z, u.w);
-            d0 = __ffma2_rn(s0[2 * m], ka, d0);
-            d1 = __ffma2_rn(s1[2 * m], ka, d1);
-            d0 = __ffma2_rn(s0[2 * m + 1], kb, d0);
-            d1 = __ffma2_rn(s1[2 * m + 1], kb, d1);
-          }
-          dot0 = d0.x + d0.y;
-          dot1 = d1.x + d1.y;
-        } else {  // two accumulators per row: shorter dependency chains
-          float2 d0 = make_float2(0.f, 0.f), d1 = make_float2(0.f, 0.f);
-          float2 e0 = make_float2(0.f, 0.f), e1 = make_float2(0.f, 0.f);
-#pragma unroll
-          for (int m = 0; m < 8; ++m) {
-            const float4 u = kj[LPR * m];
-            const float2 ka = make_float2(u.x, u.y), kb = make_float2(u.z, u.w);
-            d0 = __ffma2_rn(s0[2 * m], ka, d0);
-            d1 = __ffma2_rn(s1[2 * m], ka, d1);
-            e0 = __ffma2_rn(s0[2 * m + 1], kb, e0);
-            e1 = __ffma2_rn(s1[2 * m + 1], kb, e1);
-          }
-          dot0 = ((d0.x + d0.y) + (e0.x + e0.y)) * gam;
-          dot1 = ((d1.x + d1.y) + (e1.x + e1.y)) * gam;
-        }
-#pragma unroll
-        for (int o = 1; o < LPR; o <<= 1) {
-          dot0 += __shfl_xor_sync(kFull, dot0, o);
-          dot1 += __shfl_xor_sync(kFull, dot1, o);
-        }
-        const float bj = bbuf[j];
-        float c0 = bj * (vbuf[(size_t)j * DV + r0] - dot0);
-        float c1 = has1 ? bj * (vbuf[(size_t)j * DV + r1] - dot1) : 0.f;
-        if (!KDA) {
-          c0 *= igam;
-          c1 *= igam;
-        }
-        const float2 cc0 = make_float2(c0, c0), cc1 = make_float2(c1, c1);
-#pragma unroll
-        for (int m = 0; m < 8; ++m) {
-          const float4 u = kj[LPR * m];
-          const float2 ka = make_float2(u.x, u.y), kb = make_float2(u.z, u.w);
-          s0[2 * m] = __ffma2_rn(cc0, ka, s0[2 * m]);
-          s0[2 * m + 1] = __ffma2_rn(cc0, kb, s0[2 * m + 1]);
-          s1[2 * m] = __ffma2_rn(cc1, ka, s1[2 * m]);
-          s1[2 * m + 1] = __ffma2_rn(cc1, kb, s1[2 * m + 1]);
-        }
-      }
-      if (!KDA) {
-        const float2 gg = make_float2(gam, gam);
-#pragma unroll
-        for (int m = 0; m < 16; ++m) {
-          s0[m] = __fmul2_rn(s0[m], gg);
-          s1[m] = __fmul2_rn(s1[m], gg);
-        }
-      }
-#pragma unroll
-      for (int m = 0; m < 8; ++m) {
-        row0[LPR * m] = make_float4(s0[2 * m].x, s0[2 * m].y, s0[2 * m + 1].x, s0[2 * m + 1].y);
-        if (has1) row1[LPR * m] = make_float4(s1[2 * m].x, s1[2 * m].y, s1[2 * m + 1].x, s1[2 * m + 1].y);
-      }
-      if (a.Sr) {
-        uint2* rr0 = reinterpret_cast<uint2*>(a.Sr + ((size_t)t * DV + r0) * DK) + q;
-        uint2* rr1 = reinterpret_cast<uint2*>(a.Sr + ((size_t)t * DV + (has1 ? r1 : r0)) * DK) + q;
-#pragma unroll
-        for (int m = 0; m < 8; ++m) {
-          rr0[LPR * m] = make_uint2(pack_bf16x2(s0[2 * m].x, s0[2 * m].y), pack_bf16x2(s0[2 * m + 1].x, s0[2 * m + 1].y));
-          if (has1)
-            rr1[LPR * m] = make_uint2(pack_bf16x2(s1[2 * m].x, s1[2 * m].y), pack_bf16x2(s1[2 * m + 1].x, s1[2 * m + 1].y));
-        }
-      }
+      load_row_pair<DK>(a.S + g0 * DK, a.S + g1 * DK, has1, q, s0, s1);
+      fold_row_pair<DK, KDA>(s0, s1, has1, r0, r1, n, DV, q, kbuf, abuf, vbuf, bbuf, rbuf);
+      store_row_pair<DK>(a.S, a.Sr, g0, g1, has1, q, s0, s1);
     }
     __syncthreads();
     if (tid == 0)
@@ -777,6 +812,191 @@ __global__ void __launch_bounds__(kDFoldThreads, 2) delta_fold_kernel(const DFol
         a.head[seq] = (hd + n) % W;
         a.len[seq] = 0;
       });
+  }
+}
+
+// Rows of the prefetching fold: one row chunk of a head per unit, the rows
+// that one pass of the block's threads holds (two per row slot).
+__host__ __device__ constexpr int fold_chunk_rows(int DK, int DV) {
+  return DV < 2 * kDFoldThreads * 32 / DK ? DV : 2 * kDFoldThreads * 32 / DK;
+}
+
+__host__ __device__ inline size_t smem_take(size_t& o, size_t bytes) {
+  const size_t at = o;
+  o = align_up(o + bytes, 128);
+  return at;
+}
+
+// Shared-memory layout of the prefetching fold (byte offsets): the staged
+// row chunk of S; the next unit's raw ring entries (k, v, KDA gate rows in
+// entry order; the scalar fields' whole [Wd] blocks in slot order); the
+// current unit's entries widened to float; one mbarrier.
+struct DFoldSmem {
+  size_t s, kraw, vraw, araw, braw, kbuf, abuf, vbuf, bbuf, rbuf, bar, total;
+  __host__ __device__ DFoldSmem(int DK, int DV, int W, int ti, bool kda) {
+    const size_t R = fold_chunk_rows(DK, DV), Wd = ring_wd(W);
+    size_t o = 0;
+    s = smem_take(o, R * DK * 4);
+    kraw = smem_take(o, (size_t)W * DK * ti);
+    vraw = smem_take(o, (size_t)W * DV * ti);
+    araw = smem_take(o, kda ? (size_t)W * DK * 4 : Wd * 4);
+    braw = smem_take(o, Wd * 4);
+    kbuf = smem_take(o, (size_t)W * DK * 4);
+    abuf = smem_take(o, kda ? (size_t)W * DK * 4 : (size_t)W * 4);
+    vbuf = smem_take(o, (size_t)W * DV * 4);
+    bbuf = smem_take(o, (size_t)W * 4);
+    rbuf = smem_take(o, (size_t)W * 4);
+    bar = smem_take(o, 8);
+    total = o;
+  }
+};
+
+// Ring rows of `cols` elements of entries 0..n-1 of one head (entry j in
+// slot (hd + j) mod W of the head's [W][cols] block) into dst [n][cols] with
+// 16-byte cp.async from every thread (cols * sizeof(T) a multiple of 16).
+template <typename T>
+__device__ __forceinline__ void prefetch_ring_rows(T* dst, const T* head_rows, int cols, int n,
+                                                   int hd, int W) {
+  constexpr int epc = 16 / (int)sizeof(T);
+  const int cpr = cols / epc;
+  for (int idx = threadIdx.x; idx < n * cpr; idx += blockDim.x) {
+    const int j = idx / cpr, c = idx - j * cpr;
+    const int slot = hd + j < W ? hd + j : hd + j - W;
+    cp_async16(dst + (size_t)j * cols + c * epc, head_rows + (size_t)slot * cols + c * epc);
+  }
+}
+
+// `count` elements (a multiple of 16 bytes' worth) of shared memory widened to float.
+template <typename T>
+__device__ __forceinline__ void widen_smem(float* dst, const T* src, int count) {
+  constexpr int epc = 16 / (int)sizeof(T);
+  for (int idx = threadIdx.x; idx < count / epc; idx += blockDim.x) {
+    float f[epc];
+    unpack<T>(reinterpret_cast<const uint4*>(src)[idx], f);
+    float4* d = reinterpret_cast<float4*>(dst + (size_t)idx * epc);
+#pragma unroll
+    for (int e = 0; e < epc / 4; ++e) d[e] = make_float4(f[4 * e], f[4 * e + 1], f[4 * e + 2], f[4 * e + 3]);
+  }
+}
+
+// Consolidate for the delta-rule layers, prefetching form. The same fold as
+// delta_fold_kernel on units of (folding head, row chunk), but the next
+// unit's row chunk (one bulk copy, completion on an mbarrier) and ring
+// entries (cp.async) are in flight while the block folds the current one, so
+// the state stream overlaps the serial per-entry arithmetic. Per unit:
+// wait for its copies; widen its entries to float; move its rows from shared
+// memory to registers; barrier; issue the next unit's copies; fold and store.
+// Each unit's arrival on the sequence's counter comes after the barrier that
+// follows its stores; the last of the H x chunks arrivals moves the pointers.
+template <int DK, typename TI, bool KDA>
+__global__ void __launch_bounds__(kDFoldThreads, 2) delta_fold_stream_kernel(const DFold a) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  __shared__ FoldList fl;
+  constexpr int LPR = DK / 32;                 // lanes per row
+  constexpr int SLOTS = kDFoldThreads / LPR;   // row slots per pass
+  const int tid = threadIdx.x, q = tid % LPR, rs = tid / LPR;
+  const int H = a.H, DV = a.DV, W = a.W, Wd = ring_wd(W);
+  const int R = fold_chunk_rows(DK, DV), nch = (DV + R - 1) / R;
+  const DFoldSmem L(DK, DV, W, (int)sizeof(TI), KDA);
+  float* sS = reinterpret_cast<float*>(smem + L.s);
+  TI* kraw = reinterpret_cast<TI*>(smem + L.kraw);
+  TI* vraw = reinterpret_cast<TI*>(smem + L.vraw);
+  float* araw = reinterpret_cast<float*>(smem + L.araw);
+  float* braw = reinterpret_cast<float*>(smem + L.braw);
+  float* kbuf = reinterpret_cast<float*>(smem + L.kbuf);
+  float* abuf = reinterpret_cast<float*>(smem + L.abuf);
+  float* vbuf = reinterpret_cast<float*>(smem + L.vbuf);
+  float* bbuf = reinterpret_cast<float*>(smem + L.bbuf);
+  float* rbuf = reinterpret_cast<float*>(smem + L.rbuf);
+  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + L.bar);
+  const TI* rk = reinterpret_cast<const TI*>(a.ring_k);
+  const TI* rv = reinterpret_cast<const TI*>(a.ring_v);
+  const uint64_t pol = l2_evict_first_policy();
+
+  if (tid == 0) {
+    mbar_init(bar, 1);
+    fence_mbar_init();
+  }
+  // (its barriers also publish the mbarrier's initialisation)
+  collect_folds(fl, (long long)a.batch * H, H, a.len, a.head, a.status, W, a.k_next, a.force);
+  const int units = fl.count * nch;
+
+  auto issue = [&](int u) {
+    const int f = u / nch, c0 = (u - f * nch) * R;
+    const int t = fl.tile[f], n = fl.len[f], hd = fl.head[f];
+    const int rows = DV - c0 < R ? DV - c0 : R;
+    if (tid == 0) {
+      const uint32_t bytes = (uint32_t)rows * DK * 4;
+      mbar_arrive_expect_tx(bar, bytes);
+      bulk_g2s(sS, a.S + ((size_t)t * DV + c0) * DK, bytes, bar, pol);
+    }
+    prefetch_ring_rows<TI>(kraw, rk + (size_t)t * W * DK, DK, n, hd, W);
+    prefetch_ring_rows<TI>(vraw, rv + (size_t)t * W * DV, DV, n, hd, W);
+    if (KDA) prefetch_ring_rows<float>(araw, a.ring_alpha + (size_t)t * W * DK, DK, n, hd, W);
+    for (int i = tid; i < Wd / 4; i += kDFoldThreads) {
+      cp_async16(braw + 4 * i, a.ring_beta + (size_t)t * Wd + 4 * i);
+      if (!KDA) cp_async16(araw + 4 * i, a.ring_alpha + (size_t)t * Wd + 4 * i);
+    }
+    cp_async_commit();
+  };
+  // the last arrival of a sequence's units moves its pointers
+  auto arrive = [&](int u) {
+    const int f = u / nch;
+    const int seq = fl.tile[f] / H, hd = fl.head[f], n = fl.len[f];
+    arrive_and_finish(a.sync + seq, 1, H * nch, [&] {
+      a.head[seq] = (hd + n) % W;
+      a.len[seq] = 0;
+    });
+  };
+
+  if (units > 0) issue(0);
+  uint32_t ph = 0;
+  for (int u = 0; u < units; ++u) {
+    const int f = u / nch, c0 = (u - f * nch) * R;
+    const int t = fl.tile[f], n = fl.len[f], hd = fl.head[f];
+    const int rows = DV - c0 < R ? DV - c0 : R;
+    cp_async_wait_all();
+    const bool landed = mbar_wait(bar, ph);
+    // unit u's copies are visible to every thread, and every thread is done
+    // with unit u - 1 (its float entries, its stores)
+    const bool ok = __syncthreads_and(landed) != 0;
+    if (tid == 0 && u > 0) arrive(u - 1);
+    if (!ok) {
+      if (tid == 0) {
+        for (int g = f; g < fl.count; ++g) atomicOr(a.status + fl.tile[g] / H, REPLAYSSM_SEQ_TIMEOUT);
+        mbar_wait(bar, ph);  // no bulk copy may land after the block exits
+      }
+      return;
+    }
+    ph ^= 1;
+    widen_smem<TI>(kbuf, kraw, n * DK);
+    widen_smem<TI>(vbuf, vraw, n * DV);
+    if (KDA) widen_smem<float>(abuf, araw, n * DK);
+    for (int j = tid; j < n; j += kDFoldThreads) {
+      const int slot = hd + j < W ? hd + j : hd + j - W;
+      bbuf[j] = braw[slot];
+      if (!KDA) {
+        const float al = araw[slot];
+        abuf[j] = al;
+        rbuf[j] = 1.f / al;
+      }
+    }
+    // rows is a multiple of 32, so both flags are uniform over each warp
+    const bool has0 = rs < rows, has1 = rs + SLOTS < rows;
+    float2 s0[16], s1[16];
+    if (has0) load_row_pair<DK>(sS + (size_t)rs * DK, sS + (size_t)(rs + SLOTS) * DK, has1, q, s0, s1);
+    __syncthreads();  // entries widened; the staged chunk and raw entries are free
+    if (u + 1 < units) issue(u + 1);
+    if (has0) {
+      const int r0 = c0 + rs, r1 = r0 + SLOTS;
+      const size_t g0 = (size_t)t * DV + r0, g1 = (size_t)t * DV + (has1 ? r1 : r0);
+      fold_row_pair<DK, KDA>(s0, s1, has1, r0, r1, n, DV, q, kbuf, abuf, vbuf, bbuf, rbuf);
+      store_row_pair<DK>(a.S, a.Sr, g0, g1, has1, q, s0, s1);
+    }
+  }
+  if (units > 0) {
+    __syncthreads();
+    if (tid == 0) arrive(units - 1);
   }
 }
 
@@ -1125,19 +1345,35 @@ cudaError_t launch_delta_fold(const replayssm_dims& d, const replayssm_state& s,
           reinterpret_cast<bf16*>(s.S_read), s.ring_k, s.ring_v, s.ring_alpha, s.ring_beta,
           s.ring_head, s.ring_len, s.status, s.sync};
   const bool kda = d.kind == REPLAYSSM_KDA;
-  const size_t smem = 4 * ((size_t)d.window * d.dk + align_up((size_t)d.window * (kda ? d.dk : 1), 4) +
-                           (size_t)d.window * d.dv + 2 * (size_t)d.window);
+  const bool in16 = d.in_dtype == REPLAYSSM_BF16;
+  const DeviceInfo& dev = device_info();
   const long long heads = (long long)d.batch * d.heads;
   const int grid = (int)std::max<long long>((heads + kMaxFoldTiles - 1) / kMaxFoldTiles,
-                                            std::min<long long>(heads, (long long)device_info().sms * 2));
-  const bool in16 = d.in_dtype == REPLAYSSM_BF16;
+                                            std::min<long long>(heads, (long long)dev.sms * 2));
+  // The prefetching form where two of its blocks fit on an SM (static fold
+  // list and the per-block reservation included), else the synchronous one.
+  const DFoldSmem L(d.dk, d.dv, d.window, in16 ? 2 : 4, kda);
+  const bool prefetch = 2 * (L.total + sizeof(FoldList) + 1024) <= (size_t)dev.smem_sm;
   void (*kern)(const DFold);
-  if (d.dk == 128)
-    kern = in16 ? (kda ? delta_fold_kernel<128, bf16, true> : delta_fold_kernel<128, bf16, false>)
-                : (kda ? delta_fold_kernel<128, float, true> : delta_fold_kernel<128, float, false>);
-  else
-    kern = in16 ? (kda ? delta_fold_kernel<64, bf16, true> : delta_fold_kernel<64, bf16, false>)
-                : (kda ? delta_fold_kernel<64, float, true> : delta_fold_kernel<64, float, false>);
+  size_t smem;
+  if (prefetch) {
+    smem = L.total;
+    if (d.dk == 128)
+      kern = in16 ? (kda ? delta_fold_stream_kernel<128, bf16, true> : delta_fold_stream_kernel<128, bf16, false>)
+                  : (kda ? delta_fold_stream_kernel<128, float, true> : delta_fold_stream_kernel<128, float, false>);
+    else
+      kern = in16 ? (kda ? delta_fold_stream_kernel<64, bf16, true> : delta_fold_stream_kernel<64, bf16, false>)
+                  : (kda ? delta_fold_stream_kernel<64, float, true> : delta_fold_stream_kernel<64, float, false>);
+  } else {
+    smem = 4 * ((size_t)d.window * d.dk + align_up((size_t)d.window * (kda ? d.dk : 1), 4) +
+                (size_t)d.window * d.dv + 2 * (size_t)d.window);
+    if (d.dk == 128)
+      kern = in16 ? (kda ? delta_fold_kernel<128, bf16, true> : delta_fold_kernel<128, bf16, false>)
+                  : (kda ? delta_fold_kernel<128, float, true> : delta_fold_kernel<128, float, false>);
+    else
+      kern = in16 ? (kda ? delta_fold_kernel<64, bf16, true> : delta_fold_kernel<64, bf16, false>)
+                  : (kda ? delta_fold_kernel<64, float, true> : delta_fold_kernel<64, float, false>);
+  }
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   kern<<<grid, kDFoldThreads, smem, st>>>(a);

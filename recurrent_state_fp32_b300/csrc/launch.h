@@ -54,7 +54,8 @@ struct StepLayout {
 // Device facts cached per device (SM count, opt-in shared memory per block).
 struct DeviceInfo {
   int sms;
-  int smem_optin;
+  int smem_optin;  // shared memory one block may opt in to
+  int smem_sm;     // shared memory per SM, all resident blocks together
 };
 const DeviceInfo& device_info();
 

@@ -51,6 +51,23 @@ def test_small_batch_row_split(batch):
     run(Session("kda", wl, "bf16"), wl.steps, check_every=5)
 
 
+def test_fold_row_chunks():
+    """d_v = 160 at d_k = 128: each folding head is two row chunks (128 + 32
+    rows) of the prefetching consolidate, each unit re-staging the ring."""
+    wl = synth.DeltaWorkload("gdn", batch=3, heads=3, dk=128, dv=160, window=16, steps=36,
+                             in_dtype="bf16", seed=16)
+    run(Session("gdn", wl, "bf16"), wl.steps, check_every=7)
+
+
+def test_fold_synchronous_form():
+    """KDA with FP32 inputs at W = 16 (and W = 40) needs more shared memory
+    than two prefetching fold blocks per SM allow: the synchronous fold runs."""
+    for window, steps in ((16, 36), (40, 84)):
+        wl = synth.DeltaWorkload("kda", batch=3, heads=2, dk=128, dv=128, window=window,
+                                 steps=steps, in_dtype="f32", seed=17)
+        run(Session("kda", wl, "bf16"), wl.steps, check_every=11)
+
+
 def test_window_one_and_no_optional_fields():
     wl = synth.DeltaWorkload("gdn", batch=2, heads=3, dk=128, dv=64, window=1, steps=8, seed=14)
     run(Session("gdn", wl, "f32", store_optional=False), wl.steps, check_every=1)
