@@ -59,13 +59,16 @@ def test_fold_row_chunks():
     run(Session("gdn", wl, "bf16"), wl.steps, check_every=7)
 
 
-def test_fold_synchronous_form():
-    """KDA with FP32 inputs at W = 16 (and W = 40) needs more shared memory
-    than two prefetching fold blocks per SM allow: the synchronous fold runs."""
-    for window, steps in ((16, 36), (40, 84)):
-        wl = synth.DeltaWorkload("kda", batch=3, heads=2, dk=128, dv=128, window=window,
-                                 steps=steps, in_dtype="f32", seed=17)
-        run(Session("kda", wl, "bf16"), wl.steps, check_every=11)
+@pytest.mark.parametrize("kind,window,in_dtype,steps", [
+    ("gdn", 20, "bf16", 44),   # a longer ring, still prefetched
+    ("kda", 16, "f32", 36),    # staging too large for two blocks per SM: synchronous fold
+    ("kda", 40, "f32", 84),    # synchronous fold, longer ring
+])
+def test_fold_forms(kind, window, in_dtype, steps):
+    """Consolidate shapes on both sides of the prefetching fold's shared-memory limit."""
+    wl = synth.DeltaWorkload(kind, batch=3, heads=2, dk=128, dv=128, window=window,
+                             steps=steps, in_dtype=in_dtype, seed=17)
+    run(Session(kind, wl, "bf16"), wl.steps, check_every=11)
 
 
 def test_window_one_and_no_optional_fields():
