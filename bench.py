@@ -184,9 +184,11 @@ class ClockSampler:
     def __enter__(self):
         try:
             self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            # lowest CPU priority and a 200 ms period: the sampler must not
+            # delay the host thread that enqueues the timed launches
             self.proc = subprocess.Popen(
-                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.Q}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                ["nice", "-n", "19", "nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
                 stdout=self.file, stderr=subprocess.DEVNULL)
             time.sleep(0.3)
         except OSError:
