@@ -54,11 +54,6 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
-__device__ __forceinline__ void mbar_arrive_cnt(uint64_t* bar, uint32_t count) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
-               : "memory");
-}
-
 // Per-thread asynchronous copies global -> shared (completion: cp_async_wait_all).
 __device__ __forceinline__ void cp_async4(void* dst, const void* src) {
   asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst)), "l"(src)
@@ -166,9 +161,6 @@ __device__ __forceinline__ float to_f<bf16>(bf16 v) {
   return __bfloat162float(v);
 }
 
-// exp with full float accuracy (the library's expf).
-__device__ __forceinline__ float __expf_acc(float x) { return expf(x); }
-
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
@@ -250,21 +242,7 @@ __device__ __forceinline__ void block_copy_warp(void* dst, const void* src, int 
   for (int i = lane; i < bytes / 16; i += 32) d[i] = s[i];
 }
 
-// Copies `bytes` (a multiple of 16) between 16-byte aligned buffers with
-// every thread of the block taking strided 16-byte chunks.
-__device__ __forceinline__ void block_copy16(void* dst, const void* src, int bytes) {
-  const uint4* s = reinterpret_cast<const uint4*>(src);
-  uint4* d = reinterpret_cast<uint4*>(dst);
-  for (int i = threadIdx.x; i < (bytes >> 4); i += blockDim.x) d[i] = s[i];
-}
-
 // ------------------------------------------------------------ reductions
-
-__device__ __forceinline__ float warp_sum(float v) {
-#pragma unroll
-  for (int o = 16; o >= 1; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
-  return v;
-}
 
 // Reduce-scatter across groups of L lanes: lane l holds L partial sums
 // v[0..L-1]; on return lane l holds the total, over its group, of partial
