@@ -156,6 +156,39 @@ def restart_keeps_length(self, seqs, S0):
     self.status[seqs] = 0
 
 
+def spec_verify_unchained(self, K, drafts):
+    """Every draft stepped from the committed state: drafts blind to each other."""
+    ok = self.len + K <= self.W
+    self.status[~ok] |= om.RING_FULL
+    outs, states = [], []
+    for i in range(K):
+        tok = {k: np.asarray(v)[:, i] for k, v in drafts.items()}
+        self._write(ok, (self.head + self.len + i) % self.W, tok)
+        S, o = self._step(self.committed, tok)
+        outs.append(o)
+        states.append(S)
+    out = np.stack(outs, axis=1)
+    out[~ok] = np.nan
+    self._drafts, self._verified = states, ok
+    return out
+
+
+_orig_accept = om.ReplayOracle.accept
+
+
+def accept_moves_by_K(self, m, K):
+    """The pointer advances over every verified draft, accepted or not."""
+    _orig_accept(self, m, K)
+    m = np.asarray(m, np.int64)
+    good = (m >= 0) & (m <= K)
+    self.len[good] += (K - m[good]).astype(np.int32)
+
+
+def accept_clamps_silently(self, m, K):
+    """An out-of-range accept count is clamped instead of flagged."""
+    _orig_accept(self, np.clip(np.asarray(m, np.int64), 0, K), K)
+
+
 MUTANTS = [
     (rec, "mamba2_step", m2_no_skip),
     (rec, "mamba2_step", m2_old_state_output),
@@ -176,6 +209,9 @@ MUTANTS = [
     (om.ReplayOracle, "_write", write_next_slot),
     (om.ReplayOracle, "restart", restart_keeps_checkpoint),
     (om.ReplayOracle, "restart", restart_keeps_length),
+    (om.ReplayOracle, "spec_verify", spec_verify_unchained),
+    (om.ReplayOracle, "accept", accept_moves_by_K),
+    (om.ReplayOracle, "accept", accept_clamps_silently),
 ]
 
 
