@@ -127,8 +127,14 @@ class LayerState:
         return self._c
 
     def set_checkpoint(self, S: torch.Tensor, stream=None) -> None:
-        """Copies S into the FP32 checkpoint and refreshes the read copy."""
-        self.S_ckpt.copy_(S)
+        """Copies S into the FP32 checkpoint and refreshes the read copy, both on
+        `stream` (default: the current stream), so the refresh sees the copy."""
+        if stream is None:
+            self.S_ckpt.copy_(S)
+        else:
+            s = stream if isinstance(stream, torch.cuda.Stream) else torch.cuda.ExternalStream(int(stream))
+            with torch.cuda.stream(s):
+                self.S_ckpt.copy_(S)
         if self.S_read is not None:
             refresh_read_copy(self.dims, self, stream)
 
