@@ -68,6 +68,14 @@ def _stream(stream) -> int | None:
     return int(stream)
 
 
+def _int32(t, name: str):
+    """Index and count tensors are int32 [n] on the device; anything else
+    would be misread by the kernels, so it is refused here."""
+    if not isinstance(t, torch.Tensor) or t.dtype != torch.int32:
+        raise TypeError(f"{name} must be an int32 tensor")
+    return t
+
+
 def ring_wd(W: int) -> int:
     """Entries per (sequence, head) of a scalar ring field: W rounded up to 4."""
     return (W + 3) & ~3
@@ -196,6 +204,9 @@ def mamba2_spec_verify(dims, state, K, A, D, x, B, C, dt, y, stream=None):
 
 
 def accept(dims, state, m, K, stream=None):
+    _int32(m, "m")
+    if m.numel() != dims.batch:
+        raise ValueError("m must hold one count per sequence")
     d, s = _refs(dims, state)
     _call("replayssm_accept", d, s, _ptr(m), int(K), _stream(stream))
 
@@ -224,13 +235,18 @@ def conventional_gdn_verify(dims, S, K, q, k, v, alpha, beta, scale, snapshots, 
 
 def conventional_accept(dims, S, snapshots, m, K, status=None, stream=None):
     """Baseline accept: S = snapshot m - 1 per sequence (m = 0: unchanged)."""
+    _int32(m, "m")
+    if m.numel() != dims.batch:
+        raise ValueError("m must hold one count per sequence")
     _call("replayssm_conventional_accept", ctypes.byref(dims.c()), _ptr(S), _ptr(snapshots),
           _ptr(m), int(K), _ptr(status), _stream(stream))
 
 
 def copy_sequences(dims, src, src_idx, dst, dst_idx, stream=None):
     """Copy whole sequences (checkpoint, read copy, ring, pointers) between states."""
-    n = int(src_idx.numel())
+    n = int(_int32(src_idx, "src_idx").numel())
+    if _int32(dst_idx, "dst_idx").numel() != n:
+        raise ValueError("src_idx and dst_idx must have the same length")
     _call("replayssm_copy_sequences", ctypes.byref(dims.c()), ctypes.byref(src.c()),
           _ptr(src_idx), ctypes.byref(dst.c()), _ptr(dst_idx), n, _stream(stream))
 

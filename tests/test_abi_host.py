@@ -229,3 +229,22 @@ def test_copy_sequences_arguments():
     assert cs(r(g), r(state()), None, r(state()), FAKE, 2, None) == _abi.ERR_INVALID_ARG
     assert cs(r(g), r(state(S_read=None)), FAKE, r(state()), FAKE, 2, None) == _abi.ERR_INVALID_ARG
     assert cs(r(g), r(state()), FAKE, r(state(ring_k=None)), FAKE, 2, None) == _abi.ERR_INVALID_ARG
+
+
+def test_binding_refuses_bad_index_tensors():
+    """The Python binding checks count and index tensors (int32, one per
+    sequence, equal lengths) before it builds any call."""
+    import torch
+
+    from recurrent_state_fp32_b300 import api
+
+    dims = api.LayerDims("gdn", 3, 2, dk=128, dv=128)
+    with pytest.raises(TypeError):
+        api.accept(dims, None, torch.zeros(3, dtype=torch.int64), 4)
+    with pytest.raises(ValueError):
+        api.accept(dims, None, torch.zeros(2, dtype=torch.int32), 4)
+    with pytest.raises(TypeError):
+        api.conventional_accept(dims, None, None, [0, 1, 2], 4)
+    with pytest.raises(ValueError):
+        api.copy_sequences(dims, None, torch.zeros(2, dtype=torch.int32), None,
+                           torch.zeros(3, dtype=torch.int32))
