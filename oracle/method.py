@@ -139,6 +139,23 @@ class ReplayOracle:
         self.len[seqs] = 0
         self.status[seqs] = 0
 
+    def copy_sequences(self, src, dst) -> None:
+        """Sequence dst[i] becomes a copy of sequence src[i]: checkpoint,
+        committed state, ring pointers, status and every ring slot.
+
+        A sequence is fully described by its checkpoint, its ring and its
+        pointers ("NVIDIA y Princeton aceleran…", paragraph 2), so a copy
+        resumes where its source stands without replaying history (the
+        prefix-cache and continuous-batching setting of "NVIDIA présente
+        ReplaySSM…", "D'où vient le problème de l'état"). All sources are
+        read before any destination is written.
+        """
+        src = np.asarray(src, np.int64)
+        dst = np.asarray(dst, np.int64)
+        for arr in (self.committed, self.ckpt, self.head, self.len, self.status,
+                    *self.ring.values()):
+            arr[dst] = arr[src].copy()
+
     # ---------------------------------------------------------- the calls
     def consolidate(self, k_next: int = 1, force: bool = False) -> np.ndarray:
         """Fold where len + k_next > W (or force and len > 0); returns the fold mask."""

@@ -459,6 +459,46 @@ def pin_restart_is_a_fresh_sequence():
         assert orc.len[1] == (T - t_join - 1) % W + 1, f"{kind} restarted slot length"
 
 
+def pin_copied_sequence_continues_its_source():
+    """A sequence copied mid-ring into a slot at another ring phase, then fed
+    its own tokens, gives exactly what the plain recurrence gives from its
+    source's history (the source's tokens up to the copy, then its own), and
+    its checkpoint, ring and pointers replay to that output. Checked through
+    later folds, for every layer kind."""
+    for kind in ("mamba2", "gdn", "kda"):
+        r = _rng(53)
+        b, H, rows, cols, W, T, t_copy = 3, 2, 4, 6, 7, 23, 7
+        S0 = r.standard_normal((b, H, rows, cols))
+        if kind == "mamba2":
+            A, D = m2_params(r, H)
+            toks = m2_tokens(r, b, H, 1, rows, cols, T)
+            orc = om.ReplayOracle(kind, S0, W, A=A, D=D)
+            step = lambda S, k: rec.mamba2_step(S, k["x"], k["B"], k["C"], k["dt"], A, D)  # noqa: E731
+        else:
+            toks = delta_tokens(r, b, H, cols, rows, T, kind == "kda")
+            orc = om.ReplayOracle(kind, S0, W, scale=0.8)
+            step = lambda S, k: rec.delta_step(S, k["q"], k["k"], k["v"], k["alpha"],  # noqa: E731
+                                               k["beta"], 0.8)
+        ref = S0.copy()  # plain recurrence of sequences 0 and 1 (and 2 after the copy)
+        for t, tok in enumerate(toks):
+            if t == 5:  # the destination slot starts a new sequence: another phase
+                orc.restart([2], np.zeros((1, H, rows, cols)))
+            if t == t_copy:
+                assert orc.len[0] > 0 and (orc.head[0], orc.len[0]) != (orc.head[2], orc.len[2])
+                orc.copy_sequences([0], [2])
+                ref[2] = ref[0]
+            orc.consolidate(1, force=(t == 3))  # an early partial fold moves the head
+            y = orc.decode(tok)
+            ref, y_ref = step(ref, tok)
+            for q in (0, 1) if t < t_copy else (0, 1, 2):
+                _close(y[q], y_ref[q], 1e-11, f"{kind} step {t} sequence {q}")
+            # every sequence's checkpoint, ring and pointers replay to its output
+            _close(orc.replay_output(tok, "f64"), y, 1e-11, f"{kind} replay step {t}")
+        _close(orc.committed, ref, 1e-11, f"{kind} committed state")
+        orc.consolidate(1, force=True)
+        _close(orc.ckpt, ref, 1e-11, f"{kind} checkpoint after a forced fold")
+
+
 def pin_rollback_equals_accepted_prefix():
     """Verify K drafts then accept m equals decoding only the m accepted tokens.
 

@@ -189,6 +189,20 @@ def accept_clamps_silently(self, m, K):
     _orig_accept(self, np.clip(np.asarray(m, np.int64), 0, K), K)
 
 
+def copy_without_ring(self, src, dst):
+    """The copy takes the checkpoint and the pointers but not the ring bytes."""
+    src, dst = np.asarray(src, np.int64), np.asarray(dst, np.int64)
+    for arr in (self.committed, self.ckpt, self.head, self.len, self.status):
+        arr[dst] = arr[src].copy()
+
+
+def copy_without_pointers(self, src, dst):
+    """The copy takes the states and the ring but keeps the destination's pointers."""
+    src, dst = np.asarray(src, np.int64), np.asarray(dst, np.int64)
+    for arr in (self.committed, self.ckpt, *self.ring.values()):
+        arr[dst] = arr[src].copy()
+
+
 MUTANTS = [
     (rec, "mamba2_step", m2_no_skip),
     (rec, "mamba2_step", m2_old_state_output),
@@ -212,6 +226,8 @@ MUTANTS = [
     (om.ReplayOracle, "spec_verify", spec_verify_unchained),
     (om.ReplayOracle, "accept", accept_moves_by_K),
     (om.ReplayOracle, "accept", accept_clamps_silently),
+    (om.ReplayOracle, "copy_sequences", copy_without_ring),
+    (om.ReplayOracle, "copy_sequences", copy_without_pointers),
 ]
 
 
