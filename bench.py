@@ -61,13 +61,12 @@ TRAFFIC_B64 = {
     ("mamba2", "bf16"): 136.526592e6 + 3.470848e6 + 10.205184e6,
     ("gdn", "bf16"): 77.416192e6 + 1.435392e6,
 }
-# The same for one fused Mamba-2 fold + decode call (prep + step stream
-# kernels), averaged over 16 consecutive calls of which one folds every
-# sequence: a sixteenth of the batch folds per call on average, in lockstep
-# or with staggered ring phases alike.
-TRAFFIC_B64_FUSED = {
-    ("mamba2", "bf16"): 178.543408e6,
-}
+# The same for one fused Mamba-2 fold + decode call (coefficient + step
+# stream kernels), averaged over 16 consecutive calls of which one folds
+# every sequence: a sixteenth of the batch folds per call on average, in
+# lockstep or with staggered ring phases alike. Empty until captured for the
+# current kernels.
+TRAFFIC_B64_FUSED: dict = {}
 
 
 def traffic_per_call(wl: dict, read: str, fused: bool):
@@ -190,9 +189,16 @@ class ClockSampler:
                 ["nice", "-n", "19", "nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.Q}",
                  "--format=csv,noheader,nounits", "-lms", "200"],
                 stdout=self.file, stderr=subprocess.DEVNULL)
-            time.sleep(0.3)
         except OSError:
             self.proc = None
+            return self
+        # nvidia-smi takes a while to start; its start-up must not overlap
+        # the timed region, so wait (at most 5 s) for its first sample
+        t0 = time.time()
+        while time.time() - t0 < 5.0 and self.proc.poll() is None:
+            if os.path.getsize(self.file.name) > 0:
+                break
+            time.sleep(0.05)
         return self
 
     def __exit__(self, *exc):
@@ -315,7 +321,7 @@ class Layer:
 
     def decode_kernels(self):
         if self.fused:
-            return "mamba2_prep_kernel + mamba2_step_stream_kernel (one fused call)"
+            return "mamba2_step_coef_kernel + mamba2_step_stream_kernel (one fused call)"
         if self.wl["kind"] == "mamba2":
             return "mamba2_prep_kernel + stream_kernel (one decode call)"
         return "delta_fused_kernel (one decode call)"
@@ -373,6 +379,18 @@ class Layer:
             lens += 1
         return dec, fold
 
+    def fold_steps(self, lens, steps):
+        """For each of `steps` steps from ring lengths `lens`: whether the
+        step's consolidate(k_next = 1) folds any sequence."""
+        lens = self.np.array(lens, dtype=self.np.int64)
+        W, out = self.wl["window"], []
+        for _ in range(steps):
+            f = lens + 1 > W
+            out.append(bool(f.any()))
+            lens[f] = 0
+            lens += 1
+        return out
+
     def stagger(self):
         """Puts sequence s at ring phase s mod W: W lockstep steps, before the
         j-th of which the sequences with s mod W == j restart from their
@@ -402,6 +420,18 @@ def run_ours(args, rank, local_rank, world):
     stream = torch.cuda.current_stream(device)
     K, Wm = args.steps, args.warmup
 
+    # The clock sampler starts first (its start-up takes the host for a
+    # while); the A/B and end-to-end loops then run, and the warm-up steps
+    # and the timed steps follow them directly, so the GPU does not idle
+    # (and drop its clocks) just before the timed region.
+    clocks = ClockSampler(local_rank) if not args.no_extras else None
+    if clocks:
+        clocks.__enter__()
+    extras = {}
+    if not args.no_extras:
+        extras["ab"] = run_ab(layer, K, Wm, stream, world)
+        extras["e2e"] = run_e2e(layer, args, stream, world)
+
     # warm-up
     for i in range(Wm):
         layer.step(layer.pool[i % POOL])
@@ -414,9 +444,6 @@ def run_ours(args, rank, local_rank, world):
     start, end = ev(), ev()
     d0 = [ev() for _ in range(K)]
     d1 = [ev() for _ in range(K)]
-    clocks = ClockSampler(local_rank) if not args.no_extras else None
-    if clocks:
-        clocks.__enter__()
     barrier(world)
     torch.cuda.synchronize()
     start.record(stream)
@@ -438,6 +465,7 @@ def run_ours(args, rank, local_rank, world):
         clocks.__exit__(None, None, None)
     ms = max_over_ranks(start.elapsed_time(end), world)
     dec_ms = [d0[i].elapsed_time(d1[i]) for i in range(K)]
+    gaps_us = [1e3 * d1[i].elapsed_time(d0[i + 1]) for i in range(K - 1)]
     bad = int(layer.state.status.ne(0).sum().item())
     if bad:
         print(f"warning: {bad} sequences report device status bits "
@@ -470,15 +498,27 @@ def run_ours(args, rank, local_rank, world):
         },
         "gpu_launches": K * layer.step_launches(),
         "device_status_ok": bad == 0,
+        "calls": call_stats(dec_ms, gaps_us, layer.fold_steps(lens0, K)),
     }
     if clocks:
         res["clocks"] = clocks.summary()
-    if not args.no_extras:
-        res["ab"] = run_ab(layer, K, Wm, stream, world)
-        res["e2e"] = run_e2e(layer, args, stream, world)
-        if rank == 0:
-            res["cpu_baseline"] = cpu_baseline(wl, args.cpu_seconds)
+    res.update(extras)
+    if not args.no_extras and rank == 0:
+        res["cpu_baseline"] = cpu_baseline(wl, args.cpu_seconds)
     return res
+
+
+def call_stats(dec_ms, gaps_us, folds):
+    """Per-call device times of the timed steps: the median of the calls that
+    fold nothing, the mean of those that fold, and the median idle gap on the
+    device between one call's end and the next call's start (host-bound
+    stretches show up there)."""
+    plain = [1e3 * t for t, f in zip(dec_ms, folds) if not f]
+    fold = [1e3 * t for t, f in zip(dec_ms, folds) if f]
+    return {"plain_call_us_median": round(statistics.median(plain), 2) if plain else None,
+            "fold_call_us": round(sum(fold) / len(fold), 2) if fold else None,
+            "fold_calls": len(fold),
+            "host_gap_us_median": round(statistics.median(gaps_us), 2) if gaps_us else None}
 
 
 def run_ab(layer, K, Wm, stream, world):

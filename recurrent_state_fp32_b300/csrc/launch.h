@@ -31,24 +31,25 @@ struct WorkLayout {
 constexpr int kStepMaxW = 16;
 
 // Layout of state.work for the fused Mamba-2 fold + decode step: one row of
-// `row` floats per (sequence, head) -- buffer terms [0, P), decode decay at
-// P, fold decay at P + 1, fold weights at [P + 2, P + 2 + kStepMaxW), the x
-// row of the entry the token overwrites at [xo, xo + P) -- then per
-// (sequence, group) the folded B rows as [kStepMaxW][N] floats, then one
-// int32 per sequence.
+// kStepRow floats per (sequence, head) -- the decode weights
+// c_j = w_j (C . B_j) of the buffered entries at [0, kStepMaxW) (zero past
+// the entries the decode replays), the token's weight plus D at kStepTok,
+// the decode decay at kStepDecay, the fold decay at kStepFoldDecay and the
+// fold weights w_j at [kStepFoldW, kStepFoldW + kStepMaxW) -- then per
+// (sequence, group) the folded B rows as [kStepMaxW][N] floats.
+constexpr int kStepTok = kStepMaxW;
+constexpr int kStepDecay = kStepMaxW + 1;
+constexpr int kStepFoldDecay = kStepMaxW + 2;
+constexpr int kStepFoldW = kStepMaxW + 4;
+constexpr int kStepRow = kStepFoldW + kStepMaxW;
 struct StepLayout {
-  int row, xo;
-  long long rows, batch, bf0, flag0;  // float offsets
+  long long rows, bf0, total;  // float offsets
   explicit StepLayout(const replayssm_dims& d) {
-    xo = (d.dv + 2 + kStepMaxW + 3) & ~3;
-    row = (xo + d.dv + 3) & ~3;
-    batch = d.batch;
-    rows = batch * d.heads;
-    bf0 = rows * row;
-    flag0 = bf0 + batch * d.groups * kStepMaxW * d.dk;
+    rows = (long long)d.batch * d.heads;
+    bf0 = rows * kStepRow;
+    total = bf0 + (long long)d.batch * d.groups * kStepMaxW * d.dk;
   }
-  long long bytes() const { return flag0 * 4 + ((batch * 4 + 15) & ~15LL); }
-  int32_t* flags(float* work) const { return reinterpret_cast<int32_t*>(work + flag0); }
+  long long bytes() const { return total * 4; }
 };
 
 // Device facts cached per device (SM count, opt-in shared memory per block).

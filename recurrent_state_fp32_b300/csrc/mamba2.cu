@@ -44,11 +44,6 @@ struct M2Prep {
   float* work;     // [b, H, wrow]: buffer terms [0, P), decay at P
   int wrow;
   int32_t* flags;  // [b]
-  // fused fold + decode only: fold decay at P + 1, fold weights at
-  // [P + 2, P + 2 + kStepMaxW) and entry 0's x row at [xo, xo + P) of each
-  // work row; folded B rows [b, G, kStepMaxW, N]
-  int xo;
-  float* bfold;
 };
 
 // Shared memory of one prep warp (byte offsets): kPrepDepth head stages
@@ -85,17 +80,7 @@ struct M2PrepSmem {
 // last arrival bumps len. A sequence whose ring is full (or whose pointers
 // are out of range) gets a status bit and flags[seq] = 0 and is untouched.
 // PT is the head dimension P when known at compile time (0: runtime P).
-//
-// STEP: preparation of the fused fold + decode step. A sequence whose ring
-// is full (len + 1 > W) is first folded: its n = len entries leave the ring
-// (head += n, len = 0) and the token is decoded after them, so the decode
-// terms above use only the token. The fold itself runs in the stream kernel;
-// this warp gives it, from the n entries (n <= kStepMaxW), the fold decay
-// exp(A_h sum_j dt_j), the weights w_j (zero past n) and the x row of entry
-// 0, whose slot the token takes, and the head's group gets its B_j as
-// floats (read before the append). The ring pointers are left alone (the
-// stream kernel moves them), so no arrival happens here.
-template <int N, int PT, typename TI, bool STEP>
+template <int N, int PT, typename TI>
 __global__ void __launch_bounds__(32 * kPrepWarps) mamba2_prep_kernel(const M2Prep a) {
   extern __shared__ __align__(128) unsigned char smem[];
   constexpr int kNL = N / 32;
@@ -129,7 +114,6 @@ __global__ void __launch_bounds__(32 * kPrepWarps) mamba2_prep_kernel(const M2Pr
   int i_seq = v0 / H, i_h = v0 - (v0 / H) * H;
   int i_len = 0, i_hd = 0;
   bool i_ok = false;
-  int i_nf = 0;       // STEP: entries folded before the token (0: no fold)
   int i_loaded = -1;  // sequence whose pointers the issue side holds
   int i_t = 0;        // next head (offset from v0) to fetch
   auto issue = [&]() {
@@ -141,13 +125,7 @@ __global__ void __launch_bounds__(32 * kPrepWarps) mamba2_prep_kernel(const M2Pr
       }
       i_len = __shfl_sync(kFull, l, 0);
       i_hd = __shfl_sync(kFull, hh, 0);
-      i_ok = pointers_ok(i_hd, i_len, W) && (STEP || i_len + 1 <= W);
-      i_nf = 0;
-      if (STEP && i_ok && i_len + 1 > W) {  // fold first: pointers after the fold
-        i_nf = i_len;
-        i_hd = (i_hd + i_len) % W;
-        i_len = 0;
-      }
+      i_ok = pointers_ok(i_hd, i_len, W) && i_len + 1 <= W;
       i_loaded = i_seq;
     }
     const int v = v0 + i_t;
@@ -156,13 +134,7 @@ __global__ void __launch_bounds__(32 * kPrepWarps) mamba2_prep_kernel(const M2Pr
       int* hdr = reinterpret_cast<int*>(st + L.hdr);
       hdr[0] = i_len;
       hdr[1] = i_hd;
-      hdr[2] = (i_ok ? 1 : 0) | (i_nf << 8);
-    }
-    if (STEP && i_nf > 0) {
-      // the x row of entry 0 of the fold, at row 0 of the (unused) entry rows
-      const int slot0 = (i_hd - i_nf + W) % W;
-      const unsigned char* xs = ringx + ((size_t)v * W + slot0) * row;
-      for (int c = lane; c < cpr; c += 32) cp_async16(st + L.xr + c * 16, xs + c * 16);
+      hdr[2] = i_ok ? 1 : 0;
     }
     if (i_ok) {
       const unsigned char* xs = ringx + (size_t)v * W * row;
@@ -195,7 +167,7 @@ __global__ void __launch_bounds__(32 * kPrepWarps) mamba2_prep_kernel(const M2Pr
   };
 
   // ---- compute side
-  int cur_seq = -1, len = 0, hd = 0, nf = 0;
+  int cur_seq = -1, len = 0, hd = 0;
   bool ok = false;
   int cb_seq = -1, cb_g = -1;  // (sequence, group) whose C.B_j the cache holds
   int seq_first = v0;          // first head of the current sequence in this range
@@ -213,13 +185,12 @@ __global__ void __launch_bounds__(32 * kPrepWarps) mamba2_prep_kernel(const M2Pr
     __syncwarp();
     const int v = v0 + t;
     if (seq != cur_seq) {
-      if (!STEP && cur_seq >= 0 && ok && lane == 0)  // leaving a sequence: arrive with its heads
+      if (cur_seq >= 0 && ok && lane == 0)  // leaving a sequence: arrive with its heads
         arrive_and_finish(a.sync + cur_seq, v - seq_first, H, [&] { a.len[cur_seq] = len + 1; });
       const int* hdr = reinterpret_cast<const int*>(wbase + (size_t)(t % kPrepDepth) * L.stage + L.hdr);
       len = hdr[0];
       hd = hdr[1];
       ok = (hdr[2] & 1) != 0;
-      nf = hdr[2] >> 8;
       cur_seq = seq;
       seq_first = v;
       if (h == 0 && lane == 0) {
@@ -330,32 +301,6 @@ __global__ void __launch_bounds__(32 * kPrepWarps) mamba2_prep_kernel(const M2Pr
         if (act) *reinterpret_cast<float2*>(wrow + p) = make_float2(e0, e1);
       }
       if (lane == 0) wrow[P] = __expf(Ah * total);
-      if constexpr (STEP) {
-        if (nf > 0) {
-          // fold over entries 0..nf-1 (oldest at slot hd0): weights
-          // w_j = dt_j exp(A_h sum_{i>j} dt_i) (lane j) and decay exp(A_h sum_i dt_i)
-          const int hd0 = (hd - nf + W) % W;
-          const float fj = lane < nf ? dtr[hd0 + lane < W ? hd0 + lane : hd0 + lane - W] : 0.f;
-          float sfx = fj;  // inclusive suffix sum
-#pragma unroll
-          for (int o = 1; o < 32; o <<= 1) {
-            const float u = __shfl_down_sync(kFull, sfx, o);
-            if (lane + o < 32) sfx += u;
-          }
-          if (lane < kStepMaxW) wrow[P + 2 + lane] = fj * expf(Ah * (sfx - fj));
-          if (lane == 0) wrow[P + 1] = expf(Ah * sfx);
-          for (int p = lane; p < P; p += 32) wrow[a.xo + p] = to_f(xr[p]);
-          // the group's B rows as floats
-          if (hg == 0) {
-            float* Bs = a.bfold + ((size_t)seq * G + g) * kStepMaxW * N;
-            for (int j = 0; j < nf; ++j) {
-              const int slot = hd0 + j < W ? hd0 + j : hd0 + j - W;
-              const TI* Bo = rB + (((size_t)seq * W + slot) * G + g) * N;
-              for (int c = lane; c < N; c += 32) Bs[(size_t)j * N + c] = to_f(Bo[c]);
-            }
-          }
-        }
-      }
       // append the token: x row and dt of this head, B and C of its group
       const int slot = hd + len < W ? hd + len : hd + len - W;
       uint4* xd = reinterpret_cast<uint4*>(const_cast<unsigned char*>(ringx) +
@@ -383,8 +328,192 @@ __global__ void __launch_bounds__(32 * kPrepWarps) mamba2_prep_kernel(const M2Pr
     }
   }
   cp_async_wait_all();
-  if (!STEP && cur_seq >= 0 && ok && lane == 0)
+  if (cur_seq >= 0 && ok && lane == 0)
     arrive_and_finish(a.sync + cur_seq, v1 - seq_first, H, [&] { a.len[cur_seq] = len + 1; });
+}
+
+// ------------------------------------------------- fused step: coefficients
+
+constexpr int kCoefWarps = 8;   // warps per coefficient block
+constexpr int kCoefHeads = 16;  // heads per warp
+
+struct M2Coef {
+  int batch, H, G, W;
+  const float* A;
+  const float* D;
+  const void* B;      // token inputs [b, G, N]
+  const void* C;
+  const float* dt;    // [b, H]
+  void* ring_B;
+  void* ring_C;
+  float* ring_dt;
+  const int32_t* head;
+  const int32_t* len;
+  int32_t* status;
+  float* work;   // [b, H, kStepRow]
+  float* bfold;  // [b, G, kStepMaxW, N]
+};
+
+// Per-head coefficients of the fused fold + decode step. A sequence whose
+// ring is full (len + 1 > W) is folded first: its nf = len entries leave the
+// ring (head += nf, len = 0) and the token is decoded after them. The decode
+// then replays the ld buffered entries (ld = len without a fold, 0 with one)
+// and the token, entry ld; with dA_i = exp(dt_i A_h) over those entries:
+//   c_j    = w_j (C . B_j),  w_j = dt_j exp(A_h sum_{i>j} dt_i),  j < ld
+//   c_tok  = dt_tok (C . B_tok) + D_h
+//   decay  = exp(A_h sum_i dt_i)
+// and for a fold, over its nf entries, the fold weights w_j and the fold
+// decay exp(A_h sum_j dt_j). The stream kernel computes the buffer terms
+// sum_j c_j x_j[p] + c_tok x[p] itself from the ring x rows, so this grid
+// reads no x at all and is short: its dependent stream kernel launches at
+// once and streams state rows while it runs.
+//
+// One warp per (sequence, chunk of kCoefHeads heads); half-warps take one
+// head each, lane j of a half holding entry j. C . B_j is computed once per
+// group the chunk touches. The token's dt goes into the ring here, and the
+// warp holding a group's first head copies the group's folded B rows out as
+// floats and then appends the token's B and C. The x row of the token is
+// appended by the stream kernel, row by row, after it has read the ring.
+// No slot this grid writes is one it, or any other warp of the grid, reads:
+// without a fold the token's slot is past the buffered entries, and with one
+// only the writing warp reads the old entries, first.
+template <int N, typename TI>
+__global__ void __launch_bounds__(32 * kCoefWarps, 4) mamba2_step_coef_kernel(const M2Coef a) {
+  constexpr int E = N / 32;  // B and C elements per lane
+  griddep_launch_dependents();  // the stream kernel may start streaming state rows
+  const int lane = threadIdx.x & 31;
+  const int H = a.H, G = a.G, W = a.W, hpg = H / G, Wd = ring_wd(W);
+  const int nch = (H + kCoefHeads - 1) / kCoefHeads;
+  const long long wv = (long long)blockIdx.x * kCoefWarps + (threadIdx.x >> 5);
+  if (wv >= (long long)a.batch * nch) return;
+  const int seq = (int)(wv / nch);
+  const int h0 = (int)(wv - (long long)seq * nch) * kCoefHeads, h1 = min(h0 + kCoefHeads, H);
+  int l = 0, hh = 0;
+  if (lane == 0) {
+    l = a.len[seq];
+    hh = a.head[seq];
+  }
+  const int len = __shfl_sync(kFull, l, 0), hd = __shfl_sync(kFull, hh, 0);
+  if (!pointers_ok(hd, len, W)) {
+    if (h0 == 0 && lane == 0) atomicOr(a.status + seq, REPLAYSSM_SEQ_BAD_POINTER);
+    return;
+  }
+  const int nf = len + 1 > W ? len : 0;     // entries folded before the token
+  const int hdd = nf ? (hd + len) % W : hd;  // ring head of the decode
+  const int ld = nf ? 0 : len;              // buffered entries the decode replays
+  auto slot_of = [W](int s) { return s < W ? s : s - W; };
+  const int tslot = slot_of(hdd + ld);      // the token's slot
+  const TI* Bin = reinterpret_cast<const TI*>(a.B);
+  const TI* Cin = reinterpret_cast<const TI*>(a.C);
+  const TI* rB = reinterpret_cast<const TI*>(a.ring_B);
+
+  // C . B_j of group g for the decode's entries 0..ld (entry ld: the token);
+  // lane l ends with entry l & 15 (ld < kStepMaxW = 16).
+  auto cb_of = [&](int g) -> float {
+    float cf[E];
+    load_vec<TI, E>(Cin + ((size_t)seq * G + g) * N + lane * E, cf);
+    float vv[kStepMaxW];
+#pragma unroll
+    for (int q = 0; q < kStepMaxW; ++q) {
+      float pp = 0.f;
+      if (q <= ld) {
+        const TI* Bj = q < ld ? rB + (((size_t)seq * W + slot_of(hdd + q)) * G + g) * N
+                              : Bin + ((size_t)seq * G + g) * N;
+        float bv[E];
+        load_vec<TI, E>(Bj + lane * E, bv);
+#pragma unroll
+        for (int e = 0; e < E; ++e) pp = fmaf(cf[e], bv[e], pp);
+      }
+      vv[q] = pp;
+    }
+    const float tot = reduce_scatter<kStepMaxW>(vv, lane);
+    return tot + __shfl_xor_sync(kFull, tot, 16);
+  };
+
+  const int half = lane >> 4, j = lane & 15;
+  int cg = -1;      // group whose C . B_j the cache holds
+  float cv = 0.f;
+  for (int hA = h0; hA < h1; hA += 2) {
+    const int gA = hA / hpg, gB = min(hA + 1, h1 - 1) / hpg;
+    float cvA, cvB;
+    if (gA == cg) {
+      cvA = cv;
+    } else {
+      cvA = cb_of(gA);
+      cg = gA;
+      cv = cvA;
+    }
+    if (gB == gA) {
+      cvB = cvA;
+    } else {
+      cvB = cb_of(gB);
+      cg = gB;
+      cv = cvB;
+    }
+    const float cb = half ? cvB : cvA;
+    const int h = hA + half;
+    const bool act = h < h1;
+    const size_t v = (size_t)seq * H + (act ? h : hA);
+    const float* rdt = a.ring_dt + v * Wd;
+    const float dtt = a.dt[v], Ah = a.A[act ? h : hA], Dh = a.D[act ? h : hA];
+    // decode weights: inclusive suffix sums of dt over the half's 16 lanes
+    const float d = j < ld ? rdt[slot_of(hdd + j)] : (j == ld ? dtt : 0.f);
+    float sfx = d;
+#pragma unroll
+    for (int o = 1; o < 16; o <<= 1) {
+      const float t = __shfl_down_sync(kFull, sfx, o, 16);
+      if (j + o < 16) sfx += t;
+    }
+    const float total = __shfl_sync(kFull, sfx, 0, 16);
+    // exponents lie in [A_h sum dt, 0]; the fast exponential's relative
+    // error (about 1e-6 there) is far inside the output tolerance
+    const float c = d * __expf(Ah * (sfx - d)) * cb;
+    float* wr = a.work + v * kStepRow;
+    if (act) {
+      wr[j] = j < ld ? c : 0.f;
+      if (j == ld) wr[kStepTok] = c + Dh;
+      if (j == 0) wr[kStepDecay] = __expf(Ah * total);
+    }
+    if (nf) {  // fold weights over the nf entries from the old head
+      const float f = j < nf ? rdt[slot_of(hd + j)] : 0.f;
+      float fs = f;
+#pragma unroll
+      for (int o = 1; o < 16; o <<= 1) {
+        const float t = __shfl_down_sync(kFull, fs, o, 16);
+        if (j + o < 16) fs += t;
+      }
+      const float ftot = __shfl_sync(kFull, fs, 0, 16);
+      if (act) {
+        wr[kStepFoldW + j] = j < nf ? f * expf(Ah * (fs - f)) : 0.f;
+        if (j == 0) wr[kStepFoldDecay] = expf(Ah * ftot);
+      }
+    }
+    // the token's dt, after the half has read the row (the shuffles above
+    // consumed every load); with a fold its slot is entry 0's
+    __syncwarp();
+    if (act && j == 0) a.ring_dt[v * Wd + tslot] = dtt;
+  }
+
+  // Groups whose first head is in this chunk: folded B rows, then the
+  // token's B and C.
+  for (int g = h0 / hpg; g * hpg < h1; ++g) {
+    if (g * hpg < h0) continue;
+    const size_t gi = (size_t)seq * G + g;
+    if (nf) {
+      float* Bs = a.bfold + gi * kStepMaxW * N;
+      for (int jj = 0; jj < nf; ++jj) {
+        const TI* Bo = rB + (((size_t)seq * W + slot_of(hd + jj)) * G + g) * N;
+        for (int cc = lane; cc < N; cc += 32) Bs[(size_t)jj * N + cc] = to_f(Bo[cc]);
+      }
+      __syncwarp();
+    }
+    TI* dB = reinterpret_cast<TI*>(a.ring_B) + (((size_t)seq * W + tslot) * G + g) * N;
+    for (int cc = lane; cc < N; cc += 32) dB[cc] = Bin[gi * N + cc];
+    if (a.ring_C) {
+      TI* dC = reinterpret_cast<TI*>(a.ring_C) + (((size_t)seq * W + tslot) * G + g) * N;
+      for (int cc = lane; cc < N; cc += 32) dC[cc] = Cin[gi * N + cc];
+    }
+  }
 }
 
 // -------------------------------------------------------------- verify prep
@@ -778,8 +907,7 @@ __global__ void __launch_bounds__(kThreads) mamba2_conventional_kernel(const M2C
 
 namespace {
 
-// Launches the preparation kernel (plain decode, or the fused step when STEP).
-template <bool STEP>
+// Launches the preparation kernel of the plain decode.
 cudaError_t launch_prep(const replayssm_dims& d, const M2Prep& p, cudaStream_t st) {
   const bool in16 = d.in_dtype == REPLAYSSM_BF16;
   const int ti = in16 ? 2 : 4;
@@ -793,7 +921,7 @@ cudaError_t launch_prep(const replayssm_dims& d, const M2Prep& p, cudaStream_t s
   cudaError_t e;
 #define RS_PREP(N_, PT_, TI_)                                                                   \
   {                                                                                            \
-    auto k = mamba2_prep_kernel<N_, PT_, TI_, STEP>;                                           \
+    auto k = mamba2_prep_kernel<N_, PT_, TI_>;                                                 \
     e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);       \
     if (e != cudaSuccess) return e;                                                            \
     k<<<(unsigned)grid, 32 * kPrepWarps, smem, st>>>(p);                                       \
@@ -819,8 +947,8 @@ cudaError_t launch_mamba2_decode(const replayssm_dims& d, const replayssm_state&
   const bool in16 = d.in_dtype == REPLAYSSM_BF16;
   M2Prep p{d.batch, d.heads, d.groups, d.dv, d.window, A, D, x, B, C, dt,
            s.ring_x, s.ring_B, s.ring_C, s.ring_dt, s.ring_head, s.ring_len, s.status, s.sync,
-           s.work, wl.row, wl.flags(s.work), 0, nullptr};
-  cudaError_t e = launch_prep<false>(d, p, st);
+           s.work, wl.row, wl.flags(s.work)};
+  cudaError_t e = launch_prep(d, p, st);
   if (e != cudaSuccess) return e;
   // Stream: y = decay * (S C) + extra, C straight from the token input.
   StreamArgs sa{};
@@ -944,6 +1072,26 @@ cudaError_t launch_mamba2_conventional(const replayssm_dims& d, float* S, const 
 
 namespace {
 
+// Launches the coefficient kernel of the fused step. Its blocks use no shared
+// memory (and ask for the shared-memory carveout the stream kernel needs),
+// so the stream kernel's blocks fit beside them and start at once.
+cudaError_t launch_step_coef(const replayssm_dims& d, const M2Coef& p, cudaStream_t st) {
+  const long long warps = (long long)d.batch * ((d.heads + kCoefHeads - 1) / kCoefHeads);
+  const unsigned grid = (unsigned)((warps + kCoefWarps - 1) / kCoefWarps);
+  void (*kern)(const M2Coef);
+  if (d.dk == 128)
+    kern = d.in_dtype == REPLAYSSM_BF16 ? mamba2_step_coef_kernel<128, bf16>
+                                        : mamba2_step_coef_kernel<128, float>;
+  else
+    kern = d.in_dtype == REPLAYSSM_BF16 ? mamba2_step_coef_kernel<64, bf16>
+                                        : mamba2_step_coef_kernel<64, float>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                       (int)cudaSharedmemCarveoutMaxShared);
+  if (e != cudaSuccess) return e;
+  kern<<<grid, 32 * kCoefWarps, 0, st>>>(p);
+  return cudaGetLastError();
+}
+
 template <int N, typename TS, typename TV>
 cudaError_t launch_step_stream(const StepArgs& a, size_t smem, int grid, int threads,
                                cudaStream_t st) {
@@ -1004,10 +1152,10 @@ cudaError_t launch_mamba2_fold_decode(const replayssm_dims& d, const replayssm_s
   const size_t smem = StepSmem(RB, d.dk, ts, NS, nloc_max, xblk).total;
 
   const StepLayout sl(d);
-  M2Prep p{d.batch, d.heads, d.groups, d.dv, d.window, A, D, x, B, C, dt,
-           s.ring_x, s.ring_B, s.ring_C, s.ring_dt, s.ring_head, s.ring_len, s.status, s.sync,
-           s.work, sl.row, sl.flags(s.work), sl.xo, s.work + sl.bf0};
-  cudaError_t e = launch_prep<true>(d, p, st);
+  M2Coef p{d.batch, d.heads, d.groups, d.window, A, D, B, C, dt,
+           s.ring_B, s.ring_C, s.ring_dt, s.ring_head, s.ring_len, s.status,
+           s.work, s.work + sl.bf0};
+  cudaError_t e = launch_step_coef(d, p, st);
   if (e != cudaSuccess) return e;
 
   StepArgs a{};
@@ -1026,10 +1174,9 @@ cudaError_t launch_mamba2_fold_decode(const replayssm_dims& d, const replayssm_s
   a.S_read = reinterpret_cast<bf16*>(s.S_read);
   a.out = y;
   a.work = s.work;
-  a.wrow = sl.row;
   a.xblk = xblk;
-  a.xo = sl.xo;
   a.bfold = s.work + sl.bf0;
+  a.x = x;
   a.C = C;
   a.ring_x = s.ring_x;
   a.head = s.ring_head;

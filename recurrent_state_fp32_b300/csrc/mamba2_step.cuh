@@ -8,21 +8,31 @@
 // buffer fills" follow "NVIDIA y Princeton aceleran modelos híbridos al
 // guardar entradas recientes en lugar del estado completo", paragraph 2.
 //
+// A short coefficient grid runs first (mamba2_step_coef_kernel): per head
+// the decode weights c_j = w_j (C . B_j) of the l buffered entries, the
+// token's weight c_tok (with D), the decode decay, and for a fold the fold
+// weights and fold decay. This kernel is its programmatic dependent: its
+// producer streams state rows at once, its consumers wait for the weights.
+//
 // Units are (sequence, head, row block of RB rows), dealt to the blocks in
 // turn (unit u goes to block u mod grid), so the folds of any set of
 // sequences spread over all SMs. In each block a producer warp fills a ring
 // of NS shared-memory stages with one bulk copy per stage and consumer
 // groups of GU warps take the block's units round robin. Two kinds of unit:
 //   decode  (ring not full): one stage of read-copy rows;
-//           y[r] = decay * (S[r, :] . C) + extra[r]
+//           y[r] = decay * (S[r, :] . C) + sum_{j<l} c_j x_j[r] + c_tok x[r]
+//           with the ring x rows x_j loaded by the consumer itself
 //   fold    (ring full, n = len entries): FS = 4 / sizeof(TS) stages of FP32
-//           checkpoint rows, each with the rows' fold coefficients
-//           c_j[r] = w_j x_j[r] (from the preparation grid) beside it;
+//           checkpoint rows, the head's ring x block beside the first;
+//           c_j[r] = w_j x_j[r],
 //           S'[r, :] = fold_decay * S[r, :] + sum_j c_j[r] B_j,
 //           S' written to the checkpoint and read copy, then
-//           y[r] = decay * (S'_read[r, :] . C) + extra[r]
+//           y[r] = decay * (S'_read[r, :] . C) + c_tok x[r]
 // where S'_read is the row as the read copy holds it (the BF16 rounding when
-// there is one), so outputs equal those of a consolidate then a decode.
+// there is one), so outputs equal those of a consolidate then a decode. Each
+// unit then appends the token's x for its own rows (with a fold, into entry
+// 0's slot: no unit reads another unit's rows, and a fold unit's own rows
+// were copied before it writes).
 // The kind of every unit is fixed at block start from the ring pointers,
 // which nothing changes until the last unit of a sequence is done: each
 // block arrives on a sequence's counter once per unit of it when all its
@@ -33,8 +43,7 @@
 // for its units (a fold unit takes FS consecutive ones), so a group only
 // waits for a stage's next fill after it has consumed the previous one and
 // the mbarrier parity of a wait cannot alias an older phase. The producer
-// fills the stages of unit i's group in unit order. It streams state rows
-// before the preparation grid ends; consumers wait for it.
+// fills the stages of unit i's group in unit order.
 #pragma once
 
 #include "common.cuh"
@@ -49,12 +58,11 @@ struct StepArgs {
   float* S_ckpt;        // FP32 checkpoint [b, H, P, N]
   bf16* S_read;         // BF16 read copy or null
   float* out;           // y [b, H, P]
-  const float* work;    // rows of wrow floats per (sequence, head), StepLayout
-  int wrow;
-  int xo;               // entry 0's x row in the work row
+  const float* work;    // rows of kStepRow floats per (sequence, head), StepLayout
   const float* bfold;   // folded B rows [b, G, kStepMaxW, N]
+  const void* x;        // token input x [b, H, P]
   const void* C;        // token input C [b, G, N]
-  const void* ring_x;   // [b, H, W, P]
+  void* ring_x;         // [b, H, W, P]
   int32_t* head;
   int32_t* len;
   int32_t* status;
@@ -248,6 +256,9 @@ __global__ void __launch_bounds__(kStreamMaxThreads, 1) mamba2_step_stream_kerne
     const int cd = RD::chunk_of(lane) * kE;  // decode units: this lane's elements of C
     const int cf = RF::chunk_of(lane) * 4;   // fold units: this lane's four columns
     const TV* Cin = reinterpret_cast<const TV*>(a.C);
+    const TV* xin = reinterpret_cast<const TV*>(a.x);
+    TV* rx = reinterpret_cast<TV*>(a.ring_x);
+    auto slot_of = [W](int s) { return s < W ? s : s - W; };
     // Work rows and folded B rows come from the preparation grid (this grid
     // may start before it ends).
     griddep_wait();
@@ -274,15 +285,29 @@ __global__ void __launch_bounds__(kStreamMaxThreads, 1) mamba2_step_stream_kerne
         }
       }
       const int row0 = rb * RB + part * RBp;  // first row of this warp within the head
-      const float* w0 = a.work + (size_t)hg * a.wrow;
+      const float* w0 = a.work + (size_t)hg * kStepRow;
       float* yrow = a.out + (size_t)hg * P + row0;
-      const float scale = w0[P];
+      const float scale = w0[kStepDecay];
+      const float ctok = w0[kStepTok];
+      const int hd = (code >> 16) & 0xff, l = (code >> 8) & 0xff;
+      // the token's ring slot: after the buffered entries, or entry 0's after a fold
+      const int tslot = slot_of(fold ? hd : hd + l);
+      const TV* xh = xin + (size_t)hg * P + row0;                 // the token's x rows
+      TV* rxh = rx + (size_t)hg * W * P + row0;                   // the head's ring x rows
       const bool aborted = __shfl_sync(kFull, abort_flag, 0) != 0;
       if (!fold) {
         // -------------------------------------------------- decode unit
+        // buffer terms of this lane's row from the ring x rows of the l
+        // buffered entries, loaded before the wait for the state rows
         float vec[kE];
         load_vec<TV, kE>(Cin + ((size_t)seq * a.G + g) * N + cd, vec);
-        const float extra = w0[row0 + RD::row_of(lane)];
+        const int r = RD::row_of(lane);
+        const float cj = w0[lane & (kStepMaxW - 1)];
+        const TV xtr = xh[r];
+        TV xj[kStepMaxW];
+#pragma unroll
+        for (int j = 0; j < kStepMaxW; ++j)
+          if (j < l) xj[j] = rxh[(size_t)slot_of(hd + j) * P + r];
         const int s = s0;
         const bool landed = !aborted && mbar_wait_warp(&full[s], ph0);
         if (!aborted && !landed && lane == 0) {
@@ -303,11 +328,20 @@ __global__ void __launch_bounds__(kStreamMaxThreads, 1) mamba2_step_stream_kerne
           __syncwarp();
           if (lane == 0) mbar_arrive(&empty[s]);
         }
-        if (ok) yrow[RD::row_of(lane)] = fmaf(scale, d, extra);
+        float extra = ctok * to_f(xtr);
+#pragma unroll
+        for (int j = 0; j < kStepMaxW; ++j) {
+          const float c = __shfl_sync(kFull, cj, j);
+          if (j < l) extra = fmaf(c, to_f(xj[j]), extra);
+        }
+        if (ok) {
+          yrow[r] = fmaf(scale, d, extra);
+          rxh[(size_t)tslot * P + r] = xtr;  // append the token's x
+        }
       } else {
         // ---------------------------------------------------- fold unit
-        const int nf = (code >> 8) & 0xff, hd0 = (code >> 16) & 0xff;
-        const float fdec = w0[P + 1];
+        const int nf = l, hd0 = hd;
+        const float fdec = w0[kStepFoldDecay];
         // B_j of the head's group, this lane's columns (zero past the n entries)
         const float* Bs = a.bfold + ((size_t)seq * a.G + g) * kStepMaxW * N + cf;
         float4 Bq[kStepMaxW];
@@ -318,8 +352,8 @@ __global__ void __launch_bounds__(kStreamMaxThreads, 1) mamba2_step_stream_kerne
         float c4[4];
         load_vec<TV, 4>(Cin + ((size_t)seq * a.G + g) * N + cf, c4);
         const int r = fold_row<RF::kLpr, RF::kRpi, kCS>(lane);
-        const float extra = w0[row0 + r];
-        const float x0 = w0[a.xo + row0 + lane];  // entry 0 of this lane's row
+        const TV xtr = xh[r];  // the token (decoded after the fold, n = 1)
+        const float extra = ctok * to_f(xtr);
         // this warp's stage: the unit's first, or the second of a two-stage
         // unit; the first also holds the ring x block, so every warp waits for it
         const bool second = FS > 1 && part == 1;
@@ -331,9 +365,9 @@ __global__ void __launch_bounds__(kStreamMaxThreads, 1) mamba2_step_stream_kerne
           atomicOr(a.status + seq, REPLAYSSM_SEQ_TIMEOUT);
         }
         if (group_any(!landed)) break;
-        // coefficients c_j = w_j x_j of row row0 + lane: entry 0 from the
-        // saved row (the token has taken its slot), entry j > 0 from slot
-        // hd0 + j of the copied ring x block (slots this call does not write)
+        // coefficients c_j = w_j x_j of row row0 + lane from slot hd0 + j of
+        // the copied ring x block: no warp writes this unit's rows of the
+        // ring (the token goes into entry 0's slot) before the copy landed
         const int off = FS > 1 ? 0 : part * RBp;  // this warp's rows in its stage
         float* coef = reinterpret_cast<float*>(smem + L.sides + (size_t)s * L.side) +
                       (size_t)off * kStepMaxW;
@@ -341,14 +375,8 @@ __global__ void __launch_bounds__(kStreamMaxThreads, 1) mamba2_step_stream_kerne
           const TV* xs = reinterpret_cast<const TV*>(smem + L.sides + (size_t)s0 * L.side);
           float cj[kStepMaxW];
 #pragma unroll
-          for (int j = 0; j < kStepMaxW; ++j) {
-            float xv = x0;
-            if (j > 0 && j < nf) {
-              const int slot = hd0 + j < W ? hd0 + j : hd0 + j - W;
-              xv = to_f(xs[(size_t)slot * P + row0 + lane]);
-            }
-            cj[j] = j < nf ? w0[P + 2 + j] * xv : 0.f;
-          }
+          for (int j = 0; j < kStepMaxW; ++j)
+            cj[j] = j < nf ? w0[kStepFoldW + j] * to_f(xs[(size_t)slot_of(hd0 + j) * P + row0 + lane]) : 0.f;
           // every warp of the unit has read the x block before any
           // coefficients overwrite it
           if (GU == 1) {
@@ -401,6 +429,7 @@ __global__ void __launch_bounds__(kStreamMaxThreads, 1) mamba2_step_stream_kerne
           if ((lane & (kFoldChunks - 1)) == m) mine = d;
         }
         yrow[r] = fmaf(scale, mine, extra);
+        rxh[(size_t)tslot * P + r] = xtr;  // append the token's x
         __syncwarp();
         if (lane == 0) {
           mbar_arrive(&empty[s0]);

@@ -165,10 +165,11 @@ def test_fold_decode_arguments():
 
 def test_workspace_size():
     r = ctypes.byref
-    # Mamba-2: the fused fold + decode step's rows (P + 2 + 16 floats padded
-    # to 4, then P) and 16 B rows per (sequence, group); verify rows for K = 4
+    # Mamba-2: the fused fold + decode step's rows (16 decode weights, the
+    # token's weight, two decays, padding, 16 fold weights: 36 floats) and 16
+    # B rows per (sequence, group); verify rows for K = 4
     m = dims(batch=2, heads=4, dk=128, dv=64)
-    step = 2 * 4 * 148 * 4 + 2 * 16 * 128 * 4 + 16
+    step = 2 * 4 * 36 * 4 + 2 * 16 * 128 * 4
     assert _abi.lib.replayssm_workspace_bytes(r(m), 1) == step
     assert _abi.lib.replayssm_workspace_bytes(r(m), 4) == max(4 * 2 * 4 * 68 * 4 + 16, step)
     g = dims(kind=_abi.GDN, batch=3, heads=2, dk=128, dv=96)
