@@ -14,10 +14,19 @@ import numpy as np
 import torch
 
 import synth
+from oracle import replay as rep
 from oracle.method import ReplayOracle
 from recurrent_state_fp32_b300 import api
 
 DEV = "cuda"
+
+
+def spread(batch, n=8):
+    """n sequences spread over the batch, first and last included: their units
+    fall on the first, middle and last persistent blocks alike."""
+    if n <= 1 or batch <= 1:
+        return [0]
+    return sorted({int(round(i * (batch - 1) / (n - 1))) for i in range(n)})
 
 
 def dev(a, dtype=torch.float32):
@@ -95,6 +104,7 @@ class Session:
                                        store_optional=store_optional)
         self.vt = self.dims.vec_dtype
         self.worst = 0.0
+        self.last_tok = None
 
     # --------------------------------------------------------------- inputs
     def token(self, t):
@@ -145,6 +155,15 @@ class Session:
             S32 = S.astype(np.float32)[s_idx][:, self.heads]
             self.oracle.restart(o_idx, S32)
 
+    def fork(self, src, dst):
+        """Sequences dst[i] become copies of sequences src[i] (replayssm_copy_sequences
+        on the GPU; the oracle copies its own rows). Both lists must be sampled."""
+        src, dst = np.asarray(src, np.int32), np.asarray(dst, np.int32)
+        api.copy_sequences(self.dims, self.state, dev(src, torch.int32), self.state,
+                           dev(dst, torch.int32))
+        pos = {int(s): i for i, s in enumerate(self.seqs)}
+        self.oracle.copy_sequences([pos[int(s)] for s in src], [pos[int(d)] for d in dst])
+
     def consolidate(self, k_next=1, force=False):
         api.consolidate(self.dims, self.state, self.dA if self.kind == "mamba2" else None,
                         k_next, force)
@@ -152,6 +171,7 @@ class Session:
 
     def decode(self, t, check=True):
         tok = self.token(t)
+        self.last_tok = tok
         g = self._to_dev(tok)
         rows = self.wl.P if self.kind == "mamba2" else self.wl.dv
         y = torch.full((self.wl.batch, self.wl.heads, rows), float("nan"), device=DEV)
@@ -171,6 +191,7 @@ class Session:
         """One Mamba-2 step through the fused call; the oracle takes the same
         step as consolidate(k_next=1) followed by decode."""
         tok = self.token(t)
+        self.last_tok = tok
         g = self._to_dev(tok)
         y = torch.full((self.wl.batch, self.wl.heads, self.wl.P), float("nan"), device=DEV)
         api.mamba2_fold_decode(self.dims, self.state, self.dA, self.dD, g["x"], g["B"], g["C"],
@@ -217,6 +238,55 @@ class Session:
     def accept(self, m, K):
         api.accept(self.dims, self.state, dev(m, torch.int32), K)
         self.oracle.accept(np.asarray(m)[self.seqs], K)
+
+    # ----------------------------------------------- every unit of a call
+    def snapshot(self):
+        """Host copies of what the next decode reads: the checkpoint as the
+        kernels read it (the read copy, else the FP32 checkpoint), every ring
+        field and the ring pointers, for the whole batch."""
+        st = self.state
+        S = st.S_read if st.S_read is not None else st.S_ckpt
+        return {"S": S.cpu(), "ring": {k: v.cpu() for k, v in st.ring.items()},
+                "head": st.ring_head.cpu().numpy().astype(np.int64),
+                "len": st.ring_len.cpu().numpy().astype(np.int64)}
+
+    def check_all_units(self, snap, tok, out, what, chunk=16):
+        """Every (sequence, head) output of the decode that followed ``snap``,
+        against the oracle's replay formula evaluated on the GPU's own
+        checkpoint copy and ring, the values the kernels read. This reaches
+        every unit of every persistent block, whatever the sampled oracle
+        follows. The decode must not have folded (len + 1 <= W everywhere)."""
+        wl, W = self.wl, self.wl.window
+        head, lens = snap["head"], snap["len"]
+        assert (lens + 1 <= W).all(), "a folding step: use a plain one"
+        out = host(out)
+        for lo in range(0, wl.batch, chunk):
+            for n in np.unique(lens[lo:lo + chunk]):
+                sel = np.arange(lo, min(lo + chunk, wl.batch))
+                sel = sel[lens[sel] == n]
+                ent = [self._ring_entry(snap, sel, (head[sel] + j) % W) for j in range(n)]
+                cur = {k: np.asarray(v)[sel] for k, v in tok.items()}
+                Sc = snap["S"][torch.from_numpy(sel)].double().numpy()
+                if self.kind == "mamba2":
+                    ent.append({k: cur[k] for k in ("x", "B", "dt")})
+                    ref = rep.mamba2_replay_output(Sc, ent, cur["C"], self.A, self.D)
+                else:
+                    ent.append({k: cur[k] for k in ("k", "v", "alpha", "beta")})
+                    ref = rep.delta_replay_output(Sc, ent, cur["q"], self.scale)
+                f32_close(out[sel], ref, f"{what}: all units, sequences {sel[0]}..{sel[-1]}")
+
+    def _ring_entry(self, snap, sel, slot):
+        """Ring entry at per-sequence slots ``slot`` of sequences ``sel``, in
+        the oracle's entry layout (float64)."""
+        r, rows, n = snap["ring"], torch.from_numpy(sel), np.arange(len(sel))
+        slot = np.asarray(slot, np.int64)
+        # per-head fields are [b, H, W(d), ...]: pick slot[i] of sequence sel[i]
+        per_head = lambda name: r[name][rows].double().numpy()[n, :, slot]  # noqa: E731
+        if self.kind == "mamba2":
+            return {"x": per_head("x"), "dt": per_head("dt"),
+                    "B": r["B"][rows, torch.from_numpy(slot)].double().numpy()}
+        return {"k": per_head("k"), "v": per_head("v"), "alpha": per_head("alpha"),
+                "beta": per_head("beta")}
 
     # ------------------------------------------------------------- checks
     def check_pointers(self, what=""):

@@ -5,17 +5,20 @@ import pytest
 import torch
 
 import synth
-from gpu_harness import Session, dev, f32_close, host
+from gpu_harness import Session, dev, f32_close, host, spread
 from oracle import recurrences as rec
 from recurrent_state_fp32_b300 import api
 
 pytestmark = pytest.mark.gpu
 
 
-def run(s, steps, check_every=8):
+def run(s, steps, check_every=8, all_units_at=()):
     for t in range(steps):
         s.consolidate(1)
-        s.decode(t)
+        snap = s.snapshot() if t in all_units_at else None
+        y, _ = s.decode(t)
+        if snap is not None:
+            s.check_all_units(snap, s.last_tok, y, f"step {t}")
         if t % check_every == 0:
             s.check_pointers(f"step {t}")
             s.check_ring(f"step {t}")
@@ -87,21 +90,29 @@ def test_full_ring_is_refused():
     s.check_ring()
 
 
+@pytest.mark.parametrize("read", ["bf16", "f32"])
 @pytest.mark.parametrize("kind", ["gdn", "kda"])
-def test_full_size_sampled(kind):
-    """b256, H32, d_k = d_v = 128, W16, 256 steps, BF16 read copy; oracle on a sample."""
+def test_full_size_sampled(kind, read):
+    """b256, H32, d_k = d_v = 128, W16, 256 steps, BF16 inputs, BF16 read copy
+    or FP32 read path. The oracle follows every head of 8 sequences spread
+    over the batch; at three steps every (sequence, head) output is also
+    checked against the replay formula on the GPU's own checkpoint copy and
+    ring."""
     wl = synth.DeltaWorkload(kind, batch=256, heads=32, dk=128, dv=128, window=16, steps=256,
                              in_dtype="bf16", seed=3 if kind == "gdn" else 5)
-    s = Session(kind, wl, "bf16", seqs=[0, 131, 255], heads=[0, 17, 31])
-    run(s, wl.steps, check_every=41)
+    s = Session(kind, wl, read, seqs=spread(wl.batch))
+    run(s, wl.steps, check_every=41, all_units_at=(6, 130, 249))
 
 
-@pytest.mark.parametrize("kind", ["gdn", "kda"])
-def test_full_size_fp32_read_sampled(kind):
-    wl = synth.DeltaWorkload(kind, batch=256, heads=32, dk=128, dv=128, window=16, steps=40,
-                             in_dtype="bf16", seed=3)
-    s = Session(kind, wl, "f32", seqs=[2, 200], heads=[5, 30])
-    run(s, wl.steps, check_every=13)
+@pytest.mark.parametrize("batch", [1, 8, 64, 512])
+def test_kda_batch_sweep_sizes(batch):
+    """The KDA layer at the other batch sizes of the batch sweep (1, 8, 64,
+    512; 256 is above), 256 steps, BF16 read copy; every head of up to 8
+    sequences against the oracle, every unit at two steps."""
+    wl = synth.DeltaWorkload("kda", batch=batch, heads=32, dk=128, dv=128, window=16, steps=256,
+                             in_dtype="bf16", seed=5)
+    s = Session("kda", wl, "bf16", seqs=spread(batch, min(8, batch)))
+    run(s, wl.steps, check_every=53, all_units_at=(11, 200))
 
 
 @pytest.mark.parametrize("kind", ["gdn", "kda"])

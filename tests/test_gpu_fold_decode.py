@@ -15,18 +15,21 @@ import pytest
 import torch
 
 import synth
-from gpu_harness import Session, bf16_close, f32_close, host
+from gpu_harness import Session, bf16_close, f32_close, host, spread
 from recurrent_state_fp32_b300 import api
 
 pytestmark = pytest.mark.gpu
 
 
-def run(s, steps, check_every=8, joins=False):
+def run(s, steps, check_every=8, joins=False, all_units_at=()):
     folds = 0
     for t in range(steps):
         if joins and t % 3 == 0:  # a slot changes hands: ring phases spread
             s.join([(t // 3) % s.wl.batch], seed=2000 + t)
-        _, _, fold = s.fold_decode(t)
+        snap = s.snapshot() if t in all_units_at else None
+        y, _, fold = s.fold_decode(t)
+        if snap is not None:
+            s.check_all_units(snap, s.last_tok, y, f"fused step {t}")
         folds += int(fold.sum())
         if t % check_every == 0:
             s.check_pointers(f"step {t}")
@@ -113,12 +116,17 @@ def test_same_as_two_calls(read):
         assert torch.equal(rd, b.state.S_ckpt.to(torch.bfloat16).view(torch.int16))
 
 
-def test_full_size_sampled():
-    """b256, H128, P64, N128, W16, BF16 read copy, 48 steps; oracle on a sample."""
-    wl = synth.Mamba2Workload(batch=256, heads=128, P=64, N=128, window=16, steps=48,
+@pytest.mark.parametrize("read", ["bf16", "f32"])
+def test_full_size_sampled(read):
+    """b256, H128, P64, N128, W16, 256 steps (16 lockstep folds), BF16 read
+    copy or FP32 read path. The oracle follows every head of 8 sequences
+    spread over the batch; at three steps that fold nothing every (sequence,
+    head) output is also checked against the replay formula on the GPU's own
+    checkpoint copy and ring."""
+    wl = synth.Mamba2Workload(batch=256, heads=128, P=64, N=128, window=16, steps=256,
                               in_dtype="bf16", seed=2)
-    s = Session("mamba2", wl, "bf16", seqs=[0, 97, 255], heads=[0, 61, 127])
-    assert run(s, wl.steps, check_every=17) > 0
+    s = Session("mamba2", wl, read, seqs=spread(wl.batch))
+    assert run(s, wl.steps, check_every=37, all_units_at=(3, 77, 250)) > 0
 
 
 def test_full_size_staggered_sampled():

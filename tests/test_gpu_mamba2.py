@@ -5,17 +5,20 @@ import pytest
 import torch
 
 import synth
-from gpu_harness import Session, dev, f32_close, host
+from gpu_harness import Session, dev, f32_close, host, spread
 from oracle import recurrences as rec
 from recurrent_state_fp32_b300 import api
 
 pytestmark = pytest.mark.gpu
 
 
-def run(s, steps, check_every=8):
+def run(s, steps, check_every=8, all_units_at=()):
     for t in range(steps):
         s.consolidate(1)
-        s.decode(t)
+        snap = s.snapshot() if t in all_units_at else None
+        y, _ = s.decode(t)
+        if snap is not None:
+            s.check_all_units(snap, s.last_tok, y, f"step {t}")
         if t % check_every == 0:
             s.check_pointers(f"step {t}")
             s.check_ring(f"step {t}")
@@ -87,19 +90,16 @@ def test_forced_fold_with_empty_ring_is_a_noop():
     s.check_pointers()
 
 
-def test_full_size_sampled():
-    """b256, H128, P64, N128, W16, 256 steps, BF16 read copy; oracle on a sample."""
+@pytest.mark.parametrize("read", ["bf16", "f32"])
+def test_full_size_sampled(read):
+    """b256, H128, P64, N128, W16, 256 steps, BF16 inputs, BF16 read copy or
+    FP32 read path. The oracle follows every head of 8 sequences spread over
+    the batch; at three steps every (sequence, head) output is also checked
+    against the replay formula on the GPU's own checkpoint copy and ring."""
     wl = synth.Mamba2Workload(batch=256, heads=128, P=64, N=128, window=16, steps=256,
                               in_dtype="bf16", seed=2)
-    s = Session("mamba2", wl, "bf16", seqs=[0, 97, 255], heads=[0, 61, 127])
-    run(s, wl.steps, check_every=37)
-
-
-def test_full_size_fp32_read_sampled():
-    wl = synth.Mamba2Workload(batch=256, heads=128, P=64, N=128, window=16, steps=48,
-                              in_dtype="bf16", seed=2)
-    s = Session("mamba2", wl, "f32", seqs=[1, 128, 254], heads=[3, 64, 126])
-    run(s, wl.steps, check_every=16)
+    s = Session("mamba2", wl, read, seqs=spread(wl.batch))
+    run(s, wl.steps, check_every=37, all_units_at=(5, 120, 250))
 
 
 @pytest.mark.parametrize("N,P", [(128, 64), (64, 96)])

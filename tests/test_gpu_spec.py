@@ -4,7 +4,7 @@ import numpy as np
 import pytest
 
 import synth
-from gpu_harness import Session
+from gpu_harness import Session, spread
 
 pytestmark = pytest.mark.gpu
 
@@ -67,11 +67,13 @@ def test_bad_accept_and_full_ring():
 
 
 def test_full_size_sampled():
-    """b512, H32, d_k = d_v = 128, K = 4, W = 16 (the speculative workload), 24 rounds."""
+    """b512, H32, d_k = d_v = 128, K = 4, W = 16 (the speculative workload), its
+    128 rounds; the oracle follows every head of 4 sequences spread over the
+    batch."""
     wl = synth.DeltaWorkload("gdn", batch=512, heads=32, dk=128, dv=128, window=16, K=4,
                              in_dtype="bf16", seed=4)
-    s = Session("gdn", wl, "bf16", seqs=[0, 311, 511], heads=[0, 16, 31])
-    run(s, 24, 4, check_every=7)
+    s = Session("gdn", wl, "bf16", seqs=spread(wl.batch, 4))
+    run(s, 128, 4, check_every=17)
 
 
 @pytest.mark.parametrize("kind,dk,dv,in_dtype", [("gdn", 128, 128, "bf16"), ("kda", 64, 96, "f32")])

@@ -1,51 +1,39 @@
 """Sequence state copies (prefix caching / continuous batching): a sequence
-forked mid-stream into another slot continues exactly like its source."""
+forked mid-stream into another slot resumes from the copied checkpoint, ring
+and pointers; the oracle forks the same way and both sides must agree."""
 
-import numpy as np
 import pytest
-import torch
 
 import synth
-from gpu_harness import Session, dev, host
-
-from recurrent_state_fp32_b300 import api
+from gpu_harness import Session, host
 
 pytestmark = pytest.mark.gpu
 
 
 def _fork_and_continue(s, steps_before, steps_after, src, dst):
+    """Decode, fork src into dst mid-ring (dst at another ring phase: it
+    restarted earlier), and decode on; the oracle forks too, and every
+    output, pointer, ring byte and the final checkpoint match it, for the
+    sources and the copies alike."""
     for t in range(steps_before):
-        s.consolidate(1)
-        s.decode(t, check=False)
-    api.copy_sequences(s.dims, s.state, dev(np.array(src, np.int32), torch.int32), s.state,
-                       dev(np.array(dst, np.int32), torch.int32))
+        if t == 2:
+            s.join(dst, seed=700)  # the destination slots take a new sequence
+        s.consolidate(1, force=(t == 4))  # a partial fold moves the ring head
+        s.decode(t)
+    h, ln = host(s.state.ring_head), host(s.state.ring_len)
+    assert all(ln[q] > 0 for q in src), "fork taken mid-ring"
+    assert any((h[a], ln[a]) != (h[b], ln[b]) for a, b in zip(src, dst)), "phases differ"
+    s.check_pointers("before the fork")
+    s.fork(src, dst)
+    s.check_pointers("after the fork")
+    s.check_ring("after the fork")
     for t in range(steps_before, steps_before + steps_after):
-        tok = s.token(t)
-        # the forked sequences get their sources' tokens
-        for k, v in tok.items():
-            if s.kind == "mamba2" and k in ("B", "C"):
-                v[dst] = v[src]
-            else:
-                v[dst] = v[src]
-        g = s._to_dev(tok)
-        api.consolidate(s.dims, s.state, s.dA if s.kind == "mamba2" else None, 1, False)
-        rows = s.wl.P if s.kind == "mamba2" else s.wl.dv
-        y = torch.full((s.wl.batch, s.wl.heads, rows), float("nan"), device="cuda")
-        if s.kind == "mamba2":
-            api.mamba2_decode(s.dims, s.state, s.dA, s.dD, g["x"], g["B"], g["C"], g["dt"], y)
-        else:
-            api.gdn_decode(s.dims, s.state, g["q"], g["k"], g["v"], g["alpha"], g["beta"], 1.0, y)
-        yh = host(y)
-        assert np.array_equal(yh[dst], yh[src]), f"step {t}: forked outputs differ"
-    st = s.state
-    for name in ("ring_head", "ring_len", "status"):
-        a = host(getattr(st, name))
-        assert np.array_equal(a[dst], a[src]), name
-    for k, v in st.ring.items():
-        a = host(v)
-        assert np.array_equal(a[dst], a[src]), f"ring {k}"
-    S = host(st.S_ckpt)
-    assert np.array_equal(S[dst], S[src])
+        s.consolidate(1)
+        s.decode(t)
+        s.check_pointers(f"step {t}")
+        s.check_ring(f"step {t}")
+    s.consolidate(1, force=True)
+    s.check_checkpoint("end")
 
 
 def test_mamba2_fork_mid_ring():
