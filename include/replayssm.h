@@ -321,15 +321,18 @@ REPLAYSSM_API replayssm_status replayssm_conventional_accept(const replayssm_dim
  * may be NULL; every other state field, input and output is as for
  * replayssm_mamba2_decode, and the caller still owns all of them.
  *
- * Limit: align256(replayssm_workspace_bytes(dims, 1)) + 4 * batch bytes must
- * not exceed REPLAYSSM_NOALLOC_SCRATCH_BYTES, else the call returns
- * REPLAYSSM_ERR_SCRATCH_LIMIT before any CUDA call. (Batch 256 x 128 heads
- * at P = 64 needs about 8.5 MiB.)
+ * Limit: replayssm_mamba2_decode_noalloc_bytes(dims) bytes must not exceed
+ * REPLAYSSM_NOALLOC_SCRATCH_BYTES, else the call returns
+ * REPLAYSSM_ERR_SCRATCH_LIMIT before any CUDA call. That is the plain
+ * decode's per-head rows, batch * heads * align4(P + 1) * 4 bytes, plus one
+ * 4-byte flag per sequence rounded up to 16 bytes, rounded up to 256 bytes,
+ * plus 4 * batch bytes of arrival counters. (Batch 256 x 128 heads at
+ * P = 64 needs about 8.5 MiB.)
  *
  * The array exists once per GPU that loads the library and is held until the
- * process exits. The first call on a device (with that device current) looks
- * up the array's device address, once; make that first call before any stream
- * capture. Each call clears the arrival counters (the only part that must
+ * process exits. Every call looks up the array's device address in the
+ * current device's context (no call allocates). Each call clears the arrival
+ * counters (the only part that must
  * start at zero) on `stream` before its kernels; the workspace rows and flags
  * are written before they are read. All calls share the one array, so calls
  * whose work overlaps on the GPU (other streams, other host threads) race and
@@ -341,6 +344,14 @@ REPLAYSSM_API replayssm_status replayssm_mamba2_decode_noalloc(
 
 /* Size of the fixed scratch of replayssm_mamba2_decode_noalloc. */
 #define REPLAYSSM_NOALLOC_SCRATCH_BYTES (16u << 20)
+
+/*
+ * Bytes of the fixed scratch that replayssm_mamba2_decode_noalloc needs for
+ * these sizes (the formula above), so a caller can check the limit before
+ * it calls; 0 if dims is invalid or not a Mamba-2 layer. Host only, no CUDA
+ * call. The paper has no counterpart: a library convenience.
+ */
+REPLAYSSM_API int64_t replayssm_mamba2_decode_noalloc_bytes(const replayssm_dims* dims);
 
 /*
  * Copies whole sequences between two layer states of the same dims: for each

@@ -45,6 +45,7 @@ _F = ctypes.c_float
 SIGNATURES = {
     "replayssm_mamba2_decode": [_DP, _SP, _P, _P, _P, _P, _P, _P, _P, _P],
     "replayssm_mamba2_decode_noalloc": [_DP, _SP, _P, _P, _P, _P, _P, _P, _P, _P],
+    "replayssm_mamba2_decode_noalloc_bytes": [_DP],
     "replayssm_gdn_decode": [_DP, _SP, _P, _P, _P, _P, _P, _F, _P, _P],
     "replayssm_consolidate": [_DP, _SP, _P, _I, _I, _P],
     "replayssm_mamba2_fold_decode": [_DP, _SP, _P, _P, _P, _P, _P, _P, _P, _P],
@@ -74,7 +75,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         fn = getattr(lib, name)
         fn.argtypes = args
         fn.restype = {"replayssm_status_string": ctypes.c_char_p,
-                      "replayssm_workspace_bytes": ctypes.c_int64}.get(name, ctypes.c_int32)
+                      "replayssm_workspace_bytes": ctypes.c_int64,
+                      "replayssm_mamba2_decode_noalloc_bytes": ctypes.c_int64}.get(name, ctypes.c_int32)
     return lib
 
 

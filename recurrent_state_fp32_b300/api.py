@@ -172,6 +172,12 @@ def mamba2_decode_noalloc(dims, state, A, D, x, B, C, dt, y, stream=None):
           _ptr(dt), _ptr(y), _stream(stream))
 
 
+def mamba2_decode_noalloc_bytes(dims: LayerDims) -> int:
+    """Bytes of the fixed scratch mamba2_decode_noalloc needs for these sizes
+    (at most NOALLOC_SCRATCH_BYTES, else the call is refused); 0 if invalid."""
+    return int(_abi.lib.replayssm_mamba2_decode_noalloc_bytes(ctypes.byref(dims.c())))
+
+
 def mamba2_fold_decode(dims, state, A, D, x, B, C, dt, y, stream=None):
     """consolidate(k_next=1) then mamba2_decode in one call: a full ring is
     folded while its state rows stream past."""

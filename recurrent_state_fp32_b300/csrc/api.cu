@@ -279,24 +279,14 @@ struct NoallocLayout {
   }
 };
 
-// Device address of g_noalloc_scratch on the current device, looked up once
-// per device with that device current.
+// Device address of g_noalloc_scratch in the current device's context,
+// looked up on every call (a cheap query next to the launches): a cached
+// address would go stale if the context were torn down and made again.
 cudaError_t noalloc_scratch(unsigned char** out) {
-  constexpr int kMaxDevices = 64;
-  static std::mutex mu;
-  static unsigned char* addr[kMaxDevices] = {};
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  void* p = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  std::lock_guard<std::mutex> lock(mu);
-  if (!addr[dev]) {
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-    if (e != cudaSuccess) return e;
-    addr[dev] = static_cast<unsigned char*>(p);
-  }
-  *out = addr[dev];
+  *out = static_cast<unsigned char*>(p);
   return cudaSuccess;
 }
 
@@ -540,6 +530,11 @@ REPLAYSSM_API int64_t replayssm_workspace_bytes(const replayssm_dims* dims, int3
   const long long b = rs::WorkLayout(*dims, K < 1 ? 1 : K).bytes();
   if (dims->kind != REPLAYSSM_MAMBA2) return b;
   return std::max<long long>(b, rs::StepLayout(*dims).bytes());
+}
+
+REPLAYSSM_API int64_t replayssm_mamba2_decode_noalloc_bytes(const replayssm_dims* dims) {
+  if (check_dims(dims) != REPLAYSSM_OK || dims->kind != REPLAYSSM_MAMBA2) return 0;
+  return NoallocLayout(*dims).total;
 }
 
 REPLAYSSM_API replayssm_status replayssm_mamba2_decode_noalloc(

@@ -40,15 +40,42 @@ def _noalloc(d, s, A=FAKE, y=FAKE):
         A, FAKE, FAKE, FAKE, FAKE, FAKE, y, None)
 
 
+# One sequence of P = 64 heads: each head takes a 68-float workspace row
+# (P + 1 rounded up to 4); BOUNDARY_HEADS is the most the 16 MiB array holds.
+BOUNDARY_HEADS = 61679
+
+
+def _size(batch, heads, P=64, N=128, W=16):
+    d = _abi.Dims(_abi.MAMBA2, batch, heads, 1, N, P, W, _abi.BF16)
+    return _abi.lib.replayssm_mamba2_decode_noalloc_bytes(ctypes.byref(d))
+
+
+def test_scratch_size_query():
+    """The size query follows the documented formula and puts the refusal
+    boundary where the call does."""
+    def formula(b, H, P):
+        rows = b * H * ((P + 1 + 3) // 4 * 4) * 4 + (4 * b + 15) // 16 * 16
+        return (rows + 255) // 256 * 256 + 4 * b
+
+    for b, H, P in ((1, 8, 64), (256, 128, 64), (5, 6, 96), (3, 1, 32), (1, BOUNDARY_HEADS, 64)):
+        assert _size(b, H, P) == formula(b, H, P), (b, H, P)
+    assert _size(256, 128) < 9 << 20
+    assert _size(1, BOUNDARY_HEADS) <= _abi.NOALLOC_SCRATCH_BYTES < _size(1, BOUNDARY_HEADS + 1)
+    r = ctypes.byref
+    assert _abi.lib.replayssm_mamba2_decode_noalloc_bytes(None) == 0
+    gdn = _abi.Dims(_abi.GDN, 2, 8, 1, 128, 64, 16, _abi.BF16)
+    assert _abi.lib.replayssm_mamba2_decode_noalloc_bytes(r(gdn)) == 0
+    bad = _abi.Dims(_abi.MAMBA2, 2, 8, 1, 96, 64, 16, _abi.BF16)
+    assert _abi.lib.replayssm_mamba2_decode_noalloc_bytes(r(bad)) == 0
+
+
 def test_arguments_and_the_size_limit():
     """Argument errors and the scratch limit are reported before any CUDA call."""
     no_scratch = dict(work=None, sync=None)
     big = _abi.Dims(_abi.MAMBA2, 4096, 128, 1, 128, 256, 16, _abi.BF16)
     assert _noalloc(big, _state(**no_scratch)) == _abi.ERR_SCRATCH_LIMIT
     assert b"16 MiB" in _abi.lib.replayssm_status_string(_abi.ERR_SCRATCH_LIMIT)
-    # 64 heads more than 16 MiB holds at P = 64 (68 floats a workspace row)
-    rows = (_abi.NOALLOC_SCRATCH_BYTES - 4096) // (68 * 4)
-    over = _abi.Dims(_abi.MAMBA2, 1, rows + 64, 1, 128, 64, 16, _abi.BF16)
+    over = _abi.Dims(_abi.MAMBA2, 1, BOUNDARY_HEADS + 1, 1, 128, 64, 16, _abi.BF16)
     assert _noalloc(over, _state(**no_scratch)) == _abi.ERR_SCRATCH_LIMIT
     empty = _abi.Dims(_abi.MAMBA2, 0, 8, 1, 128, 64, 16, _abi.BF16)
     assert _noalloc(empty, _state(**no_scratch)) == _abi.OK
@@ -68,24 +95,34 @@ CASES = {
     # 64 sequences of the 128-head, P = 64, N = 128, W = 16 layer, BF16 read copy
     "layer": dict(batch=64, heads=128, P=64, N=128, groups=1, window=16, in_dtype="bf16",
                   read=True),
+    # one sequence with as many heads as the fixed array holds (2 GB of state)
+    "boundary": dict(batch=1, heads=BOUNDARY_HEADS, P=64, N=128, groups=1, window=3,
+                     in_dtype="bf16", read=False),
 }
 
 
-@pytest.mark.gpu
-@pytest.mark.parametrize("case", sorted(CASES))
-def test_matches_the_allocating_entry_point(case):
+def _compare(case):
+    """Decodes a few buffered tokens through the ordinary entry point on two
+    identical states, then makes two allocation-free calls in a row (the second
+    finds the array as the first left it) and one on a full ring, each against
+    replayssm_mamba2_decode on the twin state: outputs within the parity
+    tolerance, ring bytes, pointers and status bit-exact."""
     c = CASES[case]
     b, H, P, N, G, W = (c[k] for k in ("batch", "heads", "P", "N", "groups", "window"))
     seed = 11
     dims = api.LayerDims("mamba2", b, H, dk=N, dv=P, window=W, groups=G, in_dtype=c["in_dtype"])
+    assert api.mamba2_decode_noalloc_bytes(dims) <= _abi.NOALLOC_SCRATCH_BYTES
     vt = torch.float32 if c["in_dtype"] == "f32" else torch.bfloat16
     A, D, bias = synth.mamba2_params(seed, H)
     A, D = torch.from_numpy(A).cuda(), torch.from_numpy(D).cuda()
-    S0 = torch.from_numpy(synth.mamba2_initial_state(seed, b, H, P, N)).cuda()
     ref = api.LayerState(dims, read_copy=c["read"])
     new = api.LayerState(dims, read_copy=c["read"])
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(seed)
+    S0 = torch.empty_like(ref.S_ckpt).normal_(0.0, 0.1, generator=gen)
     for st in (ref, new):
         st.set_checkpoint(S0)
+    del S0
 
     def token(t):
         tok = synth.mamba2_step_inputs(seed, t, b, H, G, P, N, bias, c["in_dtype"])
@@ -107,7 +144,7 @@ def test_matches_the_allocating_entry_point(case):
     c_new = _abi.State.from_buffer_copy(new.c())
     c_new.work = None
     c_new.sync = None
-    for t in (W - 2, W - 1):  # two calls in a row
+    for t in (W - 2, W - 1, W):  # two calls in a row, then one on a full ring
         tok = token(t)
         y_ref = torch.full((b, H, P), float("nan"), device="cuda")
         y_new = torch.full((b, H, P), float("nan"), device="cuda")
@@ -118,10 +155,27 @@ def test_matches_the_allocating_entry_point(case):
             ctypes.byref(dims.c()), ctypes.byref(c_new), A.data_ptr(), D.data_ptr(),
             *args(tok, y_new), None))
         torch.cuda.synchronize()
-        f32_close(host(y_new), host(y_ref), f"{case} token {t}: y")
         for name in ("ring_len", "ring_head", "status"):
             assert torch.equal(getattr(new, name), getattr(ref, name)), f"{case} token {t}: {name}"
         for k, v in ref.ring.items():
             assert torch.equal(new.ring[k], v), f"{case} token {t}: ring {k}"
-        assert int(ref.status.abs().sum()) == 0
-        assert (host(ref.ring_len) == t + 1).all()
+        if t < W:
+            f32_close(host(y_new), host(y_ref), f"{case} token {t}: y")
+            assert int(ref.status.abs().sum()) == 0
+            assert (host(ref.ring_len) == t + 1).all()
+        else:  # refused: status bit set, output not written, state untouched
+            assert torch.isnan(y_new).all() and torch.isnan(y_ref).all(), f"{case}: y written"
+            assert (host(new.status) == _abi.SEQ_RING_FULL).all()
+            assert (host(new.ring_len) == W).all()
+    del ref, new
+    torch.cuda.empty_cache()
+
+
+@pytest.mark.gpu
+def test_matches_the_allocating_entry_point():
+    """The cases one after another in one process, so that each call finds the
+    array holding the previous case's rows, of another layout: the small
+    ragged layer, the 128-head layer, the small one again, then the largest
+    size the array holds."""
+    for case in ("ragged", "layer", "ragged", "boundary"):
+        _compare(case)
