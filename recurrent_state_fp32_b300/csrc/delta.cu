@@ -617,143 +617,129 @@ __device__ __forceinline__ void stage_rows_f32(float* dst, const TI* head_rows, 
 
 constexpr int kDFoldThreads = 256;
 
-// The n-entry fold of two rows of one head held in registers: rows r0 and
-// r1 (r1 only when has1), each spread over DK / 32 lanes, lane q holding the
-// float4 chunks q, q + DK / 32, ... of the row. Each row evolves
-// independently,
+// Rows of the fold held per thread, and lanes per row: each lane holds 16
+// columns of each of its kFoldRowsPT rows (float4 chunks q, q + L, q + 2L and
+// q + 3L of the row, L = DK / 16 lanes per row), so a thread runs four
+// independent per-entry chains and the lanes of a row share every k_j load.
+constexpr int kFoldRowsPT = 4;
+template <int DK>
+__host__ __device__ constexpr int fold_lanes_per_row() { return DK / 16; }
+
+// The n-entry fold of a thread's kFoldRowsPT rows of one head, held in
+// registers (rows r[i], present when i < nr; absent rows compute on a
+// copy of row 0 and are never stored). Each row evolves independently,
 //   s <- alpha (.) s;  s <- s + beta (v[r] - s . k) k   for j = 0..n-1,
 // with the entries (float, entry order) in shared memory. A scalar GDN gate
-// is applied lazily: the row holds s / gam, gam the product of the gates so
-// far, and is rescaled once at the end. k_j (and a KDA gate row) are read
-// from shared memory per use: the lanes of a warp share DK / 32 addresses,
-// so each read is one broadcast.
+// is applied lazily: the rows hold s / gam, gam the product of the gates so
+// far, and are rescaled once at the end. k_j (and a KDA gate row) are read
+// once per entry from shared memory for all four rows: the L lanes of a row
+// read L consecutive float4, one conflict-free broadcast per chunk.
 template <int DK, bool KDA>
-__device__ __forceinline__ void fold_row_pair(float2 (&s0)[16], float2 (&s1)[16], bool has1,
-                                              int r0, int r1, int n, int DV, int q,
-                                              const float* kbuf, const float* abuf,
-                                              const float* vbuf, const float* bbuf,
-                                              const float* rbuf) {
-  constexpr int LPR = DK / 32;
+__device__ __forceinline__ void fold_rows(float2 (&s)[kFoldRowsPT][8], const int (&r)[kFoldRowsPT],
+                                          int n, int DV, int q, const float* kbuf,
+                                          const float* abuf, const float* vbuf,
+                                          const float* bbuf, const float* rbuf) {
+  constexpr int L = fold_lanes_per_row<DK>();
   float gam = 1.f, igam = 1.f;  // GDN: product of the gates so far, and its inverse
   for (int j = 0; j < n; ++j) {
     const float4* kj = reinterpret_cast<const float4*>(kbuf + (size_t)j * DK) + q;
+    float4 kc[4];
+#pragma unroll
+    for (int m = 0; m < 4; ++m) kc[m] = kj[L * m];
     if (KDA) {
       const float4* aj = reinterpret_cast<const float4*>(abuf + (size_t)j * DK) + q;
 #pragma unroll
-      for (int m = 0; m < 8; ++m) {
-        const float4 u = aj[LPR * m];
+      for (int m = 0; m < 4; ++m) {
+        const float4 u = aj[L * m];
         const float2 g0 = make_float2(u.x, u.y), g1 = make_float2(u.z, u.w);
-        s0[2 * m] = __fmul2_rn(s0[2 * m], g0);
-        s0[2 * m + 1] = __fmul2_rn(s0[2 * m + 1], g1);
-        s1[2 * m] = __fmul2_rn(s1[2 * m], g0);
-        s1[2 * m + 1] = __fmul2_rn(s1[2 * m + 1], g1);
+#pragma unroll
+        for (int i = 0; i < kFoldRowsPT; ++i) {
+          s[i][2 * m] = __fmul2_rn(s[i][2 * m], g0);
+          s[i][2 * m + 1] = __fmul2_rn(s[i][2 * m + 1], g1);
+        }
       }
     } else {
       gam *= abuf[j];
       igam *= rbuf[j];
     }
-    float dot0, dot1;
-    if (KDA) {
+    float dot[kFoldRowsPT];
+#pragma unroll
+    for (int i = 0; i < kFoldRowsPT; ++i) {  // two accumulators per row
       float2 d0 = make_float2(0.f, 0.f), d1 = make_float2(0.f, 0.f);
 #pragma unroll
-      for (int m = 0; m < 8; ++m) {
-        const float4 u = kj[LPR * m];
-        const float2 ka = make_float2(u.x, u.y), kb = make_float2(u.z, u.w);
-        d0 = __ffma2_rn(s0[2 * m], ka, d0);
-        d1 = __ffma2_rn(s1[2 * m], ka, d1);
-        d0 = __ffma2_rn(s0[2 * m + 1], kb, d0);
-        d1 = __ffma2_rn(s1[2 * m + 1], kb, d1);
+      for (int m = 0; m < 4; ++m) {
+        d0 = __ffma2_rn(s[i][2 * m], make_float2(kc[m].x, kc[m].y), d0);
+        d1 = __ffma2_rn(s[i][2 * m + 1], make_float2(kc[m].z, kc[m].w), d1);
       }
-      dot0 = d0.x + d0.y;
-      dot1 = d1.x + d1.y;
-    } else {  // two accumulators per row: shorter dependency chains
-      float2 d0 = make_float2(0.f, 0.f), d1 = make_float2(0.f, 0.f);
-      float2 e0 = make_float2(0.f, 0.f), e1 = make_float2(0.f, 0.f);
-#pragma unroll
-      for (int m = 0; m < 8; ++m) {
-        const float4 u = kj[LPR * m];
-        const float2 ka = make_float2(u.x, u.y), kb = make_float2(u.z, u.w);
-        d0 = __ffma2_rn(s0[2 * m], ka, d0);
-        d1 = __ffma2_rn(s1[2 * m], ka, d1);
-        e0 = __ffma2_rn(s0[2 * m + 1], kb, e0);
-        e1 = __ffma2_rn(s1[2 * m + 1], kb, e1);
-      }
-      dot0 = ((d0.x + d0.y) + (e0.x + e0.y)) * gam;
-      dot1 = ((d1.x + d1.y) + (e1.x + e1.y)) * gam;
+      dot[i] = (d0.x + d0.y) + (d1.x + d1.y);
     }
 #pragma unroll
-    for (int o = 1; o < LPR; o <<= 1) {
-      dot0 += __shfl_xor_sync(kFull, dot0, o);
-      dot1 += __shfl_xor_sync(kFull, dot1, o);
+    for (int o = 1; o < L; o <<= 1) {
+#pragma unroll
+      for (int i = 0; i < kFoldRowsPT; ++i) dot[i] += __shfl_xor_sync(kFull, dot[i], o);
     }
     const float bj = bbuf[j];
-    float c0 = bj * (vbuf[(size_t)j * DV + r0] - dot0);
-    float c1 = has1 ? bj * (vbuf[(size_t)j * DV + r1] - dot1) : 0.f;
-    if (!KDA) {
-      c0 *= igam;
-      c1 *= igam;
-    }
-    const float2 cc0 = make_float2(c0, c0), cc1 = make_float2(c1, c1);
+    const float* vj = vbuf + (size_t)j * DV;
 #pragma unroll
-    for (int m = 0; m < 8; ++m) {
-      const float4 u = kj[LPR * m];
-      const float2 ka = make_float2(u.x, u.y), kb = make_float2(u.z, u.w);
-      s0[2 * m] = __ffma2_rn(cc0, ka, s0[2 * m]);
-      s0[2 * m + 1] = __ffma2_rn(cc0, kb, s0[2 * m + 1]);
-      s1[2 * m] = __ffma2_rn(cc1, ka, s1[2 * m]);
-      s1[2 * m + 1] = __ffma2_rn(cc1, kb, s1[2 * m + 1]);
+    for (int i = 0; i < kFoldRowsPT; ++i) {
+      float c = KDA ? bj * (vj[r[i]] - dot[i]) : bj * (vj[r[i]] - dot[i] * gam) * igam;
+      const float2 cc = make_float2(c, c);
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {
+        s[i][2 * m] = __ffma2_rn(cc, make_float2(kc[m].x, kc[m].y), s[i][2 * m]);
+        s[i][2 * m + 1] = __ffma2_rn(cc, make_float2(kc[m].z, kc[m].w), s[i][2 * m + 1]);
+      }
     }
   }
   if (!KDA) {
     const float2 gg = make_float2(gam, gam);
 #pragma unroll
-    for (int m = 0; m < 16; ++m) {
-      s0[m] = __fmul2_rn(s0[m], gg);
-      s1[m] = __fmul2_rn(s1[m], gg);
+    for (int i = 0; i < kFoldRowsPT; ++i) {
+#pragma unroll
+      for (int m = 0; m < 8; ++m) s[i][m] = __fmul2_rn(s[i][m], gg);
     }
   }
 }
 
-// Two rows in the layout of fold_row_pair from a row-major [rows][DK] FP32
-// block (global or shared memory); the second row only when has1.
+// A thread's rows in the layout of fold_rows from a row-major [rows][DK]
+// FP32 block (global or shared memory): row i is block row r[i].
 template <int DK>
-__device__ __forceinline__ void load_row_pair(const float* row0, const float* row1, bool has1,
-                                              int q, float2 (&s0)[16], float2 (&s1)[16]) {
-  constexpr int LPR = DK / 32;
-  const float4* p0 = reinterpret_cast<const float4*>(row0) + q;
-  const float4* p1 = reinterpret_cast<const float4*>(has1 ? row1 : row0) + q;
+__device__ __forceinline__ void load_rows(const float* block, const int (&r)[kFoldRowsPT], int q,
+                                          float2 (&s)[kFoldRowsPT][8]) {
+  constexpr int L = fold_lanes_per_row<DK>();
 #pragma unroll
-  for (int m = 0; m < 8; ++m) {
-    const float4 u = p0[LPR * m], w = p1[LPR * m];
-    s0[2 * m] = make_float2(u.x, u.y);
-    s0[2 * m + 1] = make_float2(u.z, u.w);
-    s1[2 * m] = make_float2(w.x, w.y);
-    s1[2 * m + 1] = make_float2(w.z, w.w);
+  for (int i = 0; i < kFoldRowsPT; ++i) {
+    const float4* p = reinterpret_cast<const float4*>(block + (size_t)r[i] * DK) + q;
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+      const float4 u = p[L * m];
+      s[i][2 * m] = make_float2(u.x, u.y);
+      s[i][2 * m + 1] = make_float2(u.z, u.w);
+    }
   }
 }
 
-// The folded rows back to the FP32 checkpoint (rows g0 and g1 of S, g1 only
-// when has1) and, when Sr is set, to the BF16 read copy (round to nearest even).
+// The folded rows back to the FP32 checkpoint (row i is state row base + r[i],
+// stored when i < nr) and, when Sr is set, to the BF16 read copy (round to
+// nearest even).
 template <int DK>
-__device__ __forceinline__ void store_row_pair(float* S, bf16* Sr, size_t g0, size_t g1, bool has1,
-                                               int q, const float2 (&s0)[16],
-                                               const float2 (&s1)[16]) {
-  constexpr int LPR = DK / 32;
-  float4* row0 = reinterpret_cast<float4*>(S + g0 * DK) + q;
-  float4* row1 = reinterpret_cast<float4*>(S + g1 * DK) + q;
+__device__ __forceinline__ void store_rows(float* S, bf16* Sr, size_t base, const int (&r)[kFoldRowsPT],
+                                           int nr, int q, const float2 (&s)[kFoldRowsPT][8]) {
+  constexpr int L = fold_lanes_per_row<DK>();
 #pragma unroll
-  for (int m = 0; m < 8; ++m) {
-    row0[LPR * m] = make_float4(s0[2 * m].x, s0[2 * m].y, s0[2 * m + 1].x, s0[2 * m + 1].y);
-    if (has1) row1[LPR * m] = make_float4(s1[2 * m].x, s1[2 * m].y, s1[2 * m + 1].x, s1[2 * m + 1].y);
-  }
-  if (Sr) {
-    uint2* rr0 = reinterpret_cast<uint2*>(Sr + g0 * DK) + q;
-    uint2* rr1 = reinterpret_cast<uint2*>(Sr + g1 * DK) + q;
+  for (int i = 0; i < kFoldRowsPT; ++i) {
+    if (i >= nr) break;
+    const size_t g = base + r[i];
+    float4* row = reinterpret_cast<float4*>(S + g * DK) + q;
 #pragma unroll
-    for (int m = 0; m < 8; ++m) {
-      rr0[LPR * m] = make_uint2(pack_bf16x2(s0[2 * m].x, s0[2 * m].y), pack_bf16x2(s0[2 * m + 1].x, s0[2 * m + 1].y));
-      if (has1)
-        rr1[LPR * m] = make_uint2(pack_bf16x2(s1[2 * m].x, s1[2 * m].y), pack_bf16x2(s1[2 * m + 1].x, s1[2 * m + 1].y));
+    for (int m = 0; m < 4; ++m)
+      row[L * m] = make_float4(s[i][2 * m].x, s[i][2 * m].y, s[i][2 * m + 1].x, s[i][2 * m + 1].y);
+    if (Sr) {
+      uint2* rr = reinterpret_cast<uint2*>(Sr + g * DK) + q;
+#pragma unroll
+      for (int m = 0; m < 4; ++m)
+        rr[L * m] = make_uint2(pack_bf16x2(s[i][2 * m].x, s[i][2 * m].y),
+                               pack_bf16x2(s[i][2 * m + 1].x, s[i][2 * m + 1].y));
     }
   }
 }
@@ -761,15 +747,15 @@ __device__ __forceinline__ void store_row_pair(float* S, bf16* Sr, size_t g0, si
 // Consolidate for the delta-rule layers, synchronous form: one block per
 // folding head (a parallel pre-scan of the pointers lists them). The head's
 // n entries (k, v, gates, beta) are staged as float, then each thread folds
-// two rows x DK / 32 columns in registers (fold_row_pair). Rows are read
+// four rows x 16 columns in registers (fold_rows). Rows are read
 // once and written once (FP32 checkpoint and BF16 read copy). Used where the
 // prefetching form below does not fit two blocks per SM.
 template <int DK, typename TI, bool KDA>
 __global__ void __launch_bounds__(kDFoldThreads, 2) delta_fold_kernel(const DFold a) {
   extern __shared__ __align__(128) unsigned char smem[];
   __shared__ FoldList fl;
-  constexpr int LPR = DK / 32;                 // lanes per row
-  constexpr int SLOTS = kDFoldThreads / LPR;   // row slots per pass
+  constexpr int LPR = fold_lanes_per_row<DK>();  // lanes per row
+  constexpr int SLOTS = kDFoldThreads / LPR;      // row slots per pass
   const int tid = threadIdx.x, q = tid % LPR, rs = tid / LPR;
   const int H = a.H, DV = a.DV, W = a.W, Wd = ring_wd(W);
   float* kbuf = reinterpret_cast<float*>(smem);                   // [W][DK]
@@ -797,14 +783,19 @@ __global__ void __launch_bounds__(kDFoldThreads, 2) delta_fold_kernel(const DFol
       }
     }
     __syncthreads();
-    for (int r0 = rs; r0 < DV; r0 += 2 * SLOTS) {
-      const int r1 = r0 + SLOTS;
-      const bool has1 = r1 < DV;
-      const size_t g0 = (size_t)t * DV + r0, g1 = (size_t)t * DV + (has1 ? r1 : r0);
-      float2 s0[16], s1[16];
-      load_row_pair<DK>(a.S + g0 * DK, a.S + g1 * DK, has1, q, s0, s1);
-      fold_row_pair<DK, KDA>(s0, s1, has1, r0, r1, n, DV, q, kbuf, abuf, vbuf, bbuf, rbuf);
-      store_row_pair<DK>(a.S, a.Sr, g0, g1, has1, q, s0, s1);
+    for (int r0 = rs; r0 < DV; r0 += kFoldRowsPT * SLOTS) {
+      // rows r0 + i * SLOTS; DV is a multiple of 32, so nr is uniform over a warp
+      int r[kFoldRowsPT], nr = 0;
+#pragma unroll
+      for (int i = 0; i < kFoldRowsPT; ++i) {
+        const int ri = r0 + i * SLOTS;
+        nr += ri < DV;
+        r[i] = ri < DV ? ri : r0;
+      }
+      float2 sv[kFoldRowsPT][8];
+      load_rows<DK>(a.S + (size_t)t * DV * DK, r, q, sv);
+      fold_rows<DK, KDA>(sv, r, n, DV, q, kbuf, abuf, vbuf, bbuf, rbuf);
+      store_rows<DK>(a.S, a.Sr, (size_t)t * DV, r, nr, q, sv);
     }
     __syncthreads();
     if (tid == 0)
@@ -816,9 +807,9 @@ __global__ void __launch_bounds__(kDFoldThreads, 2) delta_fold_kernel(const DFol
 }
 
 // Rows of the prefetching fold: one row chunk of a head per unit, the rows
-// that one pass of the block's threads holds (two per row slot).
+// that one pass of the block's threads holds (kFoldRowsPT per row slot).
 __host__ __device__ constexpr int fold_chunk_rows(int DK, int DV) {
-  return DV < 2 * kDFoldThreads * 32 / DK ? DV : 2 * kDFoldThreads * 32 / DK;
+  return DV < kFoldRowsPT * kDFoldThreads * 16 / DK ? DV : kFoldRowsPT * kDFoldThreads * 16 / DK;
 }
 
 __host__ __device__ inline size_t smem_take(size_t& o, size_t bytes) {
@@ -892,8 +883,8 @@ template <int DK, typename TI, bool KDA>
 __global__ void __launch_bounds__(kDFoldThreads, 2) delta_fold_stream_kernel(const DFold a) {
   extern __shared__ __align__(128) unsigned char smem[];
   __shared__ FoldList fl;
-  constexpr int LPR = DK / 32;                 // lanes per row
-  constexpr int SLOTS = kDFoldThreads / LPR;   // row slots per pass
+  constexpr int LPR = fold_lanes_per_row<DK>();  // lanes per row
+  constexpr int SLOTS = kDFoldThreads / LPR;      // row slots per pass
   const int tid = threadIdx.x, q = tid % LPR, rs = tid / LPR;
   const int H = a.H, DV = a.DV, W = a.W, Wd = ring_wd(W);
   const int R = fold_chunk_rows(DK, DV), nch = (DV + R - 1) / R;
@@ -981,17 +972,25 @@ __global__ void __launch_bounds__(kDFoldThreads, 2) delta_fold_stream_kernel(con
         rbuf[j] = 1.f / al;
       }
     }
-    // rows is a multiple of 32, so both flags are uniform over each warp
-    const bool has0 = rs < rows, has1 = rs + SLOTS < rows;
-    float2 s0[16], s1[16];
-    if (has0) load_row_pair<DK>(sS + (size_t)rs * DK, sS + (size_t)(rs + SLOTS) * DK, has1, q, s0, s1);
+    // chunk rows rs + i * SLOTS; rows is a multiple of 32, so nr is uniform
+    // over each warp
+    int r[kFoldRowsPT], nr = 0;
+#pragma unroll
+    for (int i = 0; i < kFoldRowsPT; ++i) {
+      const int ri = rs + i * SLOTS;
+      nr += ri < rows;
+      r[i] = ri < rows ? ri : rs;
+    }
+    float2 sv[kFoldRowsPT][8];
+    if (nr > 0) load_rows<DK>(sS, r, q, sv);
     __syncthreads();  // entries widened; the staged chunk and raw entries are free
     if (u + 1 < units) issue(u + 1);
-    if (has0) {
-      const int r0 = c0 + rs, r1 = r0 + SLOTS;
-      const size_t g0 = (size_t)t * DV + r0, g1 = (size_t)t * DV + (has1 ? r1 : r0);
-      fold_row_pair<DK, KDA>(s0, s1, has1, r0, r1, n, DV, q, kbuf, abuf, vbuf, bbuf, rbuf);
-      store_row_pair<DK>(a.S, a.Sr, g0, g1, has1, q, s0, s1);
+    if (nr > 0) {
+      int rg[kFoldRowsPT];  // rows within the head
+#pragma unroll
+      for (int i = 0; i < kFoldRowsPT; ++i) rg[i] = c0 + r[i];
+      fold_rows<DK, KDA>(sv, rg, n, DV, q, kbuf, abuf, vbuf, bbuf, rbuf);
+      store_rows<DK>(a.S, a.Sr, (size_t)t * DV, rg, nr, q, sv);
     }
   }
   if (units > 0) {
