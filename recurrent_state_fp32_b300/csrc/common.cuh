@@ -234,6 +234,39 @@ __device__ __forceinline__ void load_vec(const T* p, float (&out)[E]) {
   }
 }
 
+// E consecutive elements of T kept as raw 32-bit words (a load that is not
+// yet converted holds half the registers for bf16): load_raw issues one
+// vector load of E * sizeof(T) bytes (4, 8 or 16), raw_to_f converts.
+template <typename T, int E>
+struct Raw {
+  static constexpr int kWords = (E * (int)sizeof(T) + 3) / 4;
+  uint32_t w[kWords];
+};
+template <typename T, int E>
+__device__ __forceinline__ void load_raw(const T* p, Raw<T, E>& r) {
+  constexpr int kW = Raw<T, E>::kWords;
+  static_assert(kW == 1 || kW == 2 || kW == 4, "4, 8 or 16 bytes");
+  if constexpr (kW == 4) {
+    const uint4 v = *reinterpret_cast<const uint4*>(p);
+    r.w[0] = v.x, r.w[1] = v.y, r.w[2] = v.z, r.w[3] = v.w;
+  } else if constexpr (kW == 2) {
+    const uint2 v = *reinterpret_cast<const uint2*>(p);
+    r.w[0] = v.x, r.w[1] = v.y;
+  } else {
+    r.w[0] = *reinterpret_cast<const uint32_t*>(p);
+  }
+}
+template <typename T, int E>
+__device__ __forceinline__ void raw_to_f(const Raw<T, E>& r, float (&f)[E]) {
+#pragma unroll
+  for (int e = 0; e < E; ++e) {
+    if constexpr (sizeof(T) == 2)
+      f[e] = (e & 1) ? bf16_hi(r.w[e / 2]) : bf16_lo(r.w[e / 2]);
+    else
+      f[e] = __uint_as_float(r.w[e]);
+  }
+}
+
 // Copies `bytes` (a multiple of 16, both addresses 16-byte aligned) with the
 // 32 lanes of one warp.
 __device__ __forceinline__ void block_copy_warp(void* dst, const void* src, int bytes, int lane) {
@@ -371,7 +404,8 @@ __device__ __forceinline__ void arrive_and_finish(int32_t* sync, int units, int 
 }
 
 // Tiles of one block (grid-stride over `tiles` tiles, H tiles per sequence)
-// whose sequence folds: len + k_next > W, or force and len > 0. Sequences
+// whose sequence folds: len + k_next > W, or force and len > 0 (with
+// `flags`: the sequences whose flag is set instead). Sequences
 // with out-of-range pointers get REPLAYSSM_SEQ_BAD_POINTER and are skipped. One parallel
 // load of the pointers per block, so a launch with nothing to fold is cheap.
 // The list order is arbitrary; every listed tile is independent.
@@ -390,7 +424,8 @@ __device__ __forceinline__ bool pointers_ok(int head, int len, int W) {
 
 __device__ __forceinline__ void collect_folds(FoldList& fl, long long tiles, int H,
                                               const int32_t* ring_len, const int32_t* ring_head,
-                                              int32_t* status, int W, int k_next, int force) {
+                                              int32_t* status, int W, int k_next, int force,
+                                              const int32_t* flags = nullptr) {
   if (threadIdx.x == 0) fl.count = 0;
   __syncthreads();
   for (int k = threadIdx.x; k < kMaxFoldTiles; k += blockDim.x) {
@@ -400,7 +435,7 @@ __device__ __forceinline__ void collect_folds(FoldList& fl, long long tiles, int
     const int len = ring_len[seq], head = ring_head[seq];
     if (!pointers_ok(head, len, W)) {
       if (t % H == 0) atomicOr(status + seq, REPLAYSSM_SEQ_BAD_POINTER);
-    } else if (len + k_next > W || (force && len > 0)) {
+    } else if (flags ? flags[seq] != 0 : (len + k_next > W || (force && len > 0))) {
       const int pos = atomicAdd(&fl.count, 1);
       fl.tile[pos] = (int)t;
       fl.len[pos] = len;

@@ -11,6 +11,7 @@
 //   w_j = dt_j prod_{i>j} dA_i = dt_j exp(A_h sum_{i>j} dt_i),
 //   fold: h_c <- (prod_i dA_i) h_c + sum_j w_j x_j B_j^T.
 #include <algorithm>
+#include <cstdlib>
 
 #include "common.cuh"
 #include "launch.h"
@@ -335,7 +336,7 @@ __global__ void __launch_bounds__(32 * kPrepWarps) mamba2_prep_kernel(const M2Pr
 // ------------------------------------------------- fused step: coefficients
 
 constexpr int kCoefWarps = 8;   // warps per coefficient block
-constexpr int kCoefHeads = 16;  // heads per warp
+constexpr int kCoefHeads = 8;   // heads per warp
 
 struct M2Coef {
   int batch, H, G, W;
@@ -365,21 +366,25 @@ struct M2Coef {
 // and for a fold, over its nf entries, the fold weights w_j and the fold
 // decay exp(A_h sum_j dt_j). The stream kernel computes the buffer terms
 // sum_j c_j x_j[p] + c_tok x[p] itself from the ring x rows, so this grid
-// reads no x at all and is short: its dependent stream kernel launches at
-// once and streams state rows while it runs.
+// reads no x at all and is short: its dependent stream kernel starts as it
+// ends (or earlier, on SMs it leaves).
 //
 // One warp per (sequence, chunk of kCoefHeads heads); half-warps take one
-// head each, lane j of a half holding entry j. C . B_j is computed once per
-// group the chunk touches. The token's dt goes into the ring here, and the
-// warp holding a group's first head copies the group's folded B rows out as
-// floats and then appends the token's B and C. The x row of the token is
-// appended by the stream kernel, row by row, after it has read the ring.
-// No slot this grid writes is one it, or any other warp of the grid, reads:
-// without a fold the token's slot is past the buffered entries, and with one
-// only the writing warp reads the old entries, first.
+// head each, lane j of a half holding entry j. The warp is latency-bound, so
+// it issues every load it needs (C, the B rows, and the dt rows, token dt, A
+// and D of all its heads) before it computes or stores anything. C . B_j is
+// computed once per group the chunk touches. The token's dt goes into the
+// ring here, and the warp holding a group's first head copies the group's
+// folded B rows out as floats and then appends the token's B and C. The x
+// row of the token is appended by the stream kernel, row by row, after it
+// has read the ring. No slot this grid writes is one it, or any other warp
+// of the grid, reads: without a fold the token's slot is past the buffered
+// entries, and with one only the writing warp reads the old entries, first.
 template <int N, typename TI>
-__global__ void __launch_bounds__(32 * kCoefWarps, 4) mamba2_step_coef_kernel(const M2Coef a) {
-  constexpr int E = N / 32;  // B and C elements per lane
+__global__ void __launch_bounds__(32 * kCoefWarps, 2) mamba2_step_coef_kernel(const M2Coef a) {
+  constexpr int E = N / 32;                   // B and C elements per lane
+  constexpr int kPasses = kCoefHeads / 2;     // heads per half-warp
+  constexpr int kMaxG = kCoefHeads;           // groups a chunk can touch
   griddep_launch_dependents();  // the stream kernel may start streaming state rows
   const int lane = threadIdx.x & 31;
   const int H = a.H, G = a.G, W = a.W, hpg = H / G, Wd = ring_wd(W);
@@ -406,58 +411,71 @@ __global__ void __launch_bounds__(32 * kCoefWarps, 4) mamba2_step_coef_kernel(co
   const TI* Bin = reinterpret_cast<const TI*>(a.B);
   const TI* Cin = reinterpret_cast<const TI*>(a.C);
   const TI* rB = reinterpret_cast<const TI*>(a.ring_B);
+  const int half = lane >> 4, j = lane & 15;
+  const int g0 = h0 / hpg, ng = (h1 - 1) / hpg - g0 + 1;  // groups of the chunk
 
-  // C . B_j of group g for the decode's entries 0..ld (entry ld: the token);
-  // lane l ends with entry l & 15 (ld < kStepMaxW = 16).
-  auto cb_of = [&](int g) -> float {
+  // ---- every load first: per pass (head h0 + 2 p + half) this lane's decode
+  // dt, fold dt, and the head's token dt, A and D
+  float dd[kPasses], fd[kPasses], dtt[kPasses], Av[kPasses], Dv[kPasses];
+#pragma unroll
+  for (int p = 0; p < kPasses; ++p) {
+    const int h = min(h0 + 2 * p + half, h1 - 1);
+    const size_t v = (size_t)seq * H + h;
+    const float* rdt = a.ring_dt + v * Wd;
+    dd[p] = j < ld ? rdt[slot_of(hdd + j)] : 0.f;
+    fd[p] = j < nf ? rdt[slot_of(hd + j)] : 0.f;
+    dtt[p] = a.dt[v];
+    Av[p] = a.A[h];
+    Dv[p] = a.D[h];
+  }
+  // C . B_j of each group of the chunk for the decode's entries 0..ld (entry
+  // ld: the token); lane l ends with entry l & 15 (ld < kStepMaxW = 16).
+  float cbv[kMaxG];
+#pragma unroll
+  for (int gl = 0; gl < kMaxG; ++gl) {
+    cbv[gl] = 0.f;
+    if (gl >= ng) continue;
+    const int g = g0 + gl;
     float cf[E];
     load_vec<TI, E>(Cin + ((size_t)seq * G + g) * N + lane * E, cf);
+    Raw<TI, E> bv[kStepMaxW];
+#pragma unroll
+    for (int q = 0; q < kStepMaxW; ++q) {
+      if (q <= ld) {
+        const TI* Bj = q < ld ? rB + (((size_t)seq * W + slot_of(hdd + q)) * G + g) * N
+                              : Bin + ((size_t)seq * G + g) * N;
+        load_raw<TI, E>(Bj + lane * E, bv[q]);
+      }
+    }
     float vv[kStepMaxW];
 #pragma unroll
     for (int q = 0; q < kStepMaxW; ++q) {
       float pp = 0.f;
       if (q <= ld) {
-        const TI* Bj = q < ld ? rB + (((size_t)seq * W + slot_of(hdd + q)) * G + g) * N
-                              : Bin + ((size_t)seq * G + g) * N;
-        float bv[E];
-        load_vec<TI, E>(Bj + lane * E, bv);
+        float bf[E];
+        raw_to_f<TI, E>(bv[q], bf);
 #pragma unroll
-        for (int e = 0; e < E; ++e) pp = fmaf(cf[e], bv[e], pp);
+        for (int e = 0; e < E; ++e) pp = fmaf(cf[e], bf[e], pp);
       }
       vv[q] = pp;
     }
     const float tot = reduce_scatter<kStepMaxW>(vv, lane);
-    return tot + __shfl_xor_sync(kFull, tot, 16);
-  };
+    cbv[gl] = tot + __shfl_xor_sync(kFull, tot, 16);
+  }
 
-  const int half = lane >> 4, j = lane & 15;
-  int cg = -1;      // group whose C . B_j the cache holds
-  float cv = 0.f;
-  for (int hA = h0; hA < h1; hA += 2) {
-    const int gA = hA / hpg, gB = min(hA + 1, h1 - 1) / hpg;
-    float cvA, cvB;
-    if (gA == cg) {
-      cvA = cv;
-    } else {
-      cvA = cb_of(gA);
-      cg = gA;
-      cv = cvA;
-    }
-    if (gB == gA) {
-      cvB = cvA;
-    } else {
-      cvB = cb_of(gB);
-      cg = gB;
-      cv = cvB;
-    }
-    const float cb = half ? cvB : cvA;
-    const int h = hA + half;
+  // ---- weights, one head per half-warp and pass
+#pragma unroll
+  for (int p = 0; p < kPasses; ++p) {
+    const int h = h0 + 2 * p + half;
+    if (h0 + 2 * p >= h1) break;  // warp-uniform
     const bool act = h < h1;
-    const size_t v = (size_t)seq * H + (act ? h : hA);
-    const float* rdt = a.ring_dt + v * Wd;
-    const float dtt = a.dt[v], Ah = a.A[act ? h : hA], Dh = a.D[act ? h : hA];
+    const size_t v = (size_t)seq * H + (act ? h : h1 - 1);
+    float cb = 0.f;
+#pragma unroll
+    for (int gl = 0; gl < kMaxG; ++gl)
+      if (gl == (act ? h : h1 - 1) / hpg - g0) cb = cbv[gl];
     // decode weights: inclusive suffix sums of dt over the half's 16 lanes
-    const float d = j < ld ? rdt[slot_of(hdd + j)] : (j == ld ? dtt : 0.f);
+    const float d = j == ld ? dtt[p] : dd[p];
     float sfx = d;
 #pragma unroll
     for (int o = 1; o < 16; o <<= 1) {
@@ -467,15 +485,15 @@ __global__ void __launch_bounds__(32 * kCoefWarps, 4) mamba2_step_coef_kernel(co
     const float total = __shfl_sync(kFull, sfx, 0, 16);
     // exponents lie in [A_h sum dt, 0]; the fast exponential's relative
     // error (about 1e-6 there) is far inside the output tolerance
-    const float c = d * __expf(Ah * (sfx - d)) * cb;
+    const float c = d * __expf(Av[p] * (sfx - d)) * cb;
     float* wr = a.work + v * kStepRow;
     if (act) {
       wr[j] = j < ld ? c : 0.f;
-      if (j == ld) wr[kStepTok] = c + Dh;
-      if (j == 0) wr[kStepDecay] = __expf(Ah * total);
+      if (j == ld) wr[kStepTok] = c + Dv[p];
+      if (j == 0) wr[kStepDecay] = __expf(Av[p] * total);
     }
     if (nf) {  // fold weights over the nf entries from the old head
-      const float f = j < nf ? rdt[slot_of(hd + j)] : 0.f;
+      const float f = fd[p];
       float fs = f;
 #pragma unroll
       for (int o = 1; o < 16; o <<= 1) {
@@ -484,26 +502,34 @@ __global__ void __launch_bounds__(32 * kCoefWarps, 4) mamba2_step_coef_kernel(co
       }
       const float ftot = __shfl_sync(kFull, fs, 0, 16);
       if (act) {
-        wr[kStepFoldW + j] = j < nf ? f * expf(Ah * (fs - f)) : 0.f;
-        if (j == 0) wr[kStepFoldDecay] = expf(Ah * ftot);
+        wr[kStepFoldW + j] = j < nf ? f * expf(Av[p] * (fs - f)) : 0.f;
+        if (j == 0) wr[kStepFoldDecay] = expf(Av[p] * ftot);
       }
     }
-    // the token's dt, after the half has read the row (the shuffles above
-    // consumed every load); with a fold its slot is entry 0's
-    __syncwarp();
-    if (act && j == 0) a.ring_dt[v * Wd + tslot] = dtt;
+    // the token's dt, after the half has read the row (every load of it was
+    // consumed above); with a fold its slot is entry 0's
+    if (act && j == 0) a.ring_dt[v * Wd + tslot] = dtt[p];
   }
 
-  // Groups whose first head is in this chunk: folded B rows, then the
-  // token's B and C.
-  for (int g = h0 / hpg; g * hpg < h1; ++g) {
+  // ---- groups whose first head is in this chunk: folded B rows (all loads
+  // first), then the token's B and C
+  for (int g = g0; g * hpg < h1; ++g) {
     if (g * hpg < h0) continue;
     const size_t gi = (size_t)seq * G + g;
     if (nf) {
-      float* Bs = a.bfold + gi * kStepMaxW * N;
-      for (int jj = 0; jj < nf; ++jj) {
-        const TI* Bo = rB + (((size_t)seq * W + slot_of(hd + jj)) * G + g) * N;
-        for (int cc = lane; cc < N; cc += 32) Bs[(size_t)jj * N + cc] = to_f(Bo[cc]);
+      Raw<TI, E> bq[kStepMaxW];
+#pragma unroll
+      for (int jj = 0; jj < kStepMaxW; ++jj)
+        if (jj < nf) load_raw<TI, E>(rB + (((size_t)seq * W + slot_of(hd + jj)) * G + g) * N + lane * E, bq[jj]);
+      float* Bs = a.bfold + gi * kStepMaxW * N + lane * E;
+#pragma unroll
+      for (int jj = 0; jj < kStepMaxW; ++jj) {
+        if (jj < nf) {
+          float bf[E];
+          raw_to_f<TI, E>(bq[jj], bf);
+#pragma unroll
+          for (int e = 0; e < E; ++e) Bs[(size_t)jj * N + e] = bf[e];
+        }
       }
       __syncwarp();
     }
@@ -1095,10 +1121,14 @@ cudaError_t launch_step_coef(const replayssm_dims& d, const M2Coef& p, cudaStrea
 template <int N, typename TS, typename TV>
 cudaError_t launch_step_stream(const StepArgs& a, size_t smem, int grid, int threads,
                                cudaStream_t st) {
-  auto kern = mamba2_step_stream_kernel<N, TS, TV>;
+  // The fold units' update on the tensor cores when REPLAYSSM_FOLD_TENSOR_CORES
+  // is set to 1 (a measured alternative, slower here: see the header).
+  const char* tc = std::getenv("REPLAYSSM_FOLD_TENSOR_CORES");
+  auto kern = tc && tc[0] == '1' ? mamba2_step_stream_kernel<N, TS, TV, true>
+                                 : mamba2_step_stream_kernel<N, TS, TV, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  // a programmatic dependent of the preparation kernel, as in the plain decode
+  // a programmatic dependent of the coefficient kernel
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(threads);

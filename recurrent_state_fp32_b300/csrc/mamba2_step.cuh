@@ -119,7 +119,29 @@ __device__ __forceinline__ int fold_row(int lane) {
   return lane / L + RPI * (CS * (lane & (M - 1)) + in_chunk);
 }
 
-template <int N, typename TS, typename TV>
+// x as hi + lo, each a TF32 value (round to nearest): hi carries the top 11
+// mantissa bits, lo most of the rest, so products of the pairs lose little
+// against FP32.
+__device__ __forceinline__ void tf32_split(float x, uint32_t& hi, uint32_t& lo) {
+  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(hi) : "f"(x));
+  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(lo) : "f"(x - __uint_as_float(hi)));
+}
+
+// d += a b for one 16 x 8 x 8 TF32 tile (warp-wide): a in the row-major A
+// fragment order, b in the column-major B order, d the accumulator fragment.
+__device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                         uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// MMA: the fold units' rank-n update on the tensor cores (mma.sync, TF32
+// split in two) instead of FP32 FMAs; both give the same results within
+// FP32 rounding.
+template <int N, typename TS, typename TV, bool MMA>
 __global__ void __launch_bounds__(kStreamMaxThreads, 1) mamba2_step_stream_kernel(const StepArgs a) {
   extern __shared__ __align__(128) unsigned char smem[];
   using RD = RowDot<N, TS>;     // decode units
@@ -345,13 +367,18 @@ __global__ void __launch_bounds__(kStreamMaxThreads, 1) mamba2_step_stream_kerne
         // B_j of the head's group, this lane's columns (zero past the n entries)
         const float* Bs = a.bfold + ((size_t)seq * a.G + g) * kStepMaxW * N + cf;
         float4 Bq[kStepMaxW];
-#pragma unroll
-        for (int j = 0; j < kStepMaxW; ++j)
-          Bq[j] = j < nf ? *reinterpret_cast<const float4*>(Bs + (size_t)j * N)
-                         : make_float4(0.f, 0.f, 0.f, 0.f);
         float c4[4];
-        load_vec<TV, 4>(Cin + ((size_t)seq * a.G + g) * N + cf, c4);
-        const int r = fold_row<RF::kLpr, RF::kRpi, kCS>(lane);
+        if constexpr (!MMA) {
+#pragma unroll
+          for (int j = 0; j < kStepMaxW; ++j)
+            Bq[j] = j < nf ? *reinterpret_cast<const float4*>(Bs + (size_t)j * N)
+                           : make_float4(0.f, 0.f, 0.f, 0.f);
+          load_vec<TV, 4>(Cin + ((size_t)seq * a.G + g) * N + cf, c4);
+        }
+        // the output row of this lane: one per lane, in the FMA loop's
+        // reduction order or the tensor-core tiles' row order
+        const int gq = lane >> 2, tq = lane & 3;
+        const int r = MMA ? 16 * (tq >> 1) + gq + 8 * (tq & 1) : fold_row<RF::kLpr, RF::kRpi, kCS>(lane);
         const TV xtr = xh[r];  // the token (decoded after the fold, n = 1)
         const float extra = ctok * to_f(xtr);
         // this warp's stage: the unit's first, or the second of a two-stage
@@ -391,8 +418,9 @@ __global__ void __launch_bounds__(kStreamMaxThreads, 1) mamba2_step_stream_kerne
         }
         // this warp's 32 FP32 rows
         const float* tile = reinterpret_cast<const float*>(smem + (size_t)s * L.stage) + (size_t)off * N;
-        // rows in chunks of kCS per lane; lane l ends with the total of row r
         float mine = 0.f;
+        if constexpr (!MMA) {
+        // rows in chunks of kCS per lane; lane l ends with the total of row r
 #pragma unroll 1
         for (int m = 0; m < kFoldChunks; ++m) {
           float dots[kCS];
@@ -427,6 +455,83 @@ __global__ void __launch_bounds__(kStreamMaxThreads, 1) mamba2_step_stream_kerne
           }
           const float d = reduce_chunk<RF::kLpr, kCS>(dots, lane);
           if ((lane & (kFoldChunks - 1)) == m) mine = d;
+        }
+        } else {
+        // S' = fold_decay S + c B^T on the tensor cores: mma.sync m16n8k8
+        // with TF32 operands split in two (x = hi + lo, three products
+        // hi.hi + hi.lo + lo.hi per step: about FP32 accuracy); rows
+        // 16 mt + (lane / 4) [+ 8], columns 8 nt + 2 (lane % 4) [+ 1] of each
+        // 16 x 8 tile. Then the new rows (as the read copy holds them)
+        // dotted with C.
+        uint32_t ah[2][2][4], alo[2][2][4];  // c fragments [row tile][entry step][4]
+#pragma unroll
+        for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+          for (int ks = 0; ks < 2; ++ks)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float v = coef[(size_t)(16 * mt + gq + 8 * (e & 1)) * kStepMaxW + 8 * ks + tq + 4 * (e >> 1)];
+              tf32_split(v, ah[mt][ks][e], alo[mt][ks][e]);
+            }
+        const float* Bg = a.bfold + ((size_t)seq * a.G + g) * kStepMaxW * N;
+        const TV* Cg = Cin + ((size_t)seq * a.G + g) * N;
+        float racc[2][2] = {};  // [row tile][row, row + 8]: partial dots with C
+#pragma unroll 4
+        for (int nt = 0; nt < N / 8; ++nt) {
+          const int c0 = 8 * nt;
+          uint32_t bh[2][2], blo[2][2];  // B fragments [entry step][2] (zero past nf)
+#pragma unroll
+          for (int ks = 0; ks < 2; ++ks)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const int j = 8 * ks + tq + 4 * e;
+              const float v = j < nf ? __ldg(Bg + (size_t)j * N + c0 + gq) : 0.f;
+              tf32_split(v, bh[ks][e], blo[ks][e]);
+            }
+          float2 cc;
+          if constexpr (sizeof(TV) == 2) {
+            const uint32_t w = __ldg(reinterpret_cast<const unsigned int*>(Cg + c0 + 2 * tq));
+            cc = make_float2(bf16_lo(w), bf16_hi(w));
+          } else {
+            cc = __ldg(reinterpret_cast<const float2*>(Cg + c0 + 2 * tq));
+          }
+#pragma unroll
+          for (int mt = 0; mt < 2; ++mt) {
+            const int ra = 16 * mt + gq;
+            const float2 s0 = *reinterpret_cast<const float2*>(tile + (size_t)ra * N + c0 + 2 * tq);
+            const float2 s1 = *reinterpret_cast<const float2*>(tile + (size_t)(ra + 8) * N + c0 + 2 * tq);
+            float d[4] = {fdec * s0.x, fdec * s0.y, fdec * s1.x, fdec * s1.y};
+#pragma unroll
+            for (int ks = 0; ks < 2; ++ks) {
+              mma_tf32(d, ah[mt][ks], bh[ks][0], bh[ks][1]);
+              mma_tf32(d, ah[mt][ks], blo[ks][0], blo[ks][1]);
+              mma_tf32(d, alo[mt][ks], bh[ks][0], bh[ks][1]);
+            }
+            const size_t g0 = ((size_t)hg * P + row0 + ra) * N + c0 + 2 * tq, g1 = g0 + (size_t)8 * N;
+            *reinterpret_cast<float2*>(a.S_ckpt + g0) = make_float2(d[0], d[1]);
+            *reinterpret_cast<float2*>(a.S_ckpt + g1) = make_float2(d[2], d[3]);
+            float2 r0v = make_float2(d[0], d[1]), r1v = make_float2(d[2], d[3]);
+            if constexpr (FS == 2) {
+              const uint32_t p0 = pack_bf16x2(d[0], d[1]), p1 = pack_bf16x2(d[2], d[3]);
+              *reinterpret_cast<uint32_t*>(a.S_read + g0) = p0;
+              *reinterpret_cast<uint32_t*>(a.S_read + g1) = p1;
+              r0v = make_float2(bf16_lo(p0), bf16_hi(p0));
+              r1v = make_float2(bf16_lo(p1), bf16_hi(p1));
+            }
+            racc[mt][0] = fmaf(r0v.x, cc.x, fmaf(r0v.y, cc.y, racc[mt][0]));
+            racc[mt][1] = fmaf(r1v.x, cc.x, fmaf(r1v.y, cc.y, racc[mt][1]));
+          }
+        }
+        // totals over the four lanes of a row group; lane (gq, tq) keeps row r
+#pragma unroll
+        for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+          for (int h2 = 0; h2 < 2; ++h2) {
+            racc[mt][h2] += __shfl_xor_sync(kFull, racc[mt][h2], 1);
+            racc[mt][h2] += __shfl_xor_sync(kFull, racc[mt][h2], 2);
+          }
+        mine = (tq & 2) ? ((tq & 1) ? racc[1][1] : racc[1][0])
+                        : ((tq & 1) ? racc[0][1] : racc[0][0]);
         }
         yrow[r] = fmaf(scale, mine, extra);
         rxh[(size_t)tslot * P + r] = xtr;  // append the token's x

@@ -69,6 +69,16 @@ def test_matches_oracle(case, read):
 
 
 @pytest.mark.parametrize("read", ["f32", "bf16"])
+@pytest.mark.parametrize("case", ["tiny", "groups_n64", "p128", "w1"])
+def test_tensor_core_fold_matches_oracle(case, read, monkeypatch):
+    """The same parity bar with the fold units' update on the tensor cores
+    (REPLAYSSM_FOLD_TENSOR_CORES=1: mma.sync with TF32 operands split in two)."""
+    monkeypatch.setenv("REPLAYSSM_FOLD_TENSOR_CORES", "1")
+    wl = synth.Mamba2Workload(**CASES[case])
+    assert run(Session("mamba2", wl, read), wl.steps, check_every=5) > 0
+
+
+@pytest.mark.parametrize("read", ["f32", "bf16"])
 @pytest.mark.parametrize("batch,heads", [(6, 4), (24, 32)])
 def test_staggered_phases(read, batch, heads):
     """Slots change hands, so each call mixes folding and plain sequences;
