@@ -198,11 +198,36 @@ REPLAYSSM_API replayssm_status replayssm_consolidate(
  * block (about 16 KB of rows, at most P) is not a multiple of 64 rows -- P
  * of 32 or 96, say -- the call runs the fold and the decode as two launches
  * with the same result. Sequences with out-of-range pointers get
- * REPLAYSSM_SEQ_BAD_POINTER and are untouched.
+ * REPLAYSSM_SEQ_BAD_POINTER and are untouched. With the environment variable
+ * REPLAYSSM_FOLD_TENSOR_CORES=1 the fold's rank-n update runs on the tensor
+ * cores (mma.sync, TF32 operands split in hi + lo, three products per step,
+ * about FP32 accuracy) instead of FP32 FMAs: a measured alternative, slower
+ * on B300 at these shapes, kept for that comparison.
  */
 REPLAYSSM_API replayssm_status replayssm_mamba2_fold_decode(
     const replayssm_dims* dims, const replayssm_state* state, const float* A, const float* D,
     const void* x, const void* B, const void* C, const float* dt, float* y, void* stream);
+
+/*
+ * One plain decode step of a Gated DeltaNet or KDA layer with the
+ * consolidation it needs, in one call: the result (outputs, S_ckpt, S_read,
+ * ring, pointers, status) is that of replayssm_consolidate(dims, state,
+ * NULL, 1, 0) followed by replayssm_gdn_decode with the same arguments, up
+ * to float rounding order. A sequence whose ring is full is folded and its
+ * token decoded from the new rows ("NVIDIA y Princeton aceleran modelos
+ * híbridos…", paragraph 2: the fold only when the buffer fills): S_ckpt is
+ * read once and written once, with S_read, and the output comes from the
+ * new rows as the read copy holds them, with no further read of the state.
+ * Every other sequence is decoded as by replayssm_gdn_decode. Arguments and
+ * layouts as for replayssm_gdn_decode; state->work must hold
+ * replayssm_workspace_bytes(dims, 1) bytes (it carries one flag per
+ * sequence between the two grids of the call) and state->sync must be zero
+ * (each call leaves it zero). Sequences with out-of-range pointers get
+ * REPLAYSSM_SEQ_BAD_POINTER and are untouched.
+ */
+REPLAYSSM_API replayssm_status replayssm_gdn_fold_decode(
+    const replayssm_dims* dims, const replayssm_state* state, const void* q, const void* k,
+    const void* v, const float* alpha, const float* beta, float scale, float* o, void* stream);
 
 /*
  * Speculative verify for the delta kinds ("ReplaySSM: o ganho aparece…",
@@ -383,7 +408,7 @@ REPLAYSSM_API replayssm_status replayssm_selftest_wait_timeout(int32_t* status, 
 
 /*
  * Size in bytes of state->work for decode calls (K = 1; for Mamba-2 this
- * includes replayssm_mamba2_fold_decode's per-head fold terms) and verify
+ * includes replayssm_mamba2_fold_decode's per-head weights) and verify
  * calls with up to K drafts on the given sizes (0 if dims is invalid).
  */
 REPLAYSSM_API int64_t replayssm_workspace_bytes(const replayssm_dims* dims, int32_t K);

@@ -47,6 +47,7 @@ SIGNATURES = {
     "replayssm_mamba2_decode_noalloc": [_DP, _SP, _P, _P, _P, _P, _P, _P, _P, _P],
     "replayssm_mamba2_decode_noalloc_bytes": [_DP],
     "replayssm_gdn_decode": [_DP, _SP, _P, _P, _P, _P, _P, _F, _P, _P],
+    "replayssm_gdn_fold_decode": [_DP, _SP, _P, _P, _P, _P, _P, _F, _P, _P],
     "replayssm_consolidate": [_DP, _SP, _P, _I, _I, _P],
     "replayssm_mamba2_fold_decode": [_DP, _SP, _P, _P, _P, _P, _P, _P, _P, _P],
     "replayssm_spec_verify": [_DP, _SP, _I, _P, _P, _P, _P, _P, _F, _P, _P],

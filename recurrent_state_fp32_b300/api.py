@@ -192,6 +192,14 @@ def gdn_decode(dims, state, q, k, v, alpha, beta, scale, o, stream=None):
           float(scale), _ptr(o), _stream(stream))
 
 
+def gdn_fold_decode(dims, state, q, k, v, alpha, beta, scale, o, stream=None):
+    """consolidate(k_next=1) + gdn_decode in one call: full rings are folded
+    and their token decoded from the new rows."""
+    d, s = _refs(dims, state)
+    _call("replayssm_gdn_fold_decode", d, s, _ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(beta),
+          float(scale), _ptr(o), _stream(stream))
+
+
 def consolidate(dims, state, A=None, k_next=1, force=False, stream=None):
     d, s = _refs(dims, state)
     _call("replayssm_consolidate", d, s, _ptr(A), int(k_next), int(bool(force)), _stream(stream))

@@ -353,6 +353,20 @@ REPLAYSSM_API replayssm_status replayssm_mamba2_fold_decode(
                                               static_cast<cudaStream_t>(stream)));
 }
 
+REPLAYSSM_API replayssm_status replayssm_gdn_fold_decode(
+    const replayssm_dims* dims, const replayssm_state* state, const void* q, const void* k,
+    const void* v, const float* alpha, const float* beta, float scale, float* o, void* stream) {
+  RS_TRY(check_dims(dims));
+  if (dims->kind == REPLAYSSM_MAMBA2) return REPLAYSSM_ERR_INVALID_ARG;
+  RS_TRY(check_state(dims, state));
+  RS_TRY(check_delta_token(q, k, v, alpha, beta));
+  RS_TRY(check_ptr(o));
+  if (dims->batch == 0) return REPLAYSSM_OK;
+  RS_TRY(check_smem(rs::delta_fused_smem(*dims, 1, state->S_read != nullptr)));
+  return finish(rs::launch_delta_fold_decode(*dims, *state, q, k, v, alpha, beta, scale, o,
+                                             static_cast<cudaStream_t>(stream)));
+}
+
 REPLAYSSM_API replayssm_status replayssm_spec_verify(
     const replayssm_dims* dims, const replayssm_state* state, int32_t K, const void* q,
     const void* k, const void* v, const float* alpha, const float* beta, float scale, float* o,

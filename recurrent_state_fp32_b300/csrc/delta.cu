@@ -52,6 +52,10 @@ struct DFused {
   int32_t* len;
   int32_t* status;
   int32_t* sync;
+  // fused fold + decode step only (else null): a sequence whose ring is full
+  // is not refused but left to the fold grid that follows, which decodes its
+  // token from the folded rows; flags[seq] = 1 marks it, 0 any other
+  int32_t* flags;
 };
 
 // One head stage of a prep warp (byte offsets): a header (len, head, ok),
@@ -149,6 +153,24 @@ __global__ void __launch_bounds__(32 * kFWarps, 1) delta_fused_kernel(const DFus
     fence_mbar_init();
     abort_flag = 0;
   }
+  // The sequences of this block's heads that are refused (pointers out of
+  // range, or no room for K entries: with a.flags, the full rings left to
+  // the fold grid): their state rows are not read. Read here, before any
+  // prep warp of this block runs, so before the last arrival of any of
+  // those sequences can move its pointers (it needs this block's heads).
+  // Ranges of more than kSkipSeqs sequences stream every head.
+  constexpr int kSkipSeqs = 1024;
+  __shared__ uint32_t skipmask[kSkipSeqs / 32];
+  const int seq_lo = hb0 / H, nseq = nh > 0 ? (hb1 - 1) / H - seq_lo + 1 : 0;
+  const bool use_skip = nseq <= kSkipSeqs;
+  for (int i = tid; i < kSkipSeqs / 32; i += blockDim.x) skipmask[i] = 0u;
+  __syncthreads();
+  if (use_skip) {
+    for (int i = tid; i < nseq; i += blockDim.x) {
+      const int l = a.len[seq_lo + i], hd = a.head[seq_lo + i];
+      if (!pointers_ok(hd, l, W) || l + K > W) atomicOr(&skipmask[i / 32], 1u << (i % 32));
+    }
+  }
   __syncthreads();
 
   if (warp == CW) {
@@ -159,6 +181,7 @@ __global__ void __launch_bounds__(32 * kFWarps, 1) delta_fused_kernel(const DFus
     uint32_t pk = 0;
     bool pwrap = false;
     int li = 0, rb = 0;
+    bool skip = false;  // the current head's sequence is refused or left to the fold
     for (int ul = 0; ul < nu; ++ul) {
       const int s = ps;
       if (pwrap && !mbar_wait_warp(&empty[s], pk)) {
@@ -170,10 +193,20 @@ __global__ void __launch_bounds__(32 * kFWarps, 1) delta_fused_kernel(const DFus
         if (pwrap) pk ^= 1;
         pwrap = true;
       }
+      if (rb == 0) {
+        // a refused head's stages complete without data: its rows are not
+        // needed and not read from memory
+        const int i = (hb0 + li) / H - seq_lo;
+        skip = use_skip && ((skipmask[i / 32] >> (i % 32)) & 1u) != 0;
+      }
       if (lane == 0) {
-        mbar_arrive_expect_tx(&full[s], tile_bytes);
-        bulk_g2s(smem + (size_t)s * L.stage,
-                 Sg + ((size_t)(hb0 + li) * DV + (size_t)rb * RB) * DK, tile_bytes, &full[s], pol);
+        if (skip) {
+          mbar_arrive(&full[s]);
+        } else {
+          mbar_arrive_expect_tx(&full[s], tile_bytes);
+          bulk_g2s(smem + (size_t)s * L.stage,
+                   Sg + ((size_t)(hb0 + li) * DV + (size_t)rb * RB) * DK, tile_bytes, &full[s], pol);
+        }
       }
       if (++rb == nrb) {
         rb = 0;
@@ -244,6 +277,7 @@ __global__ void __launch_bounds__(32 * kFWarps, 1) delta_fused_kernel(const DFus
         constexpr int KC = KMAX < 64 / RD::kLpr ? KMAX : 64 / RD::kLpr;
 #pragma unroll 1
         for (int q = 0; q < ngr; ++q) {
+          if (!write) break;  // (a refused head's stage holds no rows)
           const int r = 32 * q + RD::row_of(lane);
 #pragma unroll 1
           for (int k0 = 0; k0 < KMAX; k0 += KC) {
@@ -282,9 +316,9 @@ __global__ void __launch_bounds__(32 * kFWarps, 1) delta_fused_kernel(const DFus
       } else {
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-          if (q >= ngr) break;
+          if (q >= ngr || !write) break;  // (a refused head's stage holds no rows)
           const float d = RD::rows32(tile, 32 * q, vec[0], lane);
-          if (write) yrow[32 * q + RD::row_of(lane)] = d + extra[q];
+          yrow[32 * q + RD::row_of(lane)] = d + extra[q];
         }
         __syncwarp();
         if (lane == 0) {
@@ -441,9 +475,13 @@ __global__ void __launch_bounds__(32 * kFWarps, 1) delta_fused_kernel(const DFus
         ok = hdr[2] != 0;
         cur_seq = seq;
         seq_count = 0;
-        if (h == 0 && lane == 0 && !ok)
-          atomicOr(a.status + seq, pointers_ok(hd, len, W) ? REPLAYSSM_SEQ_RING_FULL
-                                                           : REPLAYSSM_SEQ_BAD_POINTER);
+        if (h == 0 && lane == 0) {
+          const bool deferred = a.flags && !ok && pointers_ok(hd, len, W);  // folds first
+          if (a.flags) a.flags[seq] = deferred ? 1 : 0;
+          if (!ok && !deferred)
+            atomicOr(a.status + seq, pointers_ok(hd, len, W) ? REPLAYSSM_SEQ_RING_FULL
+                                                             : REPLAYSSM_SEQ_BAD_POINTER);
+        }
       }
       ++seq_count;
       // the slot must have been released by the consumers of head li - NSL
@@ -592,6 +630,23 @@ struct DFold {
   int32_t* len;
   int32_t* status;
   int32_t* sync;
+  // Fused fold + decode step (flags non-null): fold the sequences the decode
+  // grid before this one flagged (full rings), then decode their token from
+  // the new rows -- o = S' u + ce v with u = A_t (scale q), ce = scale
+  // beta (k . q) -- append it (slot head + n) and set len = 1.
+  const int32_t* flags;
+  const void* q;       // token inputs [b, H, ...]
+  const void* k;
+  const void* v;
+  const float* alpha;  // [b, H] or [b, H, d_k]
+  const float* beta;   // [b, H]
+  float scale;
+  float* o;            // [b, H, d_v]
+  void* ring_q;        // optional
+  void* ring_kw;       // the same rings, writable
+  void* ring_vw;
+  float* ring_alphaw;
+  float* ring_betaw;
 };
 
 // Rows of `cols` elements (in_dtype) of ring entries 0..n-1 of one head --
@@ -744,6 +799,96 @@ __device__ __forceinline__ void store_rows(float* S, bf16* Sr, size_t base, cons
   }
 }
 
+// The token of a fused step as the fold's output needs it, from one warp:
+// u = A_t (scale q_t) into ubuf[DK], ce = scale beta_t (k_t . q_t) into *ce
+// and v_t into vt[DV] (floats), from the token's q, k, v rows, its gate
+// (a scalar, or a row for KDA) and beta. A_t x = alpha (.) (x - beta (k . x) k).
+template <int DK, typename TI, bool KDA>
+__device__ __forceinline__ void token_terms(const TI* q, const TI* k, const TI* v,
+                                            const float* alpha, float bt, float scale, int DV,
+                                            float* ubuf, float* vt, float* ce, int lane) {
+  constexpr int E = DK / 32;
+  float qf[E], kf[E];
+  load_vec<TI, E>(q + lane * E, qf);
+  load_vec<TI, E>(k + lane * E, kf);
+  float kq = 0.f;
+#pragma unroll
+  for (int e = 0; e < E; ++e) kq = fmaf(kf[e], qf[e], kq);
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) kq += __shfl_xor_sync(kFull, kq, o);
+  kq *= scale;
+#pragma unroll
+  for (int e = 0; e < E; ++e) {
+    const float al = KDA ? alpha[lane * E + e] : alpha[0];
+    ubuf[lane * E + e] = al * (scale * qf[e] - bt * kq * kf[e]);
+  }
+  for (int r = lane; r < DV; r += 32) vt[r] = to_f(v[r]);
+  if (lane == 0) *ce = bt * kq;
+}
+
+// The fold's rows times u: o[obase + r[i]] = S'_read[r[i]] . u + ce vt[r[i]]
+// (i < nr), S'_read the rows as the read copy holds them (BF16-rounded when
+// round16), reduced over the L lanes of a row.
+template <int DK>
+__device__ __forceinline__ void out_rows(float* o, size_t obase, const int (&r)[kFoldRowsPT], int nr,
+                                         int q, const float2 (&s)[kFoldRowsPT][8], bool round16,
+                                         const float* ubuf, const float* vt, float ce) {
+  constexpr int L = fold_lanes_per_row<DK>();
+  const float4* u4 = reinterpret_cast<const float4*>(ubuf) + q;
+  float acc[kFoldRowsPT];
+#pragma unroll
+  for (int i = 0; i < kFoldRowsPT; ++i) {
+    float sacc = 0.f;
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+      const float4 u = u4[L * m];
+      float x0 = s[i][2 * m].x, x1 = s[i][2 * m].y, x2 = s[i][2 * m + 1].x, x3 = s[i][2 * m + 1].y;
+      if (round16) {
+        const uint32_t p0 = pack_bf16x2(x0, x1), p1 = pack_bf16x2(x2, x3);
+        x0 = bf16_lo(p0), x1 = bf16_hi(p0), x2 = bf16_lo(p1), x3 = bf16_hi(p1);
+      }
+      sacc = fmaf(x0, u.x, fmaf(x1, u.y, fmaf(x2, u.z, fmaf(x3, u.w, sacc))));
+    }
+    acc[i] = sacc;
+  }
+#pragma unroll
+  for (int sh = 1; sh < L; sh <<= 1) {
+#pragma unroll
+    for (int i = 0; i < kFoldRowsPT; ++i) acc[i] += __shfl_xor_sync(kFull, acc[i], sh);
+  }
+  if (q == 0) {
+#pragma unroll
+    for (int i = 0; i < kFoldRowsPT; ++i)
+      if (i < nr) o[obase + r[i]] = fmaf(ce, vt[r[i]], acc[i]);
+  }
+}
+
+// The token of a fused step into ring slot `slot` of head t (block threads):
+// q (when stored), k, v, the gate and beta.
+template <int DK, typename TI, bool KDA>
+__device__ __forceinline__ void append_token(const DFold& a, size_t t, int slot, int W, int DV) {
+  const int Wd = ring_wd(W);
+  constexpr int kv = 16 / (int)sizeof(TI);  // elements per 16-byte copy
+  const size_t kr = (t * W + slot) * DK, vr = (t * W + slot) * (size_t)DV;
+  for (int c = threadIdx.x; c < DK / kv; c += blockDim.x) {
+    reinterpret_cast<uint4*>(reinterpret_cast<TI*>(a.ring_kw) + kr)[c] =
+        reinterpret_cast<const uint4*>(reinterpret_cast<const TI*>(a.k) + t * DK)[c];
+    if (a.ring_q)
+      reinterpret_cast<uint4*>(reinterpret_cast<TI*>(a.ring_q) + kr)[c] =
+          reinterpret_cast<const uint4*>(reinterpret_cast<const TI*>(a.q) + t * DK)[c];
+  }
+  for (int c = threadIdx.x; c < DV / kv; c += blockDim.x)
+    reinterpret_cast<uint4*>(reinterpret_cast<TI*>(a.ring_vw) + vr)[c] =
+        reinterpret_cast<const uint4*>(reinterpret_cast<const TI*>(a.v) + t * DV)[c];
+  if (KDA) {
+    for (int c = threadIdx.x; c < DK; c += blockDim.x)
+      a.ring_alphaw[(t * W + slot) * DK + c] = a.alpha[t * DK + c];
+  } else if (threadIdx.x == 0) {
+    a.ring_alphaw[t * Wd + slot] = a.alpha[t];
+  }
+  if (threadIdx.x == 0) a.ring_betaw[t * Wd + slot] = a.beta[t];
+}
+
 // Consolidate for the delta-rule layers, synchronous form: one block per
 // folding head (a parallel pre-scan of the pointers lists them). The head's
 // n entries (k, v, gates, beta) are staged as float, then each thread folds
@@ -763,10 +908,14 @@ __global__ void __launch_bounds__(kDFoldThreads, 2) delta_fold_kernel(const DFol
   float* vbuf = abuf + align_up((size_t)W * (KDA ? DK : 1), 4);   // [W][DV]
   float* bbuf = vbuf + (size_t)W * DV;                            // [W]
   float* rbuf = bbuf + W;                                         // GDN [W]: 1 / alpha_j
+  float* ubuf = kbuf + align_up((size_t)(rbuf - kbuf) + W, 4);    // fused step: u [DK],
+  float* vt = ubuf + DK;                                          // v_t [DV], ce
+  float* cep = vt + DV;
   const TI* rk = reinterpret_cast<const TI*>(a.ring_k);
   const TI* rv = reinterpret_cast<const TI*>(a.ring_v);
 
-  collect_folds(fl, (long long)a.batch * H, H, a.len, a.head, a.status, W, a.k_next, a.force);
+  collect_folds(fl, (long long)a.batch * H, H, a.len, a.head, a.status, W, a.k_next, a.force,
+                a.flags);
   for (int f = 0; f < fl.count; ++f) {
     const int t = fl.tile[f], n = fl.len[f], hd = fl.head[f];
     const int seq = t / H;
@@ -782,6 +931,12 @@ __global__ void __launch_bounds__(kDFoldThreads, 2) delta_fold_kernel(const DFol
         rbuf[j] = 1.f / al;
       }
     }
+    if (a.flags && tid < 32)
+      token_terms<DK, TI, KDA>(reinterpret_cast<const TI*>(a.q) + (size_t)t * DK,
+                               reinterpret_cast<const TI*>(a.k) + (size_t)t * DK,
+                               reinterpret_cast<const TI*>(a.v) + (size_t)t * DV,
+                               a.alpha + (KDA ? (size_t)t * DK : (size_t)t), a.beta[t], a.scale,
+                               DV, ubuf, vt, cep, tid);
     __syncthreads();
     for (int r0 = rs; r0 < DV; r0 += kFoldRowsPT * SLOTS) {
       // rows r0 + i * SLOTS; DV is a multiple of 32, so nr is uniform over a warp
@@ -796,12 +951,15 @@ __global__ void __launch_bounds__(kDFoldThreads, 2) delta_fold_kernel(const DFol
       load_rows<DK>(a.S + (size_t)t * DV * DK, r, q, sv);
       fold_rows<DK, KDA>(sv, r, n, DV, q, kbuf, abuf, vbuf, bbuf, rbuf);
       store_rows<DK>(a.S, a.Sr, (size_t)t * DV, r, nr, q, sv);
+      if (a.flags) out_rows<DK>(a.o, (size_t)t * DV, r, nr, q, sv, a.Sr != nullptr, ubuf, vt, *cep);
     }
+    // fused step: the token into entry 0's old slot, now that every entry is read
+    if (a.flags) append_token<DK, TI, KDA>(a, (size_t)t, (hd + n) % W, W, DV);
     __syncthreads();
     if (tid == 0)
       arrive_and_finish(a.sync + seq, 1, H, [&] {
         a.head[seq] = (hd + n) % W;
-        a.len[seq] = 0;
+        a.len[seq] = a.flags ? 1 : 0;
       });
   }
 }
@@ -823,7 +981,8 @@ __host__ __device__ inline size_t smem_take(size_t& o, size_t bytes) {
 // entry order; the scalar fields' whole [Wd] blocks in slot order); the
 // current unit's entries widened to float; one mbarrier.
 struct DFoldSmem {
-  size_t s, kraw, vraw, araw, braw, kbuf, abuf, vbuf, bbuf, rbuf, bar, total;
+  size_t s, kraw, vraw, araw, braw, kbuf, abuf, vbuf, bbuf, rbuf, ubuf, vt, ce, tq, tk, tv, ta, tb,
+      bar, total;
   __host__ __device__ DFoldSmem(int DK, int DV, int W, int ti, bool kda) {
     const size_t R = fold_chunk_rows(DK, DV), Wd = ring_wd(W);
     size_t o = 0;
@@ -837,6 +996,14 @@ struct DFoldSmem {
     vbuf = smem_take(o, (size_t)W * DV * 4);
     bbuf = smem_take(o, (size_t)W * 4);
     rbuf = smem_take(o, (size_t)W * 4);
+    ubuf = smem_take(o, (size_t)DK * 4);  // fused step: u, v_t and ce of the token,
+    vt = smem_take(o, (size_t)DV * 4);    // and the next unit's token as it arrives
+    ce = smem_take(o, 16);
+    tq = smem_take(o, (size_t)DK * ti);
+    tk = smem_take(o, (size_t)DK * ti);
+    tv = smem_take(o, (size_t)DV * ti);
+    ta = smem_take(o, kda ? (size_t)DK * 4 : 16);
+    tb = smem_take(o, 16);
     bar = smem_take(o, 8);
     total = o;
   }
@@ -899,17 +1066,27 @@ __global__ void __launch_bounds__(kDFoldThreads, 2) delta_fold_stream_kernel(con
   float* vbuf = reinterpret_cast<float*>(smem + L.vbuf);
   float* bbuf = reinterpret_cast<float*>(smem + L.bbuf);
   float* rbuf = reinterpret_cast<float*>(smem + L.rbuf);
+  float* ubuf = reinterpret_cast<float*>(smem + L.ubuf);
+  float* vt = reinterpret_cast<float*>(smem + L.vt);
+  float* cep = reinterpret_cast<float*>(smem + L.ce);
+  TI* tq = reinterpret_cast<TI*>(smem + L.tq);  // the fused step's token (raw)
+  TI* tk = reinterpret_cast<TI*>(smem + L.tk);
+  TI* tv = reinterpret_cast<TI*>(smem + L.tv);
+  float* ta = reinterpret_cast<float*>(smem + L.ta);
+  float* tb = reinterpret_cast<float*>(smem + L.tb);
   uint64_t* bar = reinterpret_cast<uint64_t*>(smem + L.bar);
   const TI* rk = reinterpret_cast<const TI*>(a.ring_k);
   const TI* rv = reinterpret_cast<const TI*>(a.ring_v);
   const uint64_t pol = l2_evict_first_policy();
+  constexpr int kTV = 16 / (int)sizeof(TI);  // elements per 16-byte copy
 
   if (tid == 0) {
     mbar_init(bar, 1);
     fence_mbar_init();
   }
   // (its barriers also publish the mbarrier's initialisation)
-  collect_folds(fl, (long long)a.batch * H, H, a.len, a.head, a.status, W, a.k_next, a.force);
+  collect_folds(fl, (long long)a.batch * H, H, a.len, a.head, a.status, W, a.k_next, a.force,
+                a.flags);
   const int units = fl.count * nch;
 
   auto issue = [&](int u) {
@@ -928,6 +1105,23 @@ __global__ void __launch_bounds__(kDFoldThreads, 2) delta_fold_stream_kernel(con
       cp_async16(braw + 4 * i, a.ring_beta + (size_t)t * Wd + 4 * i);
       if (!KDA) cp_async16(araw + 4 * i, a.ring_alpha + (size_t)t * Wd + 4 * i);
     }
+    if (a.flags) {  // the fused step's token of head t
+      const TI* qg = reinterpret_cast<const TI*>(a.q) + (size_t)t * DK;
+      const TI* kg = reinterpret_cast<const TI*>(a.k) + (size_t)t * DK;
+      const TI* vg = reinterpret_cast<const TI*>(a.v) + (size_t)t * DV;
+      for (int i = tid; i < DK / kTV; i += kDFoldThreads) {
+        cp_async16(tq + i * kTV, qg + i * kTV);
+        cp_async16(tk + i * kTV, kg + i * kTV);
+      }
+      for (int i = tid; i < DV / kTV; i += kDFoldThreads) cp_async16(tv + i * kTV, vg + i * kTV);
+      if (KDA) {
+        for (int i = tid; i < DK / 4; i += kDFoldThreads)
+          cp_async16(ta + 4 * i, a.alpha + (size_t)t * DK + 4 * i);
+      } else if (tid == 0) {
+        cp_async4(ta, a.alpha + t);
+      }
+      if (tid == 0) cp_async4(tb, a.beta + t);
+    }
     cp_async_commit();
   };
   // the last arrival of a sequence's units moves its pointers
@@ -936,7 +1130,7 @@ __global__ void __launch_bounds__(kDFoldThreads, 2) delta_fold_stream_kernel(con
     const int seq = fl.tile[f] / H, hd = fl.head[f], n = fl.len[f];
     arrive_and_finish(a.sync + seq, 1, H * nch, [&] {
       a.head[seq] = (hd + n) % W;
-      a.len[seq] = 0;
+      a.len[seq] = a.flags ? 1 : 0;
     });
   };
 
@@ -983,6 +1177,29 @@ __global__ void __launch_bounds__(kDFoldThreads, 2) delta_fold_stream_kernel(con
     }
     float2 sv[kFoldRowsPT][8];
     if (nr > 0) load_rows<DK>(sS, r, q, sv);
+    if (a.flags) {
+      if (tid < 32)
+        token_terms<DK, TI, KDA>(tq, tk, tv, ta, tb[0], a.scale, DV, ubuf, vt, cep, tid);
+      // after the head's last chunk has landed (every entry of the head
+      // staged) the token goes into entry 0's old slot
+      if (c0 + rows == DV) {
+        const int slot = (hd + n) % W;
+        const size_t kr = ((size_t)t * W + slot) * DK, vr = ((size_t)t * W + slot) * DV;
+        for (int i = tid; i < DK / kTV; i += kDFoldThreads) {
+          reinterpret_cast<uint4*>(reinterpret_cast<TI*>(a.ring_kw) + kr)[i] = reinterpret_cast<const uint4*>(tk)[i];
+          if (a.ring_q)
+            reinterpret_cast<uint4*>(reinterpret_cast<TI*>(a.ring_q) + kr)[i] = reinterpret_cast<const uint4*>(tq)[i];
+        }
+        for (int i = tid; i < DV / kTV; i += kDFoldThreads)
+          reinterpret_cast<uint4*>(reinterpret_cast<TI*>(a.ring_vw) + vr)[i] = reinterpret_cast<const uint4*>(tv)[i];
+        if (KDA) {
+          for (int i = tid; i < DK; i += kDFoldThreads) a.ring_alphaw[((size_t)t * W + slot) * DK + i] = ta[i];
+        } else if (tid == 0) {
+          a.ring_alphaw[(size_t)t * Wd + slot] = ta[0];
+        }
+        if (tid == 0) a.ring_betaw[(size_t)t * Wd + slot] = tb[0];
+      }
+    }
     __syncthreads();  // entries widened; the staged chunk and raw entries are free
     if (u + 1 < units) issue(u + 1);
     if (nr > 0) {
@@ -991,6 +1208,7 @@ __global__ void __launch_bounds__(kDFoldThreads, 2) delta_fold_stream_kernel(con
       for (int i = 0; i < kFoldRowsPT; ++i) rg[i] = c0 + r[i];
       fold_rows<DK, KDA>(sv, rg, n, DV, q, kbuf, abuf, vbuf, bbuf, rbuf);
       store_rows<DK>(a.S, a.Sr, (size_t)t * DV, rg, nr, q, sv);
+      if (a.flags) out_rows<DK>(a.o, (size_t)t * DV, rg, nr, q, sv, a.Sr != nullptr, ubuf, vt, *cep);
     }
   }
   if (units > 0) {
@@ -1294,12 +1512,13 @@ cudaError_t launch_fused_k(const DFused& a, cudaStream_t st) {
 
 cudaError_t launch_delta(const replayssm_dims& d, const replayssm_state& s, int K, int commit,
                          const void* q, const void* k, const void* v, const float* alpha,
-                         const float* beta, float scale, float* o, cudaStream_t st) {
+                         const float* beta, float scale, float* o, cudaStream_t st,
+                         int32_t* flags = nullptr) {
   DFused a{d.batch, d.heads, d.dv, d.window, K, commit, 0, 0, 0, 0, 0, 0, 0,
            s.S_read ? (const void*)s.S_read : (const void*)s.S_ckpt,
            q, k, v, alpha, beta, scale, o,
            s.ring_q, s.ring_k, s.ring_v, s.ring_alpha, s.ring_beta,
-           s.ring_head, s.ring_len, s.status, s.sync};
+           s.ring_head, s.ring_len, s.status, s.sync, flags};
   const bool rd16 = s.S_read != nullptr, in16 = d.in_dtype == REPLAYSSM_BF16;
   const bool kda = d.kind == REPLAYSSM_KDA;
 #define RS_FUSED(DK_, TS_)                                                                     \
@@ -1338,11 +1557,30 @@ cudaError_t launch_delta_verify(const replayssm_dims& d, const replayssm_state& 
   return launch_delta(d, s, K, 0, q, k, v, alpha, beta, scale, o, st);
 }
 
-cudaError_t launch_delta_fold(const replayssm_dims& d, const replayssm_state& s, int k_next,
-                              int force, cudaStream_t st) {
-  DFold a{d.batch, d.heads, d.dv, d.window, k_next, force, s.S_ckpt,
-          reinterpret_cast<bf16*>(s.S_read), s.ring_k, s.ring_v, s.ring_alpha, s.ring_beta,
-          s.ring_head, s.ring_len, s.status, s.sync};
+namespace {
+
+// The consolidate grid; with `step` (its token and flag fields set) the
+// fused step's fold + decode of the flagged sequences.
+cudaError_t launch_delta_fold_grid(const replayssm_dims& d, const replayssm_state& s, int k_next,
+                                   int force, const DFold* step, cudaStream_t st) {
+  DFold a{};
+  if (step) a = *step;
+  a.batch = d.batch;
+  a.H = d.heads;
+  a.DV = d.dv;
+  a.W = d.window;
+  a.k_next = k_next;
+  a.force = force;
+  a.S = s.S_ckpt;
+  a.Sr = reinterpret_cast<bf16*>(s.S_read);
+  a.ring_k = s.ring_k;
+  a.ring_v = s.ring_v;
+  a.ring_alpha = s.ring_alpha;
+  a.ring_beta = s.ring_beta;
+  a.head = s.ring_head;
+  a.len = s.ring_len;
+  a.status = s.status;
+  a.sync = s.sync;
   const bool kda = d.kind == REPLAYSSM_KDA;
   const bool in16 = d.in_dtype == REPLAYSSM_BF16;
   const DeviceInfo& dev = device_info();
@@ -1364,8 +1602,9 @@ cudaError_t launch_delta_fold(const replayssm_dims& d, const replayssm_state& s,
       kern = in16 ? (kda ? delta_fold_stream_kernel<64, bf16, true> : delta_fold_stream_kernel<64, bf16, false>)
                   : (kda ? delta_fold_stream_kernel<64, float, true> : delta_fold_stream_kernel<64, float, false>);
   } else {
-    smem = 4 * ((size_t)d.window * d.dk + align_up((size_t)d.window * (kda ? d.dk : 1), 4) +
-                (size_t)d.window * d.dv + 2 * (size_t)d.window);
+    smem = 4 * (align_up((size_t)d.window * d.dk + align_up((size_t)d.window * (kda ? d.dk : 1), 4) +
+                             (size_t)d.window * d.dv + 2 * (size_t)d.window, 4) +
+                d.dk + d.dv + 4);
     if (d.dk == 128)
       kern = in16 ? (kda ? delta_fold_kernel<128, bf16, true> : delta_fold_kernel<128, bf16, false>)
                   : (kda ? delta_fold_kernel<128, float, true> : delta_fold_kernel<128, float, false>);
@@ -1377,6 +1616,41 @@ cudaError_t launch_delta_fold(const replayssm_dims& d, const replayssm_state& s,
   if (e != cudaSuccess) return e;
   kern<<<grid, kDFoldThreads, smem, st>>>(a);
   return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_delta_fold(const replayssm_dims& d, const replayssm_state& s, int k_next,
+                              int force, cudaStream_t st) {
+  return launch_delta_fold_grid(d, s, k_next, force, nullptr, st);
+}
+
+cudaError_t launch_delta_fold_decode(const replayssm_dims& d, const replayssm_state& s,
+                                     const void* q, const void* k, const void* v,
+                                     const float* alpha, const float* beta, float scale, float* o,
+                                     cudaStream_t st) {
+  // The decode grid decodes every sequence with room and flags the full
+  // rings (state.work holds the flags: the delta kinds use no other
+  // workspace); the fold grid then folds exactly those and decodes their
+  // token from the new rows.
+  int32_t* flags = reinterpret_cast<int32_t*>(s.work);
+  cudaError_t e = launch_delta(d, s, 1, 1, q, k, v, alpha, beta, scale, o, st, flags);
+  if (e != cudaSuccess) return e;
+  DFold step{};
+  step.flags = flags;
+  step.q = q;
+  step.k = k;
+  step.v = v;
+  step.alpha = alpha;
+  step.beta = beta;
+  step.scale = scale;
+  step.o = o;
+  step.ring_q = s.ring_q;
+  step.ring_kw = s.ring_k;
+  step.ring_vw = s.ring_v;
+  step.ring_alphaw = s.ring_alpha;
+  step.ring_betaw = s.ring_beta;
+  return launch_delta_fold_grid(d, s, 1, 0, &step, st);
 }
 
 cudaError_t launch_delta_conventional_verify(const replayssm_dims& d, const float* S, int K,

@@ -87,6 +87,12 @@ cudaError_t launch_delta_verify(const replayssm_dims& d, const replayssm_state& 
 size_t delta_fused_smem(const replayssm_dims& d, int K, bool read16);
 cudaError_t launch_delta_fold(const replayssm_dims& d, const replayssm_state& s, int k_next,
                               int force, cudaStream_t st);
+// consolidate(k_next = 1) then decode: the decode grid, then the fold grid
+// that folds the full rings and decodes their token from the new rows
+cudaError_t launch_delta_fold_decode(const replayssm_dims& d, const replayssm_state& s,
+                                     const void* q, const void* k, const void* v,
+                                     const float* alpha, const float* beta, float scale, float* o,
+                                     cudaStream_t st);
 cudaError_t launch_delta_conventional(const replayssm_dims& d, float* S, const void* q,
                                       const void* k, const void* v, const float* alpha,
                                       const float* beta, float scale, float* o, cudaStream_t st);
