@@ -239,7 +239,10 @@ class ClockSampler:
 class Layer:
     """One SSM layer's state, token pool and step functions on one GPU."""
 
-    def __init__(self, wl: dict, read: str, device, seed: int = 2, fused: bool = False):
+    def __init__(self, wl: dict, read: str, device, seed: int = 2, fused: bool = False,
+                 share: "Layer | None" = None):
+        """share: another layer of the same workload whose token pool (and
+        Mamba-2 A, D) this one reuses; only the state is new."""
         import numpy as np
         import torch
 
@@ -258,6 +261,11 @@ class Layer:
         if self.state.S_read is not None:
             api.refresh_read_copy(self.dims, self.state)
         self.device = device
+        self.fused = fused
+        if share is not None:
+            for name in ("host_pool", "pool", "A", "D", "out", "names", "vec"):
+                setattr(self, name, getattr(share, name, None))
+            return
         dt = lambda a, ty: torch.from_numpy(np.ascontiguousarray(a)).to(device, ty)  # noqa: E731
         self.host_pool, self.pool = [], []
         if k == "mamba2":
@@ -279,7 +287,6 @@ class Layer:
         self.out = torch.empty((b, H, dv), device=device)
         self.names = names
         self.vec = vec
-        self.fused = fused and k == "mamba2"
 
     # one decode step on device-resident inputs
     def consolidate(self, stream=None):
@@ -296,9 +303,12 @@ class Layer:
 
     def step(self, tok, stream=None):
         """One whole step: the fused call, or consolidate then decode."""
-        if self.fused:
+        if self.fused and self.wl["kind"] == "mamba2":
             self.api.mamba2_fold_decode(self.dims, self.state, self.A, self.D, tok["x"], tok["B"],
                                         tok["C"], tok["dt"], self.out, stream)
+        elif self.fused:
+            self.api.gdn_fold_decode(self.dims, self.state, tok["q"], tok["k"], tok["v"],
+                                     tok["alpha"], tok["beta"], 1.0, self.out, stream)
         else:
             self.consolidate(stream)
             self.decode(tok, stream)
@@ -320,8 +330,10 @@ class Layer:
         return 1 + (2 if self.wl["kind"] == "mamba2" else 1)
 
     def decode_kernels(self):
-        if self.fused:
+        if self.fused and self.wl["kind"] == "mamba2":
             return "mamba2_step_coef_kernel + mamba2_step_stream_kernel (one fused call)"
+        if self.fused:
+            return "delta_fused_kernel + delta_fold_stream_kernel (one fused call)"
         if self.wl["kind"] == "mamba2":
             return "mamba2_prep_kernel + stream_kernel (one decode call)"
         return "delta_fused_kernel (one decode call)"
@@ -407,39 +419,20 @@ class Layer:
         return self.state_elems() * 8 + self.token_bytes() + self.out.numel() * 4
 
 
-def run_ours(args, rank, local_rank, world):
+def time_steps(layer, K, Wm, stream, world, stagger=False):
+    """W untimed warm-up steps, then K timed steps bracketed by a barrier and a
+    synchronize, with events around every decode call. Returns the step-loop
+    milliseconds (max over ranks), per-call milliseconds, the device gaps
+    between calls (us), the ring lengths before the timed steps and the
+    number of sequences with device status bits."""
     import torch
 
-    device = torch.device("cuda", local_rank)
-    torch.cuda.set_device(device)
-    wl = dict(WORKLOADS[args.workload])
-    if args.batch:
-        wl["batch"] = args.batch
-    W = wl["window"]
-    layer = Layer(wl, args.read, device, fused=args.step == "fused")
-    stream = torch.cuda.current_stream(device)
-    K, Wm = args.steps, args.warmup
-
-    # The clock sampler starts first (its start-up takes the host for a
-    # while); the A/B and end-to-end loops then run, and the warm-up steps
-    # and the timed steps follow them directly, so the GPU does not idle
-    # (and drop its clocks) just before the timed region.
-    clocks = ClockSampler(local_rank) if not args.no_extras else None
-    if clocks:
-        clocks.__enter__()
-    extras = {}
-    if not args.no_extras:
-        extras["ab"] = run_ab(layer, K, Wm, stream, world)
-        extras["e2e"] = run_e2e(layer, args, stream, world)
-
-    # warm-up
     for i in range(Wm):
         layer.step(layer.pool[i % POOL])
-    if args.stagger:
+    if stagger:
         layer.stagger()
     torch.cuda.synchronize()
     lens0 = layer.state.ring_len.cpu().numpy()
-
     ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
     start, end = ev(), ev()
     d0 = [ev() for _ in range(K)]
@@ -461,8 +454,6 @@ def run_ours(args, rank, local_rank, world):
     end.synchronize()
     barrier(world)
     torch.cuda.synchronize()
-    if clocks:
-        clocks.__exit__(None, None, None)
     ms = max_over_ranks(start.elapsed_time(end), world)
     dec_ms = [d0[i].elapsed_time(d1[i]) for i in range(K)]
     gaps_us = [1e3 * d1[i].elapsed_time(d0[i + 1]) for i in range(K - 1)]
@@ -470,7 +461,14 @@ def run_ours(args, rank, local_rank, world):
     if bad:
         print(f"warning: {bad} sequences report device status bits "
               f"{sorted(set(layer.state.status.tolist()))}", file=sys.stderr)
+    return ms, dec_ms, gaps_us, lens0, bad
 
+
+def decode_record(layer, read, K, Wm, stream, world, stagger=False):
+    """Timed steps of one layer: tokens/s, the decode call's roofline, per-call
+    times. Keys of the JSON line (metric header excluded)."""
+    wl = layer.wl
+    ms, dec_ms, gaps_us, lens0, bad = time_steps(layer, K, Wm, stream, world, stagger)
     # algorithmic bytes of the timed region
     dec_bytes, fold_bytes = layer.account(lens0, K)
     peak, peak_kind = measured_peaks()
@@ -478,21 +476,15 @@ def run_ours(args, rank, local_rank, world):
     call_bytes = dec_bytes + (fold_bytes if layer.fused else 0)
     achieved = call_bytes / dec_s / 1e9
     tokens = wl["batch"] * K * world
-    value = tokens / (ms / 1e3)
-    step_gbs = (dec_bytes + fold_bytes) / (ms / 1e3) / 1e9
-
-    res = {
-        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
-        "steps": K, "warmup": Wm, "ms_per_step": round(ms / K, 5),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "f32", "data": "synthetic (seeded; no weights or datasets)",
-        "config": decode_config(wl, args.read, world, args.stagger, layer.fused),
-        "step_hbm_gbs": round(step_gbs, 1),
+    return {
+        "value": round(tokens / (ms / 1e3), 1), "ms_per_step": round(ms / K, 5),
+        "config": decode_config(wl, read, world, stagger, layer.fused),
+        "step_hbm_gbs": round((dec_bytes + fold_bytes) / (ms / 1e3) / 1e9, 1),
         "roofline": {
             "kernel": layer.decode_kernels(), "bound": "hbm", "achieved": round(achieved, 1),
             "peak": peak, "peak_source": peak_kind, "unit": "GB/s",
             "frac": round(achieved / peak, 4),
-            "traffic": traffic_per_call(wl, args.read, layer.fused),
+            "traffic": traffic_per_call(wl, read, layer.fused),
             "bytes_per_launch": int(call_bytes / K),
             "avg_launch_us": round(1e3 * sum(dec_ms) / K, 3),
         },
@@ -500,12 +492,159 @@ def run_ours(args, rank, local_rank, world):
         "device_status_ok": bad == 0,
         "calls": call_stats(dec_ms, gaps_us, layer.fold_steps(lens0, K)),
     }
+
+
+def run_ours(args, rank, local_rank, world):
+    import torch
+
+    device = torch.device("cuda", local_rank)
+    torch.cuda.set_device(device)
+    wl = dict(WORKLOADS[args.workload])
+    if args.batch:
+        wl["batch"] = args.batch
+    layer = Layer(wl, args.read, device, fused=args.step == "fused")
+    stream = torch.cuda.current_stream(device)
+    K, Wm = args.steps, args.warmup
+
+    # The clock sampler starts first (its start-up takes the host for a
+    # while); the A/B and end-to-end loops then run, and the warm-up steps
+    # and the timed steps follow them directly, so the GPU does not idle
+    # (and drop its clocks) just before the timed region.
+    clocks = ClockSampler(local_rank) if not args.no_extras else None
     if clocks:
-        res["clocks"] = clocks.summary()
+        clocks.__enter__()
+    extras = {}
+    if not args.no_extras:
+        extras["ab"] = run_ab(layer, K, Wm, stream, world)
+        extras["e2e"] = run_e2e(layer, args, stream, world)
+    rec = decode_record(layer, args.read, K, Wm, stream, world, args.stagger)
+    res = {"metric": METRIC, "value": rec.pop("value"), "unit": UNIT, "n_gpus": world,
+           "steps": K, "warmup": Wm, "ms_per_step": rec.pop("ms_per_step"),
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+           "dtype": "f32", "data": "synthetic (seeded; no weights or datasets)"}
+    res.update(rec)
     res.update(extras)
+    if not args.no_extras and args.workload == "mamba2" and not args.batch:
+        del layer
+        torch.cuda.empty_cache()
+        res["others"] = other_workloads(args, device, stream, world)
+        res["kda_sweep"] = kda_sweep(device, stream, world)
+    if clocks:
+        clocks.__exit__(None, None, None)
+        res["clocks"] = clocks.summary()
     if not args.no_extras and rank == 0:
         res["cpu_baseline"] = cpu_baseline(wl, args.cpu_seconds)
     return res
+
+
+def other_workloads(args, device, stream, world):
+    """The GDN and KDA layers (b256) and the GDN speculative rounds (b512, K = 4)
+    measured the same way as the headline, with their conventional A/B, so the
+    line carries every workload: {name: record}."""
+    import torch
+
+    out = {}
+    K, Wm = args.steps, args.warmup
+    for name in ("gdn", "kda"):
+        layer = Layer(dict(WORKLOADS[name]), args.read, device, fused=args.step == "fused")
+        rec = {"ab": run_ab(layer, K, Wm, stream, world)}
+        rec.update(decode_record(layer, args.read, K, Wm, stream, world))
+        rec["unit"] = UNIT
+        out[name] = rec
+        del layer
+        torch.cuda.empty_cache()
+    spec_args = argparse.Namespace(**dict(vars(args), workload="gdn_spec", batch=None))
+    rec = spec_rounds(spec_args, device, world)
+    out["gdn_spec"] = rec
+    torch.cuda.empty_cache()
+    return out
+
+
+def kda_sweep(device, stream, world, steps=256, warm=16):
+    """The KDA layer (H32, d_k = d_v = 128, W16) at batch 1, 8, 64, 256 and 512:
+    replay with the BF16 read copy and with the FP32 read path, against the
+    conventional read-modify-write step, 256 steps each (16 folds). Below
+    batch 256 a step goes to the next of L layer instances in turn, L chosen
+    so that the instances' state exceeds four times the L2 cache; a row whose
+    working set still fits that bound (L capped at 256) says "hot_l2": true.
+    Tokens/s count the whole step loop; frac is its algorithmic bytes per
+    second against the measured peak."""
+    import math
+
+    import torch
+
+    l2 = torch.cuda.get_device_properties(device).L2_cache_size
+    peak, _ = measured_peaks()
+    ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+    rows = []
+    for b in (1, 8, 64, 256, 512):
+        wl = dict(WORKLOADS["kda"], batch=b)
+        row = {"batch": b}
+        base = None
+        for read in ("bf16", "f32"):
+            first = Layer(wl, read, device, seed=5, share=base)
+            base = base or first
+            per = layer_bytes(first)
+            n_inst = 1 if per >= 4 * l2 else min(256, math.ceil(4 * l2 / per))
+            layers = [first] + [Layer(wl, read, device, seed=5 + i, share=first)
+                                for i in range(1, n_inst)]
+            for i in range(warm):
+                layers[i % n_inst].step(first.pool[i % POOL])
+            torch.cuda.synchronize()
+            lens0 = [lay.state.ring_len.cpu().numpy() for lay in layers]
+            a, e = ev(), ev()
+            a.record(stream)
+            for i in range(steps):
+                layers[i % n_inst].step(first.pool[i % POOL])
+            e.record(stream)
+            e.synchronize()
+            ms = max_over_ranks(a.elapsed_time(e), world)
+            nbytes = 0.0
+            for j, lay in enumerate(layers):  # steps j, j + L, ... went to instance j
+                n_j = len(range(j, steps, n_inst))
+                dec, fold = lay.account(lens0[j], n_j)
+                nbytes += dec + fold
+            row[f"replay_{read}"] = {
+                "tokens_per_s": round(b * steps * world / (ms / 1e3), 1),
+                "us_per_step": round(1e3 * ms / steps, 2),
+                "frac": round(nbytes / (ms / 1e3) / 1e9 / peak, 4),
+                "instances": n_inst, "hot_l2": n_inst * per < 4 * l2}
+            del layers, first
+            torch.cuda.empty_cache()
+        # conventional read-modify-write on the same rotation of states
+        conv = Layer(wl, "f32", device, seed=5, share=base)
+        per = conv.state_elems() * 4
+        n_inst = 1 if per >= 4 * l2 else min(256, math.ceil(4 * l2 / per))
+        states = [conv.state.S_ckpt] + [conv.state.S_ckpt.clone() for _ in range(1, n_inst)]
+        for i in range(warm):
+            conv.conventional(states[i % n_inst], base.pool[i % POOL])
+        torch.cuda.synchronize()
+        a, e = ev(), ev()
+        a.record(stream)
+        for i in range(steps):
+            conv.conventional(states[i % n_inst], base.pool[i % POOL])
+        e.record(stream)
+        e.synchronize()
+        ms = max_over_ranks(a.elapsed_time(e), world)
+        row["conventional"] = {
+            "tokens_per_s": round(b * steps * world / (ms / 1e3), 1),
+            "us_per_step": round(1e3 * ms / steps, 2),
+            "frac": round(conv.conventional_bytes() * steps / (ms / 1e3) / 1e9 / peak, 4),
+            "instances": n_inst, "hot_l2": n_inst * per < 4 * l2}
+        row["replay_bf16_vs_conventional"] = round(
+            row["replay_bf16"]["tokens_per_s"] / row["conventional"]["tokens_per_s"], 3)
+        rows.append(row)
+        del conv, states, base
+        torch.cuda.empty_cache()
+    return {"workload": "kda_h32_d128_w16 batch sweep", "steps": steps, "warmup": warm,
+            "l2_bytes": l2, "rows": rows}
+
+
+def layer_bytes(layer):
+    """Device bytes of one layer instance's state: checkpoint, read copy, ring."""
+    st = layer.state
+    n = st.S_ckpt.numel() * 4 + (st.S_read.numel() * 2 if st.S_read is not None else 0)
+    return n + sum(t.numel() * t.element_size() for t in st.ring.values())
 
 
 def call_stats(dec_ms, gaps_us, folds):
@@ -548,51 +687,90 @@ def run_ab(layer, K, Wm, stream, world):
 
 def run_e2e(layer, args, stream, world):
     """The same step through the public API with host buffers: every step copies
-    its inputs from pinned host memory and reads the output back."""
+    its inputs from pinned host memory and reads the output back. The copies
+    run on two copy streams, one per direction, with two staging sets: step
+    i + 1's inputs go up while step i computes and step i - 1's output comes
+    down, as a serving loop that overlaps transfers with compute does."""
     import torch
 
     host = [{n: t.cpu().pin_memory() for n, t in tok.items()} for tok in layer.pool]
-    stage = {n: torch.empty_like(t) for n, t in layer.pool[0].items()}
-    y_host = torch.empty(layer.out.shape, dtype=torch.float32).pin_memory()
+    stages = [{n: torch.empty_like(t) for n, t in layer.pool[0].items()} for _ in range(2)]
+    outs = [layer.out, torch.empty_like(layer.out)]
+    y_host = [torch.empty(layer.out.shape, dtype=torch.float32).pin_memory() for _ in range(2)]
     h2d = sum(t.numel() * t.element_size() for t in host[0].values())
-    d2h = y_host.numel() * 4
+    d2h = y_host[0].numel() * 4
     K = max(16, args.steps // 4)
+    up, down = torch.cuda.Stream(layer.device), torch.cuda.Stream(layer.device)
+    ev = lambda: torch.cuda.Event()  # noqa: E731
+    landed, done, read = [ev(), ev()], [ev(), ev()], [ev(), ev()]
+    started = [False, False]
 
     def step(i):
-        for n, t in host[i % POOL].items():
-            stage[n].copy_(t, non_blocking=True)
-        layer.step(stage)
-        y_host.copy_(layer.out, non_blocking=True)
+        k = i % 2
+        with torch.cuda.stream(up):  # inputs of step i, once step i - 2 has used the set
+            if started[k]:
+                up.wait_event(done[k])
+            for n, t in host[i % POOL].items():
+                stages[k][n].copy_(t, non_blocking=True)
+            landed[k].record(up)
+        stream.wait_event(landed[k])
+        if started[k]:
+            stream.wait_event(read[k])  # step i - 2's output has been read back
+        layer.out = outs[k]
+        layer.step(stages[k])
+        done[k].record(stream)
+        with torch.cuda.stream(down):
+            down.wait_event(done[k])
+            y_host[k].copy_(outs[k], non_blocking=True)
+            read[k].record(down)
+        started[k] = True
 
     for i in range(8):
         step(i)
     torch.cuda.synchronize()
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     a.record(stream)
+    up.wait_event(a)
     for i in range(K):
         step(i)
+    stream.wait_event(read[(K - 1) % 2])
     b.record(stream)
     b.synchronize()
+    layer.out = outs[0]
     ms = max_over_ranks(a.elapsed_time(b), world)
     return {"value": round(layer.wl["batch"] * K * world / (ms / 1e3), 1), "unit": UNIT,
-            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": K}
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": K,
+            "copies": "pinned host buffers; one copy stream per direction, two staging sets"}
 
 
-# ------------------------------------------------------ speculative rounds
 def run_spec(args, rank, local_rank, world):
+    """Speculative decoding rounds as the JSON line's workload."""
+    import torch
+
+    device = torch.device("cuda", local_rank)
+    torch.cuda.set_device(device)
+    clocks = ClockSampler(local_rank) if not args.no_extras else None
+    if clocks:
+        clocks.__enter__()
+    res = spec_rounds(args, device, world)
+    if clocks:
+        clocks.__exit__(None, None, None)
+        res["clocks"] = clocks.summary()
+    return res
+
+
+def spec_rounds(args, device, world):
     """Speculative decoding rounds on a delta layer: consolidate(k_next = K),
     verify K drafts from one read of the state, accept m drafts by moving the
     ring pointer (m drawn U{0..K} per sequence and round). The A/B runs the
-    conventional baseline on the same drafts: verify with a state snapshot per
-    draft, then accept by copying snapshot m - 1 into the state."""
+    conventional baseline on the same drafts first: verify with a state
+    snapshot per draft, then accept by copying snapshot m - 1 into the state."""
     import numpy as np
     import torch
 
     import synth
     from recurrent_state_fp32_b300 import api
 
-    device = torch.device("cuda", local_rank)
-    torch.cuda.set_device(device)
     wl = dict(WORKLOADS[args.workload])
     if args.batch:
         wl["batch"] = args.batch
@@ -606,56 +784,20 @@ def run_spec(args, rank, local_rank, world):
         api.refresh_read_copy(dims, state)
     seed, rounds_pool = 4, 8
     to = lambda a, ty: torch.from_numpy(np.ascontiguousarray(a)).to(device, ty)  # noqa: E731
-    drafts, ms, m_tot = [], [], []
+    drafts, ms, m_host, m_tot = [], [], [], []
     for r in range(rounds_pool):
         dr = synth.spec_draft_inputs(seed, r, b, K, H, dk, dv, kind, "bf16")
         drafts.append({n: to(v, torch.bfloat16 if n in ("q", "k", "v") else torch.float32)
                        for n, v in dr.items()})
         m = synth.accept_counts(seed, r, b, K)
         ms.append(to(m, torch.int32))
+        m_host.append(np.asarray(m, np.int64))
         m_tot.append(int(m.sum()))
     o = torch.empty((b, K, H, dv), device=device)
-
-    def round_(i):
-        d = drafts[i % rounds_pool]
-        api.consolidate(dims, state, None, K, False)
-        api.spec_verify(dims, state, K, d["q"], d["k"], d["v"], d["alpha"], d["beta"], 1.0, o)
-        api.accept(dims, state, ms[i % rounds_pool], K)
-
-    Kt, Wm = args.steps, args.warmup
-    for i in range(Wm):
-        round_(i)
-    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream(device)
     ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
-    a0, a1 = ev(), ev()
-    clocks = ClockSampler(local_rank) if not args.no_extras else None
-    if clocks:
-        clocks.__enter__()
-    barrier(world)
-    torch.cuda.synchronize()
-    a0.record()
-    for i in range(Kt):
-        round_(Wm + i)
-    a1.record()
-    a1.synchronize()
-    barrier(world)
-    if clocks:
-        clocks.__exit__(None, None, None)
-    ms_tot = max_over_ranks(a0.elapsed_time(a1), world)
-    accepted = sum(m_tot[(Wm + i) % rounds_pool] for i in range(Kt)) * world
-    bad = int(state.status.ne(0).sum().item())
-    res = {
-        "metric": SPEC_METRIC,
-        "value": round(accepted / (ms_tot / 1e3), 1), "unit": SPEC_UNIT,
-        "n_gpus": world, "steps": Kt, "warmup": Wm, "ms_per_step": round(ms_tot / Kt, 5),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
-        "data": "synthetic (seeded; no weights or datasets)",
-        "config": spec_config(wl, args.read, world),
-        "verified_tokens_per_s": round(b * K * Kt * world / (ms_tot / 1e3), 1),
-        "gpu_launches": Kt * 3, "device_status_ok": bad == 0,
-    }
-    if clocks:
-        res["clocks"] = clocks.summary()
+    Kt, Wm = args.steps, args.warmup
+    extras = {}
     if not args.no_extras:
         # the conventional baseline: snapshots per draft, accept by copy
         S = state.S_ckpt.clone()
@@ -680,16 +822,94 @@ def run_spec(args, rank, local_rank, world):
         c1.synchronize()
         cms = max_over_ranks(c0.elapsed_time(c1), world)
         acc_c = sum(m_tot[i % rounds_pool] for i in range(Kc)) * world
-        res["ab"] = {"conventional_accepted_tokens_per_s": round(acc_c / (cms / 1e3), 1),
-                     "conventional_ms_per_round": round(cms / Kc, 5), "rounds": Kc,
-                     # verify: read S, write K snapshots; accept: copy one snapshot
-                     # for every sequence with m > 0
-                     "conventional_bytes_per_round":
-                         int(b * H * dv * dk * 4 * (1 + K) +
-                             np.mean([int((mm > 0).sum().item()) for mm in ms]) * H * dv * dk * 8)}
+        extras["ab"] = {"conventional_accepted_tokens_per_s": round(acc_c / (cms / 1e3), 1),
+                        "conventional_ms_per_round": round(cms / Kc, 5), "rounds": Kc,
+                        # verify: read S, write K snapshots; accept: copy one snapshot
+                        # for every sequence with m > 0
+                        "conventional_bytes_per_round":
+                            int(b * H * dv * dk * 4 * (1 + K) +
+                                np.mean([int((mm > 0).sum().item()) for mm in ms]) * H * dv * dk * 8)}
         del S, snaps
         torch.cuda.empty_cache()
+
+    v0 = [ev() for _ in range(Kt)]
+    v1 = [ev() for _ in range(Kt)]
+
+    def round_(i, timed=None):
+        d = drafts[i % rounds_pool]
+        api.consolidate(dims, state, None, K, False)
+        if timed is not None:
+            v0[timed].record(stream)
+        api.spec_verify(dims, state, K, d["q"], d["k"], d["v"], d["alpha"], d["beta"], 1.0, o)
+        if timed is not None:
+            v1[timed].record(stream)
+        api.accept(dims, state, ms[i % rounds_pool], K)
+
+    for i in range(Wm):
+        round_(i)
+    torch.cuda.synchronize()
+    lens0 = state.ring_len.cpu().numpy().astype(np.int64)
+    a0, a1 = ev(), ev()
+    barrier(world)
+    torch.cuda.synchronize()
+    a0.record(stream)
+    for i in range(Kt):
+        round_(Wm + i, timed=i)
+    a1.record(stream)
+    a1.synchronize()
+    barrier(world)
+    ms_tot = max_over_ranks(a0.elapsed_time(a1), world)
+    ver_ms = sum(v0[i].elapsed_time(v1[i]) for i in range(Kt))
+    accepted = sum(m_tot[(Wm + i) % rounds_pool] for i in range(Kt)) * world
+    bad = int(state.status.ne(0).sum().item())
+    ver_bytes, fold_bytes = spec_account(dims, state, lens0, [m_host[(Wm + i) % rounds_pool]
+                                                                for i in range(Kt)], K)
+    peak, peak_kind = measured_peaks()
+    res = {
+        "metric": SPEC_METRIC,
+        "value": round(accepted / (ms_tot / 1e3), 1), "unit": SPEC_UNIT,
+        "n_gpus": world, "steps": Kt, "warmup": Wm, "ms_per_step": round(ms_tot / Kt, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded; no weights or datasets)",
+        "config": spec_config(wl, args.read, world),
+        "verified_tokens_per_s": round(b * K * Kt * world / (ms_tot / 1e3), 1),
+        "step_hbm_gbs": round((ver_bytes + fold_bytes) / (ms_tot / 1e3) / 1e9, 1),
+        "roofline": {
+            "kernel": "delta_fused_kernel<K=4> (one verify call)", "bound": "hbm",
+            "achieved": round(ver_bytes / (ver_ms / 1e3) / 1e9, 1), "peak": peak,
+            "peak_source": peak_kind, "unit": "GB/s",
+            "frac": round(ver_bytes / (ver_ms / 1e3) / 1e9 / peak, 4), "traffic": None,
+            "bytes_per_launch": int(ver_bytes / Kt), "avg_launch_us": round(1e3 * ver_ms / Kt, 3)},
+        "gpu_launches": Kt * 3, "device_status_ok": bad == 0,
+    }
+    res.update(extras)
     return res
+
+
+def spec_account(dims, state, lens0, m_rounds, K):
+    """Algorithmic bytes of speculative rounds (verify, consolidate) from the
+    ring lengths before them and each round's accept counts. Verify: the
+    state read once (read copy, else FP32), the committed entries' k, v, gate
+    and beta, the K drafts read and written to the ring, the K outputs.
+    Consolidate(k_next = K): for each sequence with len + K > W, FP32 read and
+    write (and the read copy written) plus its entries."""
+    import numpy as np
+
+    b, H, dk, dv, W = dims.batch, dims.heads, dims.dk, dims.dv, dims.window
+    elems = H * dv * dk
+    ts = 2 if state.S_read is not None else 4
+    gate = H * 4 if dims.kind == "gdn" else H * dk * 4
+    entry = H * dk * 2 + H * dv * 2 + gate + H * 4        # k, v, alpha, beta of one entry
+    draft = H * dk * 2 * 2 + H * dv * 2 + gate + H * 4    # q, k, v, alpha, beta
+    lens = np.array(lens0, np.int64)
+    ver = fold = 0.0
+    for m in m_rounds:
+        f = lens + K > W
+        fold += f.sum() * (elems * (8 + (2 if ts == 2 else 0))) + lens[f].sum() * entry
+        lens[f] = 0
+        ver += b * elems * ts + lens.sum() * entry + b * K * (2 * draft) + b * K * H * dv * 4
+        lens += np.asarray(m, np.int64)
+    return ver, fold
 
 
 # --------------------------------------------------------- oracle timing
@@ -732,12 +952,13 @@ def _single_thread():
         return contextlib.nullcontext()
 
 
-def cpu_baseline(wl: dict, seconds: float):
-    """The oracle as it stands, single-threaded on the host, on a bounded sample
-    (one sequence, all heads) of the same workload; scaled to tokens/s."""
-    heads = wl["heads"]
-    orc, toks, _ = oracle_sample(wl, heads)
+def _oracle_steps(job):
+    """One host process or thread of the CPU baseline: the oracle on one
+    sequence (all heads) of the workload for about `seconds`, single-threaded.
+    Returns (steps, seconds)."""
+    wl, seconds, seed = job
     with _single_thread():
+        orc, toks, _ = oracle_sample(wl, wl["heads"], seed=seed)
         t0 = time.perf_counter()
         n = 0
         while True:
@@ -746,10 +967,32 @@ def cpu_baseline(wl: dict, seconds: float):
             n += 1
             if time.perf_counter() - t0 > seconds and n % wl["window"] == 0:
                 break
-        dt = time.perf_counter() - t0
-    return {"value": round(n / dt, 3), "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": f"1 sequence x {heads} heads, {n} consecutive decode steps "
-                      f"(consolidate + decode), float64 numpy, {dt:.1f} s"}
+        return n, time.perf_counter() - t0
+
+
+def cpu_baseline(wl: dict, seconds: float):
+    """The oracle as it stands on the host's cores, on a bounded sample of the
+    same workload: one single-threaded process per host core, each decoding
+    its own sequence (all heads) for about `seconds`; tokens/s summed over the
+    processes. The single-threaded rate of one such process is reported too.
+    The pool is spawned (never forked) so no child inherits a CUDA context."""
+    import multiprocessing as mp
+
+    host_cores = os.cpu_count() or 1
+    n1, t1 = _oracle_steps((wl, seconds, 2))
+    single = round(n1 / t1, 3)
+    procs = host_cores
+    with mp.get_context("spawn").Pool(procs) as pool:
+        runs = pool.map(_oracle_steps, [(wl, seconds, 100 + i) for i in range(procs)])
+    value = sum(n / t for n, t in runs)
+    return {"value": round(value, 3), "unit": UNIT, "cores": procs, "host_cores": host_cores,
+            "kind": "oracle",
+            "sample": f"{procs} processes x 1 sequence x {wl['heads']} heads, each about "
+                      f"{seconds:.0f} s of consecutive decode steps (consolidate + decode), "
+                      f"float64 numpy, one thread each",
+            "single_thread": {"value": single, "unit": UNIT, "cores": 1,
+                              "sample": f"1 sequence x {wl['heads']} heads, {n1} steps, "
+                                        f"{t1:.1f} s"}}
 
 
 def run_reference(args, rank, world):
