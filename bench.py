@@ -62,11 +62,14 @@ TRAFFIC_B64 = {
     ("gdn", "bf16"): 77.416192e6 + 1.435392e6,
 }
 # The same for one fused Mamba-2 fold + decode call (coefficient + step
-# stream kernels), averaged over 16 consecutive calls of which one folds
-# every sequence: a sixteenth of the batch folds per call on average, in
-# lockstep or with staggered ring phases alike. Empty until captured for the
-# current kernels.
-TRAFFIC_B64_FUSED: dict = {}
+# stream kernels), averaged over a 16-call cycle in which one call folds every
+# sequence: a plain call at ring length 5 and the folding call, captured at
+# batch 64, weighted 15 : 1. A sixteenth of the batch folds per call on
+# average, in lockstep or with staggered ring phases alike.
+TRAFFIC_B64_FUSED = {
+    ("mamba2", "bf16"): (15 * (0.756736e6 + 141.772032e6 + 3.569920e6)
+                         + (0.940544e6 + 288.052224e6 + 345.972224e6)) / 16,
+}
 
 
 def traffic_per_call(wl: dict, read: str, fused: bool):
