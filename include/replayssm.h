@@ -241,6 +241,13 @@ REPLAYSSM_API replayssm_status replayssm_gdn_fold_decode(
  * Precondition len + K <= W (consolidate with k_next = K first), else
  * RING_FULL and the sequence is untouched. Mamba-2 layers use
  * replayssm_mamba2_spec_verify (here: REPLAYSSM_ERR_UNSUPPORTED).
+ * GDN with a BF16 read copy and BF16 inputs (K > 1, W <= 16, d_k 64 or
+ * 128, d_v a multiple of 64, state->S_read 16-byte aligned) runs the
+ * tensor-core form: the products S [q_0..q_{K-1} | k_0..k_{n-1}]^T on
+ * mma.sync (BF16 operands, FP32 sums) and the sweep coefficients from a
+ * Gram tile of the keys; the environment variable
+ * REPLAYSSM_DELTA_TENSOR_CORES=0 selects the FFMA kernel instead (same
+ * results up to FP32 rounding order).
  */
 REPLAYSSM_API replayssm_status replayssm_spec_verify(
     const replayssm_dims* dims, const replayssm_state* state, int32_t K, const void* q,

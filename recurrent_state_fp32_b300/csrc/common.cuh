@@ -275,6 +275,34 @@ __device__ __forceinline__ void block_copy_warp(void* dst, const void* src, int 
   for (int i = lane; i < bytes / 16; i += 32) d[i] = s[i];
 }
 
+// ------------------------------------------------------------ tensor cores (mma.sync)
+
+// Four 8 x 8 b16 matrices from shared memory: lane l gives the address of
+// row (l mod 8) of matrix l / 8; register i holds matrix i in the mma
+// fragment layout (lane 4g + t: row g, elements 2t and 2t + 1).
+__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], uint32_t addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+// Two matrices (addresses from lanes 0-15).
+__device__ __forceinline__ void ldsm_x2(uint32_t (&r)[2], uint32_t addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0,%1}, [%2];"
+               : "=r"(r[0]), "=r"(r[1])
+               : "r"(addr));
+}
+// d += A B for a 16 x 16 BF16 A (row-major fragment a) and a 16 x 8 BF16 B
+// (column-major fragment b0, b1), FP32 accumulators: d[0..1] row g, d[2..3]
+// row g + 8, columns 2t and 2t + 1 (lane 4g + t).
+__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                               uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
 // ------------------------------------------------------------ reductions
 
 // Reduce-scatter across groups of L lanes: lane l holds L partial sums

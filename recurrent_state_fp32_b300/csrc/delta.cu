@@ -16,13 +16,88 @@
 // prep warps run the sweeps while its producer and consumer warps stream S_c
 // and write o = S_c u + buffer terms for every query. The fold applies the n updates
 // row by row in FP32 registers: s <- alpha (.) s; s <- s + beta (v_r - s.k) k.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include <algorithm>
+#include <cstdlib>
 
 #include "common.cuh"
 #include "launch.h"
 
 namespace rs {
 namespace {
+
+// ------------------------------------------------------ Gram form of the sweeps
+
+constexpr int kGramN = 16;     // entries of one Gram tile
+constexpr int kGramQ = 8;      // queries of one Gram tile (the n = 8 columns)
+constexpr int kGramT = 24;     // floats per scratch row: G[j][0..15], P[j][0..7]
+
+// Gram form of the backward sweeps of one head (GDN). With G[j][i] = k_j . k_i
+// and P[j][t] = scale k_j . q_t, the sweep of query t (entries top = len + t
+// down to 0) keeps a[j] = k_j . u for every j below the current entry: it
+// starts at P[j][t], and entry i (c_i = beta_i a[i]) turns it into
+//   a[j] <- alpha_i (a[j] - c_i G[j][i]),
+// since u <- alpha_i (u - c_i k_i). So the coefficients c come from scalar
+// updates instead of n dot products over d_k, each behind a warp reduction.
+// G and P are one tensor-core tile: mma.sync m16n8k16 on the BF16 k rows
+// (exact products, FP32 sums), the k rows doubling as the B operand of G
+// (rows past n repeat row n - 1 and queries past K are zero, so every entry
+// of the tile is finite and the unused ones are never selected). Lane j
+// holds a[j] of every query; entry i broadcasts a[i] with one shuffle per
+// query, so the queries' chains interleave. c[t][i] goes to c_out.
+template <int DK, int KMAX>
+__device__ __forceinline__ void gram_coefficients(const unsigned char* kbase, const unsigned char* qbase,
+                                                  uint32_t ks, const float* ar, const float* br, int len,
+                                                  int K, float scale, float* __restrict__ T,
+                                                  float* __restrict__ c_out, int lane) {
+  const int g = lane >> 2, t4 = lane & 3;
+  float dg0[4] = {0.f, 0.f, 0.f, 0.f}, dg1[4] = {0.f, 0.f, 0.f, 0.f}, dp[4] = {0.f, 0.f, 0.f, 0.f};
+  // ldmatrix row addresses: matrix m = lane / 8 covers row (m & 1) * 8 + lane % 8
+  // and the column half m >> 1 of each 16-column step
+  const int m = lane >> 3, n = len + K;
+  const int row = min((m & 1) * 8 + (lane & 7), n - 1);
+  const uint32_t a_addr = smem_u32(kbase) + row * ks + (m >> 1) * 16;
+  // query B fragments straight from the q rows: column g = query g
+  const uint32_t* qw = reinterpret_cast<const uint32_t*>(qbase + (g < K ? g : 0) * ks) + t4;
+  uint32_t a[DK / 16][4], b[DK / 16][2];
+#pragma unroll
+  for (int kk = 0; kk < DK / 16; ++kk) {
+    ldsm_x4(a[kk], a_addr + kk * 32);
+    b[kk][0] = g < K ? qw[kk * 8] : 0u;
+    b[kk][1] = g < K ? qw[kk * 8 + 4] : 0u;
+  }
+#pragma unroll
+  for (int kk = 0; kk < DK / 16; ++kk) {
+    mma_bf16_16816(dg0, a[kk], a[kk][0], a[kk][2]);  // columns: k rows 0-7
+    mma_bf16_16816(dg1, a[kk], a[kk][1], a[kk][3]);  // k rows 8-15
+    mma_bf16_16816(dp, a[kk], b[kk][0], b[kk][1]);   // queries 0-7
+  }
+  *reinterpret_cast<float2*>(T + g * kGramT + 2 * t4) = make_float2(dg0[0], dg0[1]);
+  *reinterpret_cast<float2*>(T + (g + 8) * kGramT + 2 * t4) = make_float2(dg0[2], dg0[3]);
+  *reinterpret_cast<float2*>(T + g * kGramT + 8 + 2 * t4) = make_float2(dg1[0], dg1[1]);
+  *reinterpret_cast<float2*>(T + (g + 8) * kGramT + 8 + 2 * t4) = make_float2(dg1[2], dg1[3]);
+  *reinterpret_cast<float2*>(T + g * kGramT + 16 + 2 * t4) = make_float2(dp[0], dp[1]);
+  *reinterpret_cast<float2*>(T + (g + 8) * kGramT + 16 + 2 * t4) = make_float2(dp[2], dp[3]);
+  __syncwarp();
+  const int j = lane & (kGramN - 1);
+  float acc[KMAX];
+#pragma unroll
+  for (int t = 0; t < KMAX; ++t) acc[t] = t < K ? scale * T[j * kGramT + 16 + t] : 0.f;
+  for (int i = n - 1; i >= 0; --i) {
+    const float gji = T[j * kGramT + i], bi = br[i], ai = ar[i];
+#pragma unroll
+    for (int t = 0; t < KMAX; ++t) {
+      const float s = __shfl_sync(kFull, acc[t], i);
+      const bool vis = t < K && i <= len + t;  // entry i is below query t's top
+      const float c = vis ? bi * s : 0.f;
+      if (vis && lane == 0) c_out[t * kGramN + i] = c;
+      acc[t] = vis && j < i ? ai * fmaf(-c, gji, acc[t]) : acc[t];
+    }
+  }
+  __syncwarp();
+}
 
 // ------------------------------------------------------ fused decode / verify
 
@@ -1396,6 +1471,96 @@ __global__ void __launch_bounds__(kThreads) delta_conventional_verify_kernel(con
   }
 }
 
+#include "delta_gram.cuh"
+
+// The tensor-map encoder of the driver, looked up once (null if absent).
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static const PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      p = nullptr;
+    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }();
+  return fn;
+}
+
+// The tensor-core kernel serves speculative verify (K > 1) of GDN with a
+// BF16 read copy and BF16 inputs, d_k of 64 or 128, d_v a multiple of 64 and
+// windows up to kGramN entries; REPLAYSSM_DELTA_TENSOR_CORES=0 selects the
+// FFMA kernel instead. (A decode has one query: S [q | k]^T is then about 16
+// multiply-adds per state element on the mma.sync pipe against one FFMA per
+// element, and the FFMA kernel is as fast: 61 us against 63 us per b256 call.)
+bool gram_eligible(const replayssm_dims& d, const replayssm_state& s, int K) {
+  if (K < 2 || d.kind != REPLAYSSM_GDN || !s.S_read || d.in_dtype != REPLAYSSM_BF16) return false;
+  if ((d.dk != 64 && d.dk != 128) || d.dv % kGRows != 0 || d.window > kGramN || K > kGramQ) return false;
+  if ((reinterpret_cast<uintptr_t>(s.S_read) & 15) != 0) return false;
+  const char* e = std::getenv("REPLAYSSM_DELTA_TENSOR_CORES");
+  return !(e && e[0] == '0');
+}
+
+// Prep warps and stages of the tensor-core kernel: among (NP, depth) with
+// NP x depth x (units per head) a multiple of the consumer groups (each
+// group then sees every fill of the prep stages it reads, so no parity wait
+// can take an older phase) and at least 4 state stages, the most heads in
+// flight (NP x depth), ties to more stages. (b512 K = 4 verify: 7 x 2 with
+// 4 stages 205 us, 6 x 2 213 us, 6 x 1 with 8 stages 215 us.)
+struct GramConfig {
+  int NS, NP, depth;
+  size_t smem;
+};
+GramConfig gram_config(int DK, int DV, int W, int K, size_t optin) {
+  GramConfig best{0, 0, 0, 0};
+  const int nrb = DV / kGRows;
+  const int cands[][2] = {{7, 2}, {6, 2}, {4, 3}, {4, 2}, {2, 4}, {6, 1}, {3, 2}, {2, 2}, {4, 1}, {2, 1}};
+  for (const auto& c : cands) {
+    const int NP = c[0], depth = c[1];
+    if ((NP * depth * nrb) % kGGroups != 0) continue;
+    const GSmem L0(DK, DV, W, K, 0, NP, depth);
+    const size_t fixed = L0.total + 2048;  // + the block's static shared memory
+    if (fixed >= optin) continue;
+    const int NS = std::min((int)((optin - fixed) / (L0.stage + 16)), 12) / kGGroups * kGGroups;
+    if (NS < 4) continue;
+    const bool better = NP * depth > best.NP * best.depth || (NP * depth == best.NP * best.depth && NS > best.NS);
+    if (better) best = GramConfig{NS, NP, depth, GSmem(DK, DV, W, K, NS, NP, depth).total};
+  }
+  return best;
+}
+
+template <int DK, int KMAX>
+cudaError_t launch_gram(const DFused& f, const bf16* S, cudaStream_t st, bool& launched) {
+  launched = false;
+  const DeviceInfo& dev = device_info();
+  const GramConfig c = gram_config(DK, f.DV, f.W, f.K, (size_t)dev.smem_optin);
+  PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
+  if (c.NP == 0 || !encode) return cudaSuccess;  // not launched: the caller falls back
+  DGram g;
+  const cuuint64_t dims[2] = {(cuuint64_t)DK, (cuuint64_t)f.batch * f.H * f.DV};
+  const cuuint64_t strides[1] = {(cuuint64_t)DK * 2};
+  const cuuint32_t box[2] = {64, (cuuint32_t)kGRows};
+  const cuuint32_t estr[2] = {1, 1};
+  if (encode(&g.tmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<bf16*>(S), dims, strides, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return cudaSuccess;
+  g.f = f;
+  g.f.RB = kGRows;
+  g.f.nrb = f.DV / kGRows;
+  g.f.NS = c.NS;
+  g.f.NP = c.NP;
+  g.f.depth = c.depth;
+  auto kern = delta_gram_kernel<DK, KMAX>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)c.smem);
+  if (e != cudaSuccess) return e;
+  const long long heads = (long long)f.batch * f.H;
+  const int grid = (int)std::min<long long>(heads, dev.sms);
+  kern<<<grid, 32 * (2 * kGGroups + 1 + c.NP), c.smem, st>>>(g);
+  launched = true;
+  return cudaGetLastError();
+}
+
 // State rows per unit: about 16 KB (at least 32 rows, dividing DV).
 int fused_rows(int DK, int ts, int DV) {
   int RB = std::max(32, 16384 / (DK * ts) / 32 * 32);
@@ -1478,6 +1643,38 @@ FusedConfig fused_config(int RB, int DK, int DV, int W, int K, int GU, bool kda,
   return best;
 }
 
+// Decode (K = 1) from the BF16 read copy: the prep warps' sweeps bound the
+// call, so the configuration with the most prep warps wins, one consumer
+// warp per unit (GU = 1) where that frees warps for them, then the most
+// state stages, then depth 1. Measured on the b256 layers: GDN 8 prep warps
+// at depth 1 with 8 stages 61 us per call, 7 at depth 2 with 4 stages 67 us;
+// KDA 8 at depth 1 80 us, 4 at depth 2 84 us. Zero NP: nothing fits.
+FusedConfig decode_config(int RB, int DK, int DV, int W, bool kda, int ti, size_t optin, int& GU) {
+  FusedConfig best{0, 0, 0, 0, 0};
+  const int gu_first = RB % 64 == 0 ? 2 : 1;
+  for (int gu = gu_first; gu >= 1; --gu) {
+    if (RB / gu > 128) continue;
+    for (int depth = 1; depth <= 2; ++depth) {
+      for (int NP = kFWarps - 1 - kFGroups * gu; NP >= 1; --NP) {
+        const int NSL = vector_slots(NP, DV / RB);
+        if (NSL == 0) continue;
+        const DFusedSmem L0(RB, DK, DV, W, 1, 0, NSL, NP, depth, kda, 2, ti);
+        const size_t fixed = L0.total + 1024;
+        if (fixed >= optin) continue;
+        const int NS = std::min((int)((optin - fixed) / (L0.stage + 16)), 12) / kFGroups * kFGroups;
+        if (NS < min_stages(2)) continue;
+        const bool better = NP > best.NP || (NP == best.NP && (NS > best.NS || (NS == best.NS && depth < best.depth)));
+        if (better) {
+          best = FusedConfig{NS, NSL, NP, depth, DFusedSmem(RB, DK, DV, W, 1, NS, NSL, NP, depth, kda, 2, ti).total};
+          GU = gu;
+        }
+        break;  // fewer prep warps at this depth only lose
+      }
+    }
+  }
+  return best;
+}
+
 // Tile shape, stage count and template instance of the fused kernel.
 template <int DK, typename TS, typename TI, bool KDA, int KMAX>
 cudaError_t launch_fused(DFused a, cudaStream_t st) {
@@ -1487,8 +1684,11 @@ cudaError_t launch_fused(DFused a, cudaStream_t st) {
   a.nrb = a.DV / RB;
   a.GU = RB % 64 == 0 ? 2 : 1;  // each warp's share must be whole 32-row groups
   if (RB / a.GU > 128 || a.K > KMAX) return cudaErrorInvalidValue;
-  const FusedConfig c = fused_config(RB, DK, a.DV, a.W, a.K, a.GU, KDA, sizeof(TS), sizeof(TI),
-                                     (size_t)dev.smem_optin);
+  FusedConfig c{0, 0, 0, 0, 0};
+  if (a.K == 1 && sizeof(TS) == 2)
+    c = decode_config(RB, DK, a.DV, a.W, KDA, sizeof(TI), (size_t)dev.smem_optin, a.GU);
+  if (c.NP == 0)
+    c = fused_config(RB, DK, a.DV, a.W, a.K, a.GU, KDA, sizeof(TS), sizeof(TI), (size_t)dev.smem_optin);
   if (c.NP == 0) return cudaErrorInvalidConfiguration;
   a.NS = c.NS;
   a.NSL = c.NSL;
@@ -1521,6 +1721,18 @@ cudaError_t launch_delta(const replayssm_dims& d, const replayssm_state& s, int 
            s.ring_head, s.ring_len, s.status, s.sync, flags};
   const bool rd16 = s.S_read != nullptr, in16 = d.in_dtype == REPLAYSSM_BF16;
   const bool kda = d.kind == REPLAYSSM_KDA;
+  if (gram_eligible(d, s, K)) {
+    bool launched = false;
+    const bf16* S = reinterpret_cast<const bf16*>(s.S_read);
+    cudaError_t e;
+    if (d.dk == 128)
+      e = K == 1 ? launch_gram<128, 1>(a, S, st, launched)
+                 : K <= 4 ? launch_gram<128, 4>(a, S, st, launched) : launch_gram<128, 8>(a, S, st, launched);
+    else
+      e = K == 1 ? launch_gram<64, 1>(a, S, st, launched)
+                 : K <= 4 ? launch_gram<64, 4>(a, S, st, launched) : launch_gram<64, 8>(a, S, st, launched);
+    if (e != cudaSuccess || launched) return e;
+  }
 #define RS_FUSED(DK_, TS_)                                                                     \
   return in16 ? (kda ? launch_fused_k<DK_, TS_, bf16, true>(a, st)                             \
                      : launch_fused_k<DK_, TS_, bf16, false>(a, st))                           \
