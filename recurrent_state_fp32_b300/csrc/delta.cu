@@ -761,9 +761,14 @@ __host__ __device__ constexpr int fold_lanes_per_row() { return DK / 16; }
 //   s <- alpha (.) s;  s <- s + beta (v[r] - s . k) k   for j = 0..n-1,
 // with the entries (float, entry order) in shared memory. A scalar GDN gate
 // is applied lazily: the rows hold s / gam, gam the product of the gates so
-// far, and are rescaled once at the end. k_j (and a KDA gate row) are read
+// far, and are rescaled once at the end -- or as soon as gam drops below
+// kGamFloor, which includes a gate of 0 (the rows are then reset to 0):
+// the running inverse 1 / gam is never formed from a huge or infinite
+// reciprocal. k_j (and a KDA gate row) are read
 // once per entry from shared memory for all four rows: the L lanes of a row
 // read L consecutive float4, one conflict-free broadcast per chunk.
+constexpr float kGamFloor = 0x1p-32f;
+
 template <int DK, bool KDA>
 __device__ __forceinline__ void fold_rows(float2 (&s)[kFoldRowsPT][8], const int (&r)[kFoldRowsPT],
                                           int n, int DV, int q, const float* kbuf,
@@ -790,7 +795,18 @@ __device__ __forceinline__ void fold_rows(float2 (&s)[kFoldRowsPT][8], const int
       }
     } else {
       gam *= abuf[j];
-      igam *= rbuf[j];
+      if (!(gam >= kGamFloor)) {  // the lazy product is applied to the rows now
+        const float2 gg = make_float2(gam, gam);
+#pragma unroll
+        for (int i = 0; i < kFoldRowsPT; ++i) {
+#pragma unroll
+          for (int m = 0; m < 8; ++m) s[i][m] = __fmul2_rn(s[i][m], gg);
+        }
+        gam = 1.f;
+        igam = 1.f;
+      } else {
+        igam *= rbuf[j];
+      }
     }
     float dot[kFoldRowsPT];
 #pragma unroll
