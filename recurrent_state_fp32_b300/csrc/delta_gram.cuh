@@ -43,10 +43,10 @@ struct alignas(128) DGram {
 
 // One prep stage (byte offsets): header (len, head, ok, seq), the vector
 // rows [K + W][ks] (queries, then the entries' keys), value rows [W][DV],
-// gates [W], betas [W], column weights [K][kGCols], value coefficients
-// [K][kGramN].
+// gates [W], betas [W], column weights [K][kGCols], value terms
+// e_t = sum_i c_{t,i} v_i [K][DV].
 struct GStage {
-  size_t ks, vec, vr, ar, br, wc, cc, bytes;
+  size_t ks, vec, vr, ar, br, wc, ev, bytes;
   __host__ __device__ GStage(int DK, int DV, int W, int K) {
     ks = (size_t)DK * 2 + 16;
     vec = 16;
@@ -54,8 +54,8 @@ struct GStage {
     ar = align_up(vr + (size_t)W * DV * 2, 16);
     br = ar + align_up((size_t)W * 4, 16);
     wc = br + align_up((size_t)W * 4, 16);
-    cc = wc + (size_t)K * kGCols * 4;
-    bytes = align_up(cc + (size_t)K * kGramN * 4, 128);
+    ev = wc + (size_t)K * kGCols * 4;
+    bytes = align_up(ev + (size_t)K * DV * 4, 128);
   }
 };
 
@@ -269,8 +269,7 @@ __global__ void __launch_bounds__(32 * kGMaxWarps, 1) delta_gram_kernel(const __
       }
       if (ok) {
         const float* wc = reinterpret_cast<const float*>(st + SG.wc);
-        const float* cc = reinterpret_cast<const float*>(st + SG.cc);
-        const bf16* vr = reinterpret_cast<const bf16*>(st + SG.vr);
+        const float* ev = reinterpret_cast<const float*>(st + SG.ev);
         const int row0 = rb * kGRows + part * 32;  // first value row of this warp
         float* ybase = a.o + ((size_t)seq * K * H + h) * DV + row0;
 #pragma unroll
@@ -287,16 +286,10 @@ __global__ void __launch_bounds__(32 * kGMaxWarps, 1) delta_gram_kernel(const __
               pr[2 * mt + 1] = fmaf(w2.x, acc[mt][nt][2], fmaf(w2.y, acc[mt][nt][3], pr[2 * mt + 1]));
             }
           }
-          // value terms: entries i = t4, t4 + 4, ... (coefficients past top are 0)
-          for (int i = t4; i < n; i += 4) {
-            const float ci = cc[t * kGramN + i];
-            const bf16* vrow = vr + (size_t)i * DV + row0 + gq;
-#pragma unroll
-            for (int q = 0; q < 4; ++q) pr[q] = fmaf(ci, to_f(vrow[8 * q]), pr[q]);
-          }
           // lane t4 of each 4-lane group ends with the row gq + 8 t4
           const float y = reduce_scatter<4>(pr, lane);
-          ybase[(size_t)t * H * DV + gq + 8 * t4] = y;
+          const int row = gq + 8 * t4;
+          ybase[(size_t)t * H * DV + row] = y + ev[t * DV + row0 + row];
         }
       }
       __syncwarp();
@@ -451,7 +444,6 @@ __global__ void __launch_bounds__(32 * kGMaxWarps, 1) delta_gram_kernel(const __
         float Ai = 1.f;
         for (int m = 0; m < n && m <= lane; ++m) Ai *= ar[m];
         float* wc = reinterpret_cast<float*>(st + SG.wc);
-        float* cc = reinterpret_cast<float*>(st + SG.cc);
         for (int t2 = 0; t2 < K; ++t2) {
           const int top = len + t2;
           const float Atop = __shfl_sync(kFull, Ai, top);
@@ -463,7 +455,24 @@ __global__ void __launch_bounds__(32 * kGMaxWarps, 1) delta_gram_kernel(const __
           if (lane < K) w = lane == t2 ? Atop * a.scale : 0.f;
           else if (i <= top) w = -cgr[t2 * kGramN + i] * Ak;
           if (lane < kGCols) wc[t2 * kGCols + lane] = w;
-          if (lane < kGramN) cc[t2 * kGramN + lane] = lane <= top ? cgr[t2 * kGramN + lane] : 0.f;
+        }
+        // e_t[r] = sum_{i <= top_t} c_{t,i} v_i[r]: lane rows r = lane + 32 m,
+        // the values read once for every query
+        const bf16* vr = reinterpret_cast<const bf16*>(st + SG.vr);
+        float* ev = reinterpret_cast<float*>(st + SG.ev);
+        for (int r = lane; r < DV; r += 32) {
+          float e[KMAX];
+#pragma unroll
+          for (int t2 = 0; t2 < KMAX; ++t2) e[t2] = 0.f;
+          for (int i = 0; i < n; ++i) {
+            const float vi = to_f(vr[(size_t)i * DV + r]);
+#pragma unroll
+            for (int t2 = 0; t2 < KMAX; ++t2)
+              if (t2 < K && i <= len + t2) e[t2] = fmaf(cgr[t2 * kGramN + i], vi, e[t2]);
+          }
+#pragma unroll
+          for (int t2 = 0; t2 < KMAX; ++t2)
+            if (t2 < K) ev[t2 * DV + r] = e[t2];
         }
       }
       __syncwarp();
