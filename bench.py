@@ -61,14 +61,20 @@ TRAFFIC_B64 = {
     ("mamba2", "bf16"): 136.526592e6 + 3.470848e6 + 10.205184e6,
     ("gdn", "bf16"): 77.416192e6 + 1.435392e6,
 }
-# The same for one fused Mamba-2 fold + decode call (coefficient + step
-# stream kernels), averaged over a 16-call cycle in which one call folds every
-# sequence: a plain call at ring length 5 and the folding call, captured at
-# batch 64, weighted 15 : 1. A sixteenth of the batch folds per call on
+# The same for one fused fold + decode call (Mamba-2: coefficient + step
+# stream kernels; GDN/KDA: decode grid + fold grid), averaged over a 16-call
+# cycle in which one call folds every sequence: a plain call (Mamba-2 at ring
+# length 5, GDN/KDA at 8) and the folding call, captured at batch 64,
+# weighted 15 : 1. A sixteenth of the batch folds per call on
 # average, in lockstep or with staggered ring phases alike.
 TRAFFIC_B64_FUSED = {
     ("mamba2", "bf16"): (15 * (0.756736e6 + 141.772032e6 + 3.569920e6)
                          + (0.940544e6 + 288.052224e6 + 345.972224e6)) / 16,
+    # decode grid + fold grid; plain call at ring length 8, and the folding call
+    ("gdn", "bf16"): (15 * (77.419264e6 + 1.047808e6 + 0.051968e6)
+                      + (0.068352e6 + 152.905472e6 + 140.516864e6)) / 16,
+    ("kda", "bf16"): (15 * (86.723072e6 + 1.925376e6 + 0.050944e6)
+                      + (0.069632e6 + 170.604032e6 + 141.200640e6)) / 16,
 }
 
 
