@@ -697,34 +697,54 @@ def run_ab(layer, K, Wm, stream, world):
 def run_e2e(layer, args, stream, world):
     """The same step through the public API with host buffers: every step copies
     its inputs from pinned host memory and reads the output back. The copies
-    run on two copy streams, one per direction, with two staging sets: step
+    run on two copy streams, one per direction, with three staging sets: step
     i + 1's inputs go up while step i computes and step i - 1's output comes
-    down, as a serving loop that overlaps transfers with compute does."""
+    down, as a serving loop that overlaps transfers with compute does. The
+    record adds each direction's copy rate alone and the token rate they
+    bound, and the host's enqueue time per step."""
     import torch
 
-    host = [{n: t.cpu().pin_memory() for n, t in tok.items()} for tok in layer.pool]
-    stages = [{n: torch.empty_like(t) for n, t in layer.pool[0].items()} for _ in range(2)]
-    outs = [layer.out, torch.empty_like(layer.out)]
-    y_host = [torch.empty(layer.out.shape, dtype=torch.float32).pin_memory() for _ in range(2)]
-    h2d = sum(t.numel() * t.element_size() for t in host[0].values())
+    # A step's inputs travel as one pinned buffer (one copy per step); the
+    # tensors the call takes are views of its device twin, 256-byte aligned.
+    names = list(layer.pool[0])
+    offs, o = {}, 0
+    for n in names:
+        offs[n] = o
+        o += -(-layer.pool[0][n].numel() * layer.pool[0][n].element_size() // 256) * 256
+    h2d = o
+
+    def views(buf):
+        return {n: buf[offs[n]:offs[n] + t.numel() * t.element_size()].view(t.dtype).view(t.shape)
+                for n, t in layer.pool[0].items()}
+
+    host = []
+    for tok in layer.pool:
+        hb = torch.empty(h2d, dtype=torch.uint8).pin_memory()
+        for n, t in views(hb).items():
+            t.copy_(tok[n].cpu())
+        host.append(hb)
+    NB = 3  # staging sets: step i + 1 goes up and step i - 1 comes down while step i runs
+    dev_bufs = [torch.empty(h2d, dtype=torch.uint8, device=layer.device) for _ in range(NB)]
+    stages = [views(b) for b in dev_bufs]
+    outs = [layer.out] + [torch.empty_like(layer.out) for _ in range(NB - 1)]
+    y_host = [torch.empty(layer.out.shape, dtype=torch.float32).pin_memory() for _ in range(NB)]
     d2h = y_host[0].numel() * 4
-    K = max(16, args.steps // 4)
+    K = max(64, args.steps // 4)
     up, down = torch.cuda.Stream(layer.device), torch.cuda.Stream(layer.device)
     ev = lambda: torch.cuda.Event()  # noqa: E731
-    landed, done, read = [ev(), ev()], [ev(), ev()], [ev(), ev()]
-    started = [False, False]
+    landed, done, read = [ev() for _ in range(NB)], [ev() for _ in range(NB)], [ev() for _ in range(NB)]
+    started = [False] * NB
 
     def step(i):
-        k = i % 2
-        with torch.cuda.stream(up):  # inputs of step i, once step i - 2 has used the set
+        k = i % NB
+        with torch.cuda.stream(up):  # inputs of step i, once step i - NB has used the set
             if started[k]:
                 up.wait_event(done[k])
-            for n, t in host[i % POOL].items():
-                stages[k][n].copy_(t, non_blocking=True)
+            dev_bufs[k].copy_(host[i % POOL], non_blocking=True)
             landed[k].record(up)
         stream.wait_event(landed[k])
         if started[k]:
-            stream.wait_event(read[k])  # step i - 2's output has been read back
+            stream.wait_event(read[k])  # step i - NB's output has been read back
         layer.out = outs[k]
         layer.step(stages[k])
         done[k].record(stream)
@@ -740,16 +760,39 @@ def run_e2e(layer, args, stream, world):
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     a.record(stream)
     up.wait_event(a)
+    t0 = time.perf_counter()
     for i in range(K):
         step(i)
-    stream.wait_event(read[(K - 1) % 2])
+    host_us = (time.perf_counter() - t0) * 1e6 / K
+    stream.wait_event(read[(K - 1) % NB])
     b.record(stream)
     b.synchronize()
     layer.out = outs[0]
     ms = max_over_ranks(a.elapsed_time(b), world)
+    # the same copies alone, each direction on its stream: the bound the
+    # transfers set on this loop (the directions overlap each other)
+    t = {}
+    for name, strm in (("up", up), ("down", down)):
+        c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        c0.record(strm)
+        with torch.cuda.stream(strm):
+            for i in range(K):
+                if name == "up":
+                    dev_bufs[i % NB].copy_(host[i % POOL], non_blocking=True)
+                else:
+                    y_host[i % NB].copy_(outs[i % NB], non_blocking=True)
+        c1.record(strm)
+        c1.synchronize()
+        t[name] = max_over_ranks(c0.elapsed_time(c1), world) / K
+    bound = layer.wl["batch"] * world / (max(t["up"], t["down"]) / 1e3)
     return {"value": round(layer.wl["batch"] * K * world / (ms / 1e3), 1), "unit": UNIT,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": K,
-            "copies": "pinned host buffers; one copy stream per direction, two staging sets"}
+            "copies": "one pinned input buffer and the output per step; one copy stream per direction, three staging sets",
+            "host_enqueue_us_per_step": round(host_us, 2),
+            "h2d_gbs": round(h2d / (t["up"] / 1e3) / 1e9, 1),
+            "d2h_gbs": round(d2h / (t["down"] / 1e3) / 1e9, 1),
+            "copy_bound_tokens_per_s": round(bound, 1)}
 
 
 def run_spec(args, rank, local_rank, world):
