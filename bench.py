@@ -547,13 +547,21 @@ def run_ours(args, rank, local_rank, world):
 
 
 def other_workloads(args, device, stream, world):
-    """The GDN and KDA layers (b256) and the GDN speculative rounds (b512, K = 4)
-    measured the same way as the headline, with their conventional A/B, so the
-    line carries every workload: {name: record}."""
+    """The headline layer with staggered ring phases (a sixteenth of the batch
+    folds in every call, as in continuous batching), the GDN and KDA layers
+    (b256) and the GDN speculative rounds (b512, K = 4), measured the same way
+    as the headline (the delta layers and the rounds with their conventional
+    A/B), so the line carries every workload: {name: record}."""
     import torch
 
     out = {}
     K, Wm = args.steps, args.warmup
+    layer = Layer(dict(WORKLOADS["mamba2"]), args.read, device, fused=args.step == "fused")
+    rec = decode_record(layer, args.read, K, Wm, stream, world, stagger=True)
+    rec["unit"] = UNIT
+    out["mamba2_staggered"] = rec
+    del layer
+    torch.cuda.empty_cache()
     for name in ("gdn", "kda"):
         layer = Layer(dict(WORKLOADS[name]), args.read, device, fused=args.step == "fused")
         rec = {"ab": run_ab(layer, K, Wm, stream, world)}
