@@ -1215,14 +1215,27 @@ __global__ void __launch_bounds__(kDFoldThreads, 2) delta_fold_stream_kernel(con
     }
     cp_async_commit();
   };
-  // the last arrival of a sequence's units moves its pointers
+  // The last arrival of a sequence's units moves its pointers. Thread 0
+  // arrives for a unit after the barrier that follows the unit's stores, and
+  // looks at the count it got back one unit later, so the atomic's round trip
+  // is off the block's path. No fence before it: the pointers it moves are
+  // read in this kernel only by the blocks that fold that sequence, before
+  // their own arrivals, and the state rows only by later launches.
+  int pend_seq = -1, pend_old = 0, pend_head = 0;
+  auto settle = [&]() {
+    if (pend_seq >= 0 && pend_old + 1 == H * nch) {
+      a.head[pend_seq] = pend_head;
+      a.len[pend_seq] = a.flags ? 1 : 0;
+      a.sync[pend_seq] = 0;
+    }
+    pend_seq = -1;
+  };
   auto arrive = [&](int u) {
+    settle();
     const int f = u / nch;
-    const int seq = fl.tile[f] / H, hd = fl.head[f], n = fl.len[f];
-    arrive_and_finish(a.sync + seq, 1, H * nch, [&] {
-      a.head[seq] = (hd + n) % W;
-      a.len[seq] = a.flags ? 1 : 0;
-    });
+    pend_seq = fl.tile[f] / H;
+    pend_head = (fl.head[f] + fl.len[f]) % W;
+    pend_old = atomicAdd(a.sync + pend_seq, 1);
   };
 
   if (units > 0) issue(0);
@@ -1239,6 +1252,7 @@ __global__ void __launch_bounds__(kDFoldThreads, 2) delta_fold_stream_kernel(con
     if (tid == 0 && u > 0) arrive(u - 1);
     if (!ok) {
       if (tid == 0) {
+        settle();
         for (int g = f; g < fl.count; ++g) atomicOr(a.status + fl.tile[g] / H, REPLAYSSM_SEQ_TIMEOUT);
         mbar_wait(bar, ph);  // no bulk copy may land after the block exits
       }
@@ -1304,7 +1318,10 @@ __global__ void __launch_bounds__(kDFoldThreads, 2) delta_fold_stream_kernel(con
   }
   if (units > 0) {
     __syncthreads();
-    if (tid == 0) arrive(units - 1);
+    if (tid == 0) {
+      arrive(units - 1);
+      settle();
+    }
   }
 }
 
