@@ -522,6 +522,28 @@ __global__ void __launch_bounds__(32 * kFWarps, 1) delta_fused_kernel(const DFus
       }
     };
 
+    // ---- arrivals: a decode's last arrival on a sequence's counter commits
+    // len + 1. Lane 0 adds its heads' count and looks at the count it got back
+    // at its next arrival, so the atomic's round trip is off the warp's path.
+    // No fence: len is read in this launch only at block start and by warps
+    // that have not yet arrived for that sequence; the appended ring entries
+    // only by later launches.
+    int pend_seq = -1, pend_old = 0, pend_units = 0, pend_len = 0;
+    auto settle = [&]() {
+      if (pend_seq >= 0 && pend_old + pend_units == H) {
+        a.len[pend_seq] = pend_len;
+        a.sync[pend_seq] = 0;
+      }
+      pend_seq = -1;
+    };
+    auto arrive_seq = [&](int sq, int units, int new_len) {
+      settle();
+      pend_seq = sq;
+      pend_units = units;
+      pend_len = new_len;
+      pend_old = atomicAdd(a.sync + sq, units);
+    };
+
     // ---- compute side
     int cur_seq = -1, len = 0, hd = 0, seq_count = 0;
     bool ok = false;
@@ -543,8 +565,7 @@ __global__ void __launch_bounds__(32 * kFWarps, 1) delta_fused_kernel(const DFus
       const int* hdr = reinterpret_cast<const int*>(st);
       const int seq = hdr[3];
       if (seq != cur_seq) {
-        if (a.commit && cur_seq >= 0 && ok && lane == 0)
-          arrive_and_finish(a.sync + cur_seq, seq_count, H, [&] { a.len[cur_seq] = len + 1; });
+        if (a.commit && cur_seq >= 0 && ok && lane == 0) arrive_seq(cur_seq, seq_count, len + 1);
         len = hdr[0];
         hd = hdr[1];
         ok = hdr[2] != 0;
@@ -680,8 +701,8 @@ __global__ void __launch_bounds__(32 * kFWarps, 1) delta_fused_kernel(const DFus
       while (h >= H) h -= H;
     }
     cp_async_wait_all();
-    if (a.commit && cur_seq >= 0 && ok && lane == 0 && !abort_flag)
-      arrive_and_finish(a.sync + cur_seq, seq_count, H, [&] { a.len[cur_seq] = len + 1; });
+    if (a.commit && cur_seq >= 0 && ok && lane == 0 && !abort_flag) arrive_seq(cur_seq, seq_count, len + 1);
+    if (lane == 0) settle();
   }
   __syncthreads();
   // No bulk copy may land after the block exits.
