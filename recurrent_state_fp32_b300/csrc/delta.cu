@@ -228,6 +228,11 @@ __global__ void __launch_bounds__(32 * kFWarps, 1) delta_fused_kernel(const DFus
     fence_mbar_init();
     abort_flag = 0;
   }
+  // (A fused step's fold grid is this grid's programmatic dependent. No early
+  // trigger: it launches as this grid completes, its launch overlapping the
+  // completion, and waits with griddepcontrol.wait before it reads the flags
+  // and pointers. Triggered at the start, its blocks queued behind this
+  // grid's and the staggered steps, which fold in every call, got slower.)
   // The sequences of this block's heads that are refused (pointers out of
   // range, or no room for K entries: with a.flags, the full rings left to
   // the fold grid): their state rows are not read. Read here, before any
@@ -1026,6 +1031,7 @@ __global__ void __launch_bounds__(kDFoldThreads, 2) delta_fold_kernel(const DFol
   const TI* rk = reinterpret_cast<const TI*>(a.ring_k);
   const TI* rv = reinterpret_cast<const TI*>(a.ring_v);
 
+  griddep_wait();  // a fused step's decode grid has written the flags and pointers
   collect_folds(fl, (long long)a.batch * H, H, a.len, a.head, a.status, W, a.k_next, a.force,
                 a.flags);
   for (int f = 0; f < fl.count; ++f) {
@@ -1196,6 +1202,7 @@ __global__ void __launch_bounds__(kDFoldThreads, 2) delta_fold_stream_kernel(con
     mbar_init(bar, 1);
     fence_mbar_init();
   }
+  griddep_wait();  // a fused step's decode grid has written the flags and pointers
   // (its barriers also publish the mbarrier's initialisation)
   collect_folds(fl, (long long)a.batch * H, H, a.len, a.head, a.status, W, a.k_next, a.force,
                 a.flags);
@@ -1880,8 +1887,22 @@ cudaError_t launch_delta_fold_grid(const replayssm_dims& d, const replayssm_stat
   }
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  kern<<<grid, kDFoldThreads, smem, st>>>(a);
-  return cudaGetLastError();
+  if (!step) {
+    kern<<<grid, kDFoldThreads, smem, st>>>(a);
+    return cudaGetLastError();
+  }
+  // the fused step: a programmatic dependent of the decode grid
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kDFoldThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, a);
 }
 
 }  // namespace
