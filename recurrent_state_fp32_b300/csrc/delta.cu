@@ -1534,7 +1534,7 @@ __global__ void __launch_bounds__(kThreads) delta_conventional_verify_kernel(con
 
 #include "delta_gram.cuh"
 
-// The tensor-map encoder of the driver, looked up once (null if absent).
+// cuTensorMapEncodeTiled from the CUDA driver API, looked up once (null if absent).
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   static const PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
     void* p = nullptr;
