@@ -53,13 +53,13 @@ WORKLOADS = {
 }
 POOL = 16  # distinct synthetic tokens, cycled through the timed steps
 
-# DRAM bytes (read + write) of one decode call at batch 64 from single-launch
-# ncu captures of the same kernels (Mamba-2: stream + prep kernels; GDN: the
-# fused kernel; ring length 8); traffic grows in proportion to the batch, so
+# DRAM bytes (read + write) of one split-step decode call at batch 64 from
+# ncu captures of the same kernels (Mamba-2: prep + stream kernels; GDN: the
+# decode kernel; ring length 8); traffic grows in proportion to the batch, so
 # it is scaled by batch / 64. Only for the captured kernels.
 TRAFFIC_B64 = {
-    ("mamba2", "bf16"): 136.526592e6 + 3.470848e6 + 10.205184e6,
-    ("gdn", "bf16"): 77.416192e6 + 1.435392e6,
+    ("mamba2", "bf16"): 136.523008e6 + 0.763136e6 + 10.210816e6,
+    ("gdn", "bf16"): 77.419264e6 + 1.037824e6,
 }
 # The same for one fused fold + decode call (Mamba-2: coefficient + step
 # stream kernels; GDN/KDA: decode grid + fold grid), averaged over a 16-call
@@ -71,10 +71,10 @@ TRAFFIC_B64_FUSED = {
     ("mamba2", "bf16"): (15 * (0.756736e6 + 141.772032e6 + 3.569920e6)
                          + (0.940544e6 + 288.052224e6 + 345.972224e6)) / 16,
     # decode grid + fold grid; plain call at ring length 8, and the folding call
-    ("gdn", "bf16"): (15 * (77.419264e6 + 1.047808e6 + 0.051968e6)
-                      + (0.068352e6 + 152.905472e6 + 140.516864e6)) / 16,
-    ("kda", "bf16"): (15 * (86.723072e6 + 1.925376e6 + 0.050944e6)
-                      + (0.069632e6 + 170.604032e6 + 141.200640e6)) / 16,
+    ("gdn", "bf16"): (15 * (77.420032e6 + 1.021184e6 + 0.052736e6)
+                      + (0.068608e6 + 152.920832e6 + 140.507648e6)) / 16,
+    ("kda", "bf16"): (15 * (86.726656e6 + 1.957888e6 + 0.051200e6)
+                      + (0.070400e6 + 170.641920e6 + 141.317632e6)) / 16,
 }
 
 
