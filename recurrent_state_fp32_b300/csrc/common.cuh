@@ -285,12 +285,6 @@ __device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], uint32_t addr) {
                : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
                : "r"(addr));
 }
-// Two matrices (addresses from lanes 0-15).
-__device__ __forceinline__ void ldsm_x2(uint32_t (&r)[2], uint32_t addr) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0,%1}, [%2];"
-               : "=r"(r[0]), "=r"(r[1])
-               : "r"(addr));
-}
 // d += A B for a 16 x 16 BF16 A (row-major fragment a) and a 16 x 8 BF16 B
 // (column-major fragment b0, b1), FP32 accumulators: d[0..1] row g, d[2..3]
 // row g + 8, columns 2t and 2t + 1 (lane 4g + t).
