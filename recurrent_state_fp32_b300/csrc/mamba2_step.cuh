@@ -545,16 +545,17 @@ __global__ void __launch_bounds__(kStreamMaxThreads, 1) mamba2_step_stream_kerne
   }
   __syncthreads();
   // The block's units are done: one arrival per unit on its sequence's
-  // counter (one fence per thread); the last of a sequence's H * nrb
-  // arrivals moves its pointers.
+  // counter; the last of a sequence's H * nrb arrivals moves its pointers.
+  // No fence: the pointers the last arrival moves are read in this launch
+  // only from the block-start tables of blocks that hold units of that
+  // sequence (before their own arrivals); the rows and the appended entries
+  // only by later launches.
   if (!abort_flag && nloc > tid) {
-    __threadfence();
     for (int i = tid; i < nloc; i += blockDim.x) {
       const int code = table[i];
       if (!(code & 1)) continue;
       const int seq = (b0 + i * G0) / per_seq;
       if (atomicAdd(a.sync + seq, 1) + 1 == per_seq) {
-        __threadfence();
         const int l = (code >> 8) & 0xff, hd = (code >> 16) & 0xff;
         if (code & 2) {
           a.head[seq] = (hd + l) % W;
