@@ -8,10 +8,11 @@ replayssm_mamba2_decode computes but takes its scratch (the per-head workspace
 and the per-sequence arrival counters) from one fixed 16 MiB array inside the
 library, so state.work and state.sync may be NULL.
 
-The GPU test calls it through the C ABI twice in a row (the second call finds
-the array as the first left it) and checks each output, ring and pointer
+The GPU tests call it through the C ABI twice in a row (the second call finds
+the array as the first left it) and check each output, ring and pointer
 against replayssm_mamba2_decode on an identical state, with the tolerance of
-the other parity tests. The file's name makes pytest collect it last.
+the other parity tests; and run decodes through it alone against the oracle.
+The file's name makes pytest collect it last.
 """
 
 import ctypes
@@ -21,7 +22,7 @@ import pytest
 import torch
 
 import synth
-from gpu_harness import f32_close, host
+from gpu_harness import Session, f32_close, host
 from recurrent_state_fp32_b300 import _abi, api
 
 FAKE = 0x10000  # 16-byte aligned, never dereferenced
@@ -179,3 +180,34 @@ def test_matches_the_allocating_entry_point():
     size the array holds."""
     for case in ("ragged", "layer", "ragged", "boundary"):
         _compare(case)
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("read", ["f32", "bf16"])
+def test_against_the_oracle(read):
+    """Decodes through the allocation-free entry point alone (the caller's
+    scratch withheld), with consolidates between them, held to the oracle
+    like every other decode: outputs within the parity tolerance, ring and
+    pointers bit-exact, the checkpoint after a forced fold."""
+    wl = synth.Mamba2Workload(batch=5, heads=6, P=64, N=128, window=8, steps=20,
+                              in_dtype="bf16", seed=63)
+    s = Session("mamba2", wl, read)
+    for t in range(wl.steps):
+        s.consolidate(1)
+        tok = s.token(t)
+        g = s._to_dev(tok)
+        y = torch.full((wl.batch, wl.heads, wl.P), float("nan"), device="cuda")
+        c = _abi.State.from_buffer_copy(s.state.c())
+        c.work = None
+        c.sync = None
+        _abi.check("replayssm_mamba2_decode_noalloc", _abi.lib.replayssm_mamba2_decode_noalloc(
+            ctypes.byref(s.dims.c()), ctypes.byref(c), s.dA.data_ptr(), s.dD.data_ptr(),
+            g["x"].data_ptr(), g["B"].data_ptr(), g["C"].data_ptr(), g["dt"].data_ptr(),
+            y.data_ptr(), None))
+        ref = s.oracle.decode(s._sub(tok))
+        torch.cuda.synchronize()
+        s.compare_out(host(y)[s.seqs][:, s.heads], ref, f"token {t}")
+        s.check_pointers(f"token {t}")
+        s.check_ring(f"token {t}")
+    s.consolidate(1, force=True)
+    s.check_checkpoint("after forced fold")
