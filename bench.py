@@ -499,7 +499,8 @@ def decode_record(layer, read, K, Wm, stream, world, stagger=False):
         },
         "gpu_launches": K * layer.step_launches(),
         "device_status_ok": bad == 0,
-        "calls": call_stats(dec_ms, gaps_us, layer.fold_steps(lens0, K)),
+        "calls": call_stats(dec_ms, gaps_us, layer.fold_steps(lens0, K), wl["window"],
+                            wl["batch"] * world),
     }
 
 
@@ -664,17 +665,28 @@ def layer_bytes(layer):
     return n + sum(t.numel() * t.element_size() for t in st.ring.values())
 
 
-def call_stats(dec_ms, gaps_us, folds):
+def call_stats(dec_ms, gaps_us, folds, window=None, tokens_per_call=None):
     """Per-call device times of the timed steps: the median of the calls that
     fold nothing, the mean of those that fold, and the median idle gap on the
     device between one call's end and the next call's start (host-bound
-    stretches show up there)."""
+    stretches show up there).
+
+    With both kinds of call present (lockstep ring phases), also the steady
+    state of one fold cycle, which does not depend on how many folds the
+    timed window happens to hold: window - 1 plain calls and one folding
+    call per cycle, each followed by the median gap."""
     plain = [1e3 * t for t, f in zip(dec_ms, folds) if not f]
     fold = [1e3 * t for t, f in zip(dec_ms, folds) if f]
-    return {"plain_call_us_median": round(statistics.median(plain), 2) if plain else None,
-            "fold_call_us": round(sum(fold) / len(fold), 2) if fold else None,
-            "fold_calls": len(fold),
-            "host_gap_us_median": round(statistics.median(gaps_us), 2) if gaps_us else None}
+    gap = statistics.median(gaps_us) if gaps_us else None
+    out = {"plain_call_us_median": round(statistics.median(plain), 2) if plain else None,
+           "fold_call_us": round(sum(fold) / len(fold), 2) if fold else None,
+           "fold_calls": len(fold),
+           "host_gap_us_median": round(gap, 2) if gap is not None else None}
+    if plain and fold and window and tokens_per_call:
+        cycle = ((window - 1) * statistics.median(plain) + sum(fold) / len(fold)) / window
+        out["cycle_call_us"] = round(cycle, 2)
+        out["cycle_tokens_per_s"] = round(tokens_per_call / ((cycle + (gap or 0.0)) * 1e-6), 1)
+    return out
 
 
 def run_ab(layer, K, Wm, stream, world):

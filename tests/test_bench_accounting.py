@@ -93,3 +93,22 @@ def test_staggered_phases_move_the_same_bytes():
     L2.out = torch.zeros((W,) + tuple(L.out.shape[1:]))
     stag = L2.account(W - np.arange(W), W)
     assert np.isclose(sum(stag) / (W * W), sum(lock) / (B * W))
+
+
+def test_fold_cycle_rate():
+    """The steady state of one fold cycle: W - 1 plain calls and one folding
+    call, each followed by the median gap, whatever share of folds the timed
+    window held."""
+    W, tokens = 16, 256
+    dec_ms = [0.100, 0.102, 0.400, 0.098, 0.100, 0.101, 0.099, 0.100]
+    folds = [False, False, True, False, False, False, False, False]
+    gaps = [2.0, 3.0, 2.0, 2.5, 2.0, 4.0, 2.0]
+    st = bench.call_stats(dec_ms, gaps, folds, W, tokens)
+    assert st["plain_call_us_median"] == 100.0 and st["fold_call_us"] == 400.0
+    assert st["fold_calls"] == 1 and st["host_gap_us_median"] == 2.0
+    cycle = (15 * 100.0 + 400.0) / 16
+    assert st["cycle_call_us"] == round(cycle, 2)
+    assert st["cycle_tokens_per_s"] == round(tokens / ((cycle + 2.0) * 1e-6), 1)
+    # every call folds (staggered phases) or none does: no cycle figure
+    assert "cycle_call_us" not in bench.call_stats(dec_ms, gaps, [True] * 8, W, tokens)
+    assert "cycle_call_us" not in bench.call_stats(dec_ms, gaps, [False] * 8, W, tokens)
