@@ -1704,14 +1704,20 @@ FusedConfig fused_config(int RB, int DK, int DV, int W, int K, int GU, bool kda,
   return best;
 }
 
-// Decode (K = 1) from the BF16 read copy: the prep warps' sweeps bound the
-// call, so the configuration with the most prep warps wins, one consumer
-// warp per unit (GU = 1) where that frees warps for them, then the most
-// state stages, then depth 1. Measured on the b256 layers: GDN 8 prep warps
-// at depth 1 with 8 stages 61 us per call, 7 at depth 2 with 4 stages 67 us;
-// KDA 8 at depth 1 80 us, 4 at depth 2 84 us. Zero NP: nothing fits.
+// Decode (K = 1) from the BF16 read copy. A configuration scores its prep
+// warps plus its consumer warps per group (GU): a second consumer warp per
+// group counts as much as a prep warp, and ties go to GU = 2, then to more
+// state stages, then to depth 1. The prep warps' sweeps set the pace, but a
+// consumer group also holds its stages while it computes; with KDA's larger
+// prep stages only four state stages fit (one per group), and halving the
+// group's time per unit is what keeps the stream going. Measured per call on
+// the b256 layers: KDA 7 prep warps at GU = 2 70-73 us against 80 us with 8
+// at GU = 1 (101 against 108 us per fused step); GDN 59.3 us either way (8
+// stages); GDN 9 prep warps at GU = 1 61.3 us against 60.8 us with 8, and 10
+// or 11 leave room for only 4 stages, 74 us. Zero NP: nothing fits.
 FusedConfig decode_config(int RB, int DK, int DV, int W, bool kda, int ti, size_t optin, int& GU) {
   FusedConfig best{0, 0, 0, 0, 0};
+  int best_gu = 0;
   const int gu_first = RB % 64 == 0 ? 2 : 1;
   for (int gu = gu_first; gu >= 1; --gu) {
     if (RB / gu > 128) continue;
@@ -1724,15 +1730,20 @@ FusedConfig decode_config(int RB, int DK, int DV, int W, bool kda, int ti, size_
         if (fixed >= optin) continue;
         const int NS = std::min((int)((optin - fixed) / (L0.stage + 16)), 12) / kFGroups * kFGroups;
         if (NS < min_stages(2)) continue;
-        const bool better = NP > best.NP || (NP == best.NP && (NS > best.NS || (NS == best.NS && depth < best.depth)));
+        const int score = NP + gu, best_score = best.NP + best_gu;
+        const bool better =
+            score > best_score ||
+            (score == best_score && gu == best_gu &&
+             (NS > best.NS || (NS == best.NS && depth < best.depth)));
         if (better) {
           best = FusedConfig{NS, NSL, NP, depth, DFusedSmem(RB, DK, DV, W, 1, NS, NSL, NP, depth, kda, 2, ti).total};
-          GU = gu;
+          best_gu = gu;
         }
         break;  // fewer prep warps at this depth only lose
       }
     }
   }
+  if (best.NP > 0) GU = best_gu;
   return best;
 }
 
