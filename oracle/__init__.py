@@ -10,18 +10,18 @@ this package imports nothing from the CUDA package.
 Sources (cited by page title and section throughout):
 
 * "ReplaySSM: o ganho aparece na carga concorrente, não no nome da
-  otimização" (fagnersouza.tech) -- intro (state = checkpoint + buffer of
+  otimização" -- intro (state = checkpoint + buffer of
   recent inputs), "Cuidados e limites" (outputs equal conventional decoding
   up to floating point; low-precision reads separated from the
   higher-precision recurrence), "O que muda para quem desenvolve" (W = 16,
   FP32 state; speculative acceptance by moving a pointer).
 * "NVIDIA y Princeton aceleran modelos híbridos al guardar entradas recientes
-  en lugar del estado completo" (ia.goatify.app) -- paragraph 2 (append to the
+  en lugar del estado completo" -- paragraph 2 (append to the
   buffer, output from the checkpoint, consolidate only when the buffer is
   full), paragraph 3 (rollback by a buffer pointer, no per-draft snapshot),
   paragraph 4 (high-precision checkpoint, lower-precision read copy).
 * "NVIDIA présente ReplaySSM : accélérer le décodage des modèles hybrides
-  Mamba et GDN" (news.hamidun.com) -- "Pourquoi les hybrides sont devenus la
+  Mamba et GDN" -- "Pourquoi les hybrides sont devenus la
   norme" names the three layer types (Mamba-2, Gated DeltaNet, Kimi Delta
   Attention), whose standard decode recurrences are restated here.
 

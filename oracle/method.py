@@ -17,7 +17,8 @@ readings are listed with their reasons in the design notes):
 * consolidate(k_next, force): a sequence folds when len + k_next > W, or when
   force is set and len > 0. Folding moves the checkpoint to the committed
   position (head += len mod W, len = 0). Folding only when the buffer would
-  overflow follows paragraph 2 of the goatify page.
+  overflow follows paragraph 2 of "NVIDIA y Princeton aceleran modelos
+  híbridos…".
 * accept(m): len += m for 0 <= m <= K and len + m <= W, else a status bit;
   nothing else moves (paragraph 3: rollback by a pointer, no per-draft copy).
 * outputs are those of conventional decoding (section "Cuidados e limites"),
