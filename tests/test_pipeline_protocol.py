@@ -1,0 +1,183 @@
+"""The mbarrier protocol of the persistent decode kernels, on the CPU.
+
+An mbarrier keeps only the parity of its phase. A wait for the completion of
+phase n (parity n % 2) passes whenever the barrier's count of completed
+phases c has c % 2 != n % 2: at c = n + 1 as intended, but also at
+c = n - 1, while phase n - 1 is still in progress. The kernels therefore
+rely on two ownership rules, stated in their sources:
+
+* state stages (stream, fused-step and delta kernels): unit u goes to stage
+  u mod NS and to consumer group u mod G, and NS is a multiple of G, so each
+  stage serves one group only and that group waits for a stage's next fill
+  only after consuming its previous one;
+* vector slots of the delta kernel: prep warp w writes the slots of heads
+  w, w + NP, ... (slot li mod NSL), consumer group g takes units
+  g, g + G, ... (head = unit // nrb); NSL is a multiple of NP and NSL * nrb
+  a multiple of G, so every fill of a slot comes from one warp, in order, and
+  every group consumes every fill of each slot it uses.
+
+This file runs both protocols, wait for wait and arrival for arrival as the
+kernels issue them, under many random interleavings (copies landing late,
+warps running ahead), and checks that nobody reads a fill meant for another
+unit or head and that no fill overwrites data still being read. A mutant of
+each rule (11 stages for 4 groups; slot counts that break either multiple)
+must fail the same check.
+"""
+
+import random
+
+import pytest
+
+
+class Barrier:
+    """Completed-phase count of one mbarrier with `count` arrivals per phase."""
+
+    def __init__(self, count=1):
+        self.count, self.pending, self.c = count, count, 0
+
+    def passes(self, parity):
+        return self.c % 2 != parity
+
+    def arrive(self):
+        self.pending -= 1
+        if self.pending == 0:
+            self.c += 1
+            self.pending = self.count
+
+
+def run_stages(NS, G, U, seed):
+    """Producer, copies in flight and G consumer groups over U units; returns
+    the violations seen (reads of another unit's fill, overwrites of a fill
+    not yet released)."""
+    rng = random.Random(seed)
+    full = [Barrier() for _ in range(NS)]
+    empty = [Barrier() for _ in range(NS)]
+    content = [None] * NS          # unit whose rows a stage holds
+    released = [True] * NS         # the consumer of `content` has released it
+    in_flight = []                 # (stage, unit) copies issued, not landed
+    nxt_p = 0                      # producer's next unit
+    nxt_c = list(range(G))         # each group's next unit
+    weight = [rng.uniform(0.05, 1.0) for _ in range(G + 2)]
+    bad = []
+    while nxt_p < U or in_flight or any(u < U for u in nxt_c):
+        acts = []
+        if nxt_p < U:
+            u, s = nxt_p, nxt_p % NS
+            n = u // NS
+            if n == 0 or empty[s].passes((n - 1) & 1):
+                acts.append(("issue", weight[G]))
+        if in_flight:
+            acts.append(("land", weight[G + 1]))
+        for g in range(G):
+            u = nxt_c[g]
+            if u < U and full[u % NS].passes((u // NS) & 1):
+                acts.append((g, weight[g]))
+        if not acts:
+            return bad + ["deadlock"]
+        act = rng.choices([a for a, _ in acts], [w for _, w in acts])[0]
+        if act == "issue":
+            in_flight.append((nxt_p % NS, nxt_p))
+            nxt_p += 1
+        elif act == "land":
+            s, u = in_flight.pop(rng.randrange(len(in_flight)))
+            if not released[s]:
+                bad.append(f"unit {u} overwrote stage {s} (unit {content[s]}) before release")
+            content[s], released[s] = u, False
+            full[s].arrive()
+        else:
+            g, u = act, nxt_c[act]
+            s = u % NS
+            if content[s] != u:
+                bad.append(f"group {g} read unit {content[s]} for unit {u} from stage {s}")
+            released[s] = True
+            empty[s].arrive()
+            nxt_c[g] += G
+    return bad
+
+
+def run_slots(NP, NSL, nrb, G, heads, seed):
+    """NP prep warps filling NSL vector slots and G consumer groups reading
+    them (nrb units per head); returns the violations seen."""
+    rng = random.Random(seed)
+    vfull = [Barrier() for _ in range(NSL)]
+    vempty = [Barrier(nrb) for _ in range(NSL)]
+    content = [None] * NSL
+    readers_left = [0] * NSL       # units of `content` not yet consumed
+    nxt_w = list(range(NP))        # each prep warp's next head
+    nxt_c = list(range(G))         # each group's next unit
+    U = heads * nrb
+    weight = [rng.uniform(0.05, 1.0) for _ in range(NP + G)]
+    bad = []
+    while any(h < heads for h in nxt_w) or any(u < U for u in nxt_c):
+        acts = []
+        for w in range(NP):
+            li = nxt_w[w]
+            if li < heads and (li < NSL or vempty[li % NSL].passes(((li // NSL) - 1) & 1)):
+                acts.append((("prep", w), weight[w]))
+        for g in range(G):
+            u = nxt_c[g]
+            if u < U:
+                li = u // nrb
+                if vfull[li % NSL].passes((li // NSL) & 1):
+                    acts.append((("cons", g), weight[NP + g]))
+        if not acts:
+            return bad + ["deadlock"]
+        (kind, i) = rng.choices([a for a, _ in acts], [w for _, w in acts])[0]
+        if kind == "prep":
+            li = nxt_w[i]
+            s = li % NSL
+            if readers_left[s]:
+                bad.append(f"warp {i} wrote head {li} over head {content[s]} in slot {s}")
+            content[s], readers_left[s] = li, nrb
+            vfull[s].arrive()
+            nxt_w[i] += NP
+        else:
+            u = nxt_c[i]
+            li = u // nrb
+            s = li % NSL
+            if content[s] != li:
+                bad.append(f"group {i} read head {content[s]} for head {li} from slot {s}")
+            else:
+                readers_left[s] -= 1
+            vempty[s].arrive()
+            nxt_c[i] += G
+    return bad
+
+
+def slot_rule(NP, nrb, G=4, cap=16):
+    """Vector slots as the delta kernel sizes them: at least NP + 4, a
+    multiple of NP, with NSL * nrb a multiple of G; 0 if none up to cap."""
+    for nsl in range(NP + 4, cap + 1):
+        if nsl % NP == 0 and (nsl * nrb) % G == 0:
+            return nsl
+    return 0
+
+
+@pytest.mark.parametrize("NS", [4, 8, 12])
+def test_owned_stages_hold(NS):
+    for seed in range(60):
+        assert run_stages(NS, 4, 90, seed) == [], (NS, seed)
+
+
+def test_stages_shared_by_groups_are_caught():
+    """11 stages for 4 groups: a stage's consecutive fills go to different
+    groups, and some interleaving lets a group pass a parity wait on a fill
+    that is not its own (the fault the ownership rule was made for)."""
+    assert any(run_stages(11, 4, 90, seed) for seed in range(200))
+
+
+@pytest.mark.parametrize("NP,nrb", [(8, 2), (7, 2), (6, 2), (4, 1), (6, 3), (5, 2), (1, 1)])
+def test_vector_slot_rule_holds(NP, nrb):
+    NSL = slot_rule(NP, nrb)
+    assert NSL, (NP, nrb)
+    for seed in range(60):
+        assert run_slots(NP, NSL, nrb, 4, 3 * NSL + 5, seed) == [], (NP, nrb, NSL, seed)
+
+
+@pytest.mark.parametrize("NP,NSL,nrb", [
+    (3, 8, 1),   # NSL not a multiple of NP: one slot's fills from several warps
+    (5, 12, 1),  # the same
+    (4, 6, 1),   # NSL * nrb not a multiple of the groups: fills skip a group
+])
+def test_vector_slot_mutants_are_caught(NP, NSL, nrb):
+    assert any(run_slots(NP, NSL, nrb, 4, 3 * NSL + 5, seed) for seed in range(300))
