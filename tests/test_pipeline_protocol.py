@@ -6,10 +6,11 @@ phases c has c % 2 != n % 2: at c = n + 1 as intended, but also at
 c = n - 1, while phase n - 1 is still in progress. The kernels therefore
 rely on two ownership rules, stated in their sources:
 
-* state stages (stream, fused-step and delta kernels): unit u goes to stage
-  u mod NS and to consumer group u mod G, and NS is a multiple of G, so each
-  stage serves one group only and that group waits for a stage's next fill
-  only after consuming its previous one;
+* state stages (stream and delta kernels): unit u goes to stage u mod NS and
+  to consumer group u mod G, and NS is a multiple of G, so each stage serves
+  one group only and that group waits for a stage's next fill only after
+  consuming its previous one (the fused Mamba-2 step gives each group its
+  own ring of NS / G stages outright, which is the same rule);
 * vector slots of the delta kernel: prep warp w writes the slots of heads
   w, w + NP, ... (slot li mod NSL), consumer group g takes units
   g, g + G, ... (head = unit // nrb); NSL is a multiple of NP and NSL * nrb
