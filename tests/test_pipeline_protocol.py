@@ -15,7 +15,11 @@ rely on two ownership rules, stated in their sources:
   w, w + NP, ... (slot li mod NSL), consumer group g takes units
   g, g + G, ... (head = unit // nrb); NSL is a multiple of NP and NSL * nrb
   a multiple of G, so every fill of a slot comes from one warp, in order, and
-  every group consumes every fill of each slot it uses.
+  every group consumes every fill of each slot it uses. The tensor-core
+  verify kernel's prep stages follow the same scheme: head li goes to warp
+  li mod NP and to that warp's stage (li / NP) mod depth, that is, to slot
+  li mod (NP * depth) of a warp's own, and its configurations keep
+  NP * depth * nrb a multiple of G.
 
 This file runs both protocols, wait for wait and arrival for arrival as the
 kernels issue them, under many random interleavings (copies landing late,
@@ -182,3 +186,24 @@ def test_vector_slot_rule_holds(NP, nrb):
 ])
 def test_vector_slot_mutants_are_caught(NP, NSL, nrb):
     assert any(run_slots(NP, NSL, nrb, 4, 3 * NSL + 5, seed) for seed in range(300))
+
+
+# (prep warps, depth) candidates of the tensor-core verify kernel
+GRAM_CANDIDATES = [(7, 2), (6, 2), (4, 3), (4, 2), (2, 4), (6, 1), (3, 2), (2, 2), (4, 1), (2, 1)]
+
+
+@pytest.mark.parametrize("NP,depth", GRAM_CANDIDATES)
+def test_tensor_core_prep_stages_hold(NP, depth):
+    """Every candidate at every row-block count its rule admits."""
+    for nrb in (1, 2, 3):
+        if (NP * depth * nrb) % 4:
+            continue
+        for seed in range(40):
+            assert run_slots(NP, NP * depth, nrb, 4, 3 * NP * depth + 5, seed) == [], \
+                (NP, depth, nrb, seed)
+
+
+@pytest.mark.parametrize("NP,depth,nrb", [(7, 2, 1), (6, 1, 1), (3, 2, 1)])
+def test_tensor_core_prep_stage_mutants_are_caught(NP, depth, nrb):
+    """Configurations the rule excludes: some interleaving breaks them."""
+    assert any(run_slots(NP, NP * depth, nrb, 4, 3 * NP * depth + 5, seed) for seed in range(300))
