@@ -21,12 +21,18 @@ rely on two ownership rules, stated in their sources:
   li mod (NP * depth) of a warp's own, and its configurations keep
   NP * depth * nrb a multiple of G.
 
-This file runs both protocols, wait for wait and arrival for arrival as the
+The fused Mamba-2 step's rings add two details: a fold unit takes FS
+consecutive stages of its group's ring (the second one, past the ring's end,
+waits for the flipped parity), and the launch requires at least FS stages
+per group.
+
+This file runs these protocols, wait for wait and arrival for arrival as the
 kernels issue them, under many random interleavings (copies landing late,
 warps running ahead), and checks that nobody reads a fill meant for another
-unit or head and that no fill overwrites data still being read. A mutant of
-each rule (11 stages for 4 groups; slot counts that break either multiple)
-must fail the same check.
+unit or head, that no fill overwrites data still being read and that nothing
+deadlocks. A mutant of each rule (11 stages for 4 groups; slot counts that
+break either multiple; a ring shorter than a fold unit; no parity flip for a
+fold unit's wrapped second stage) must fail the same check.
 """
 
 import random
@@ -207,3 +213,100 @@ def test_tensor_core_prep_stages_hold(NP, depth):
 def test_tensor_core_prep_stage_mutants_are_caught(NP, depth, nrb):
     """Configurations the rule excludes: some interleaving breaks them."""
     assert any(run_slots(NP, NP * depth, nrb, 4, 3 * NP * depth + 5, seed) for seed in range(300))
+
+
+def run_group_rings(R, FS, G, U, seed, fold_share=0.3, flip_on_wrap=True):
+    """The fused Mamba-2 step: each of G consumer groups owns a ring of R
+    stages; a decode unit takes the next stage of its group's ring, a fold
+    unit the next FS (the second of them, past the ring's end, waits for the
+    flipped parity). The producer serves whichever group's next stage is
+    free. Returns the violations seen ("deadlock" if no actor can move)."""
+    rng = random.Random(seed)
+    NS = G * R
+    fold = [rng.random() < fold_share for _ in range(U)]
+    full = [Barrier() for _ in range(NS)]
+    empty = [Barrier() for _ in range(NS)]
+    content = [None] * NS
+    released = [True] * NS
+    in_flight = []
+    # producer, per group: next unit, stages of it issued, ring position,
+    # parity of that position's fill, whether the ring has wrapped
+    p_nxt, p_f, p_t, p_ph, p_reuse = list(range(G)), [0] * G, [0] * G, [0] * G, [False] * G
+    # consumers, per group: next unit, ring position, parity
+    c_nxt, c_t, c_ph = list(range(G)), [0] * G, [0] * G
+    weight = [rng.uniform(0.05, 1.0) for _ in range(2 * G + 1)]
+    bad = []
+    while any(i < U for i in p_nxt) or in_flight or any(i < U for i in c_nxt):
+        acts = []
+        for g in range(G):
+            if p_nxt[g] < U:
+                s = g * R + p_t[g]
+                if not p_reuse[g] or empty[s].passes(p_ph[g] ^ 1):
+                    acts.append((("issue", g), weight[g]))
+            i = c_nxt[g]
+            if i < U:
+                s0, ph0 = g * R + c_t[g], c_ph[g]
+                wrap = c_t[g] + 1 == R
+                s1 = g * R + (0 if wrap else c_t[g] + 1)
+                ph1 = c_ph[g] ^ 1 if (wrap and flip_on_wrap) else c_ph[g]
+                two = fold[i] and FS > 1
+                if full[s0].passes(ph0) and (not two or full[s1].passes(ph1)):
+                    acts.append((("consume", g), weight[G + g]))
+        if in_flight:
+            acts.append((("land", 0), weight[2 * G]))
+        if not acts:
+            return bad + ["deadlock"]
+        kind, g = rng.choices([a for a, _ in acts], [w for _, w in acts])[0]
+        if kind == "issue":
+            i, s = p_nxt[g], g * R + p_t[g]
+            in_flight.append((s, (i, p_f[g])))
+            p_t[g] += 1
+            if p_t[g] == R:
+                p_t[g], p_ph[g], p_reuse[g] = 0, p_ph[g] ^ 1, True
+            p_f[g] += 1
+            if p_f[g] == (FS if fold[i] else 1):
+                p_f[g] = 0
+                p_nxt[g] += G
+        elif kind == "land":
+            s, what = in_flight.pop(rng.randrange(len(in_flight)))
+            if not released[s]:
+                bad.append(f"{what} overwrote stage {s} ({content[s]}) before release")
+            content[s], released[s] = what, False
+            full[s].arrive()
+        else:
+            i = c_nxt[g]
+            stages = []
+            for f in range(FS if fold[i] else 1):
+                stages.append(g * R + c_t[g])
+                c_t[g] += 1
+                if c_t[g] == R:
+                    c_t[g], c_ph[g] = 0, c_ph[g] ^ 1
+            for f, s in enumerate(stages):
+                if content[s] != (i, f):
+                    bad.append(f"group {g} read {content[s]} for {(i, f)} from stage {s}")
+            for s in stages:
+                released[s] = True
+                empty[s].arrive()
+            c_nxt[g] += G
+    return bad
+
+
+@pytest.mark.parametrize("R,FS", [(1, 1), (2, 1), (3, 1), (2, 2), (3, 2), (5, 2)])
+def test_fused_step_group_rings_hold(R, FS):
+    """Rings of at least FS stages per group (the launch requires
+    NS >= 4 * FS), decode and fold units mixed at random."""
+    for seed in range(60):
+        assert run_group_rings(R, FS, 4, 80, seed) == [], (R, FS, seed)
+
+
+def test_fused_step_ring_shorter_than_a_fold_unit_is_caught():
+    """One stage per group with two-stage fold units: the group would need
+    both fills of its single stage at once."""
+    assert any(run_group_rings(1, 2, 4, 80, seed) for seed in range(50))
+
+
+def test_fused_step_second_stage_parity_is_needed():
+    """A fold unit whose second stage lies past the ring's end must wait for
+    the flipped parity; waiting for the first stage's parity passes on the
+    previous fill of that stage."""
+    assert any(run_group_rings(3, 2, 4, 80, seed, flip_on_wrap=False) for seed in range(200))
