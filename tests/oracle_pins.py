@@ -572,9 +572,25 @@ def pin_status_and_refusal():
 
 
 def pin_bf16_rounding():
-    """Round-to-nearest-even bfloat16 on hand-checked values (worked_examples.json)."""
+    """Round-to-nearest-even bfloat16 on hand-checked values (worked_examples.json),
+    and bit for bit against torch's float32 -> bfloat16 conversion (also
+    round to nearest, ties to even) on random values, exact ties of both
+    parities, values just either side of a tie, and signed zeros and
+    subnormals."""
+    import torch
+
     g = _golden("worked_examples.json")["bf16_rne"]
     _close(om.bf16_rne(np.array(g["in"], np.float32)), g["out"], 0.0, "bf16 RNE")
+    r = _rng(57)
+    bits = r.integers(0, 0x7F800000, 4000, dtype=np.int64)       # finite, positive
+    ties = (bits & ~0xFFFF) | 0x8000                               # halfway cases
+    near = np.concatenate([ties - 1, ties + 1])
+    sub = r.integers(1, 0x00800000, 200, dtype=np.int64)           # subnormals
+    u = np.concatenate([bits, ties, near, sub, [0]]).astype(np.uint32)
+    f = np.concatenate([u, u | 0x80000000]).astype(np.uint32).view(np.float32)
+    want = torch.from_numpy(f.copy()).to(torch.bfloat16).to(torch.float32).numpy()
+    got = om.bf16_rne(f).astype(np.float32)
+    assert np.array_equal(got.view(np.uint32), want.view(np.uint32)), "bf16 RNE vs torch"
 
 
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

@@ -203,6 +203,19 @@ def copy_without_pointers(self, src, dst):
         arr[dst] = arr[src].copy()
 
 
+def bf16_truncate(a):
+    """Rounds toward zero (drops the low 16 bits)."""
+    u = np.ascontiguousarray(a, dtype=np.float32).view(np.uint32) & np.uint32(0xFFFF0000)
+    return u.view(np.float32).astype(np.float64)
+
+
+def bf16_ties_away(a):
+    """Rounds half away from zero instead of to even."""
+    u = np.ascontiguousarray(a, dtype=np.float32).view(np.uint32).astype(np.int64)
+    u = ((u + 0x8000) >> 16) << 16
+    return (u & 0xFFFFFFFF).astype(np.uint32).view(np.float32).astype(np.float64)
+
+
 MUTANTS = [
     (rec, "mamba2_step", m2_no_skip),
     (rec, "mamba2_step", m2_old_state_output),
@@ -228,6 +241,8 @@ MUTANTS = [
     (om.ReplayOracle, "accept", accept_clamps_silently),
     (om.ReplayOracle, "copy_sequences", copy_without_ring),
     (om.ReplayOracle, "copy_sequences", copy_without_pointers),
+    (om, "bf16_rne", bf16_truncate),
+    (om, "bf16_rne", bf16_ties_away),
 ]
 
 
