@@ -78,14 +78,35 @@ TRAFFIC_B64_FUSED = {
 }
 
 
+# Captures whose kernels changed afterwards. Their figures are no longer
+# reported as the call's traffic; the record carries them beside it, with
+# the change, until the kernels are captured again.
+_DECODE_CONFIG_CHANGE = ("the decode grid's launch configuration changed after this capture "
+                         "(two consumer warps per group and 7 prep warps instead of one and 8); "
+                         "the kernel code and the bytes each unit moves did not")
+TRAFFIC_STALE = {
+    ("mamba2", "bf16", True): ("the step stream kernel's block-end arrivals lost their fence after "
+                               "this capture; no memory access of the kernel changed"),
+    ("gdn", "bf16", True): _DECODE_CONFIG_CHANGE,
+    ("kda", "bf16", True): _DECODE_CONFIG_CHANGE,
+    ("gdn", "bf16", False): _DECODE_CONFIG_CHANGE,
+}
+
+
 def traffic_per_call(wl: dict, read: str, fused: bool):
-    """DRAM bytes of one decode call at this batch, from the batch-64 captures
-    (None for kernels or shapes without one)."""
+    """DRAM bytes of one decode call at this batch from the batch-64 captures,
+    as the roofline record's keys: {"traffic": bytes} for a kernel unchanged
+    since its capture; {"traffic": None, "traffic_last_capture": {...}} for
+    one changed since; {"traffic": None} without a capture."""
     table = TRAFFIC_B64_FUSED if fused else TRAFFIC_B64
     key = (wl["kind"], read)
     if key not in table or wl["heads"] != WORKLOADS[wl["kind"]]["heads"]:
-        return None
-    return round(table[key] * wl["batch"] / 64)
+        return {"traffic": None}
+    t = round(table[key] * wl["batch"] / 64)
+    stale = TRAFFIC_STALE.get(key + (fused,))
+    if stale:
+        return {"traffic": None, "traffic_last_capture": {"bytes": t, "changed_since": stale}}
+    return {"traffic": t}
 
 
 def parse(argv=None):
@@ -493,7 +514,7 @@ def decode_record(layer, read, K, Wm, stream, world, stagger=False):
             "kernel": layer.decode_kernels(), "bound": "hbm", "achieved": round(achieved, 1),
             "peak": peak, "peak_source": peak_kind, "unit": "GB/s",
             "frac": round(achieved / peak, 4),
-            "traffic": traffic_per_call(wl, read, layer.fused),
+            **traffic_per_call(wl, read, layer.fused),
             "bytes_per_launch": int(call_bytes / K),
             "avg_launch_us": round(1e3 * sum(dec_ms) / K, 3),
         },

@@ -112,3 +112,21 @@ def test_fold_cycle_rate():
     # every call folds (staggered phases) or none does: no cycle figure
     assert "cycle_call_us" not in bench.call_stats(dec_ms, gaps, [True] * 8, W, tokens)
     assert "cycle_call_us" not in bench.call_stats(dec_ms, gaps, [False] * 8, W, tokens)
+
+
+def test_traffic_of_changed_kernels_is_not_reported_as_current():
+    """A capture taken before its kernel changed is reported beside the
+    roofline's traffic, never as it; unchanged captures scale with the batch."""
+    for (kind, read, fused), why in bench.TRAFFIC_STALE.items():
+        wl = dict(bench.WORKLOADS[kind])
+        rec = bench.traffic_per_call(wl, read, fused)
+        assert rec["traffic"] is None
+        table = bench.TRAFFIC_B64_FUSED if fused else bench.TRAFFIC_B64
+        assert rec["traffic_last_capture"]["bytes"] == round(table[(kind, read)] * wl["batch"] / 64)
+        assert rec["traffic_last_capture"]["changed_since"] == why
+    wl = dict(bench.WORKLOADS["mamba2"])
+    cur = bench.traffic_per_call(wl, "bf16", False)
+    assert set(cur) == {"traffic"} and cur["traffic"] == round(bench.TRAFFIC_B64[("mamba2", "bf16")] * wl["batch"] / 64)
+    wl["batch"] = 128
+    assert bench.traffic_per_call(wl, "bf16", False)["traffic"] == round(bench.TRAFFIC_B64[("mamba2", "bf16")] * 2)
+    assert bench.traffic_per_call(dict(bench.WORKLOADS["kda"]), "bf16", False) == {"traffic": None}
