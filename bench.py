@@ -1142,6 +1142,9 @@ def run_reference(args, rank, world):
         "value": round(value, 4), "unit": unit,
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(1e3 * dt / args.steps, 4), "higher_is_better": True,
+        # ms_per_step is per sampled step (one sequence, a slice of its heads);
+        # a whole step or round of the workload is batch / frac of them
+        "ms_per_workload_step": round(1e3 * dt / args.steps * wl["batch"] / frac, 1),
         "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded; no weights or datasets)",
         "config": dict(spec_config(wl, args.read, world) if spec else

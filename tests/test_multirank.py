@@ -79,3 +79,7 @@ def test_reference_arm_under_torchrun_two_ranks():
     d = lines[0]
     assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["steps"] == 3
     assert d["cpu_baseline"]["kind"] == "oracle" and d["e2e"]["h2d_bytes_per_step"] == 0
+    # a whole step of the workload is batch / (sampled fraction) sampled steps
+    frac = 8 / 128  # one sequence, 8 of the layer's 128 heads per sampled step
+    assert abs(d["ms_per_workload_step"] - d["ms_per_step"] * 256 / frac) <= 0.05 * d["ms_per_workload_step"]
+    assert abs(d["ms_per_workload_step"] - 1e3 * 256 / d["value"]) <= 0.01 * d["ms_per_workload_step"]
