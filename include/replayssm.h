@@ -338,7 +338,7 @@ REPLAYSSM_API replayssm_status replayssm_conventional_accept(const replayssm_dim
 
 /*
  * Mamba-2 replay decode that allocates nothing and needs no caller scratch.
- * The paper has no counterpart: this is a library convenience.
+ * The pages have no counterpart: this is a library convenience.
  *
  * Some callers cannot allocate device memory when they decode: a plugin or
  * custom operator whose host framework owns all device memory and allows no
@@ -381,7 +381,7 @@ REPLAYSSM_API replayssm_status replayssm_mamba2_decode_noalloc(
  * Bytes of the fixed scratch that replayssm_mamba2_decode_noalloc needs for
  * these sizes (the formula above), so a caller can check the limit before
  * it calls; 0 if dims is invalid or not a Mamba-2 layer. Host only, no CUDA
- * call. The paper has no counterpart: a library convenience.
+ * call. The pages have no counterpart: a library convenience.
  */
 REPLAYSSM_API int64_t replayssm_mamba2_decode_noalloc_bytes(const replayssm_dims* dims);
 
@@ -419,6 +419,41 @@ REPLAYSSM_API replayssm_status replayssm_selftest_wait_timeout(int32_t* status, 
  * calls with up to K drafts on the given sizes (0 if dims is invalid).
  */
 REPLAYSSM_API int64_t replayssm_workspace_bytes(const replayssm_dims* dims, int32_t K);
+
+/*
+ * Launch configuration of the persistent delta-rule kernel (GDN or KDA) that
+ * replayssm_gdn_decode and the decode grid of replayssm_gdn_fold_decode
+ * (K = 1) or replayssm_spec_verify (K drafts) would run for these sizes, on
+ * a device whose blocks may use smem_limit bytes of shared memory (0: the
+ * B300's 232,448). read_copy: 1 when the state has a BF16 read copy. Host
+ * only, no CUDA call. It assumes the CUDA driver provides the tensor-map
+ * encoder the tensor-core kernel needs; without it that kernel's calls run
+ * the FFMA kernel instead. The pages have no counterpart: it reports how
+ * the library lays one block out (prep warps staging heads, consumer groups
+ * streaming state stages, the slots between them) so that the pipeline's
+ * ownership rules can be checked without a GPU.
+ * Returns REPLAYSSM_OK and fills *out; REPLAYSSM_ERR_INVALID_ARG for a NULL
+ * pointer, invalid dims, a Mamba-2 layer, K outside [1, 8] or a negative
+ * smem_limit; REPLAYSSM_ERR_UNSUPPORTED when no configuration fits.
+ */
+typedef struct replayssm_delta_config {
+  int32_t tensor_cores;             /* 1: tensor-core verify kernel, 0: FFMA kernel */
+  int32_t prep_warps;               /* NP */
+  int32_t depth;                    /* heads staged per prep warp */
+  int32_t state_stages;             /* NS, a multiple of consumer_groups */
+  int32_t vector_slots;             /* FFMA kernel: NSL; tensor-core kernel: NP x depth */
+  int32_t consumer_groups;          /* G */
+  int32_t consumer_warps_per_group; /* GU */
+  int32_t rows_per_unit;            /* state rows streamed per stage fill */
+  int32_t units_per_head;           /* d_v / rows_per_unit */
+  int32_t threads;                  /* per block */
+  int64_t smem_bytes;               /* dynamic shared memory per block */
+} replayssm_delta_config;
+
+REPLAYSSM_API replayssm_status replayssm_delta_kernel_config(const replayssm_dims* dims,
+                                                             int32_t K, int32_t read_copy,
+                                                             int64_t smem_limit,
+                                                             replayssm_delta_config* out);
 
 /* Static, NUL-terminated description of a return code. */
 REPLAYSSM_API const char* replayssm_status_string(replayssm_status status);

@@ -36,6 +36,15 @@ class State(ctypes.Structure):
                 ("status", _P), ("sync", _P), ("work", _P)]
 
 
+class DeltaConfig(ctypes.Structure):
+    _fields_ = [("tensor_cores", ctypes.c_int32), ("prep_warps", ctypes.c_int32),
+                ("depth", ctypes.c_int32), ("state_stages", ctypes.c_int32),
+                ("vector_slots", ctypes.c_int32), ("consumer_groups", ctypes.c_int32),
+                ("consumer_warps_per_group", ctypes.c_int32), ("rows_per_unit", ctypes.c_int32),
+                ("units_per_head", ctypes.c_int32), ("threads", ctypes.c_int32),
+                ("smem_bytes", ctypes.c_int64)]
+
+
 _DP = ctypes.POINTER(Dims)
 _SP = ctypes.POINTER(State)
 _I = ctypes.c_int32
@@ -61,6 +70,7 @@ SIGNATURES = {
     "replayssm_copy_sequences": [_DP, _SP, _P, _SP, _P, _I, _P],
     "replayssm_selftest_wait_timeout": [_P, _P],
     "replayssm_workspace_bytes": [_DP, _I],
+    "replayssm_delta_kernel_config": [_DP, _I, _I, ctypes.c_int64, ctypes.POINTER(DeltaConfig)],
     "replayssm_status_string": [_I],
     "replayssm_version": [],
 }

@@ -270,5 +270,15 @@ def workspace_bytes(dims: LayerDims, K: int = 1) -> int:
     return int(_abi.lib.replayssm_workspace_bytes(ctypes.byref(dims.c()), int(K)))
 
 
+def delta_kernel_config(dims: LayerDims, K: int = 1, read_copy: bool = True,
+                        smem_limit: int = 0) -> dict:
+    """Launch configuration of the GDN/KDA decode (K = 1) or verify kernel for
+    these sizes (host only; smem_limit 0 means the B300's), as a dict."""
+    out = _abi.DeltaConfig()
+    _call("replayssm_delta_kernel_config", ctypes.byref(dims.c()), int(K), int(bool(read_copy)),
+          int(smem_limit), ctypes.byref(out))
+    return {name: int(getattr(out, name)) for name, _ in _abi.DeltaConfig._fields_}
+
+
 def version() -> int:
     return int(_abi.lib.replayssm_version())

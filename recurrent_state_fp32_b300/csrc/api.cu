@@ -546,6 +546,19 @@ REPLAYSSM_API int64_t replayssm_workspace_bytes(const replayssm_dims* dims, int3
   return std::max<long long>(b, rs::StepLayout(*dims).bytes());
 }
 
+REPLAYSSM_API replayssm_status replayssm_delta_kernel_config(const replayssm_dims* dims,
+                                                             int32_t K, int32_t read_copy,
+                                                             int64_t smem_limit,
+                                                             replayssm_delta_config* out) {
+  RS_TRY(check_dims(dims));
+  if (!out || dims->kind == REPLAYSSM_MAMBA2 || K < 1 || K > 8 || K > dims->window ||
+      smem_limit < 0)
+    return REPLAYSSM_ERR_INVALID_ARG;
+  const size_t optin = smem_limit ? (size_t)smem_limit : (size_t)232448;
+  return rs::delta_kernel_config(*dims, K, read_copy != 0, optin, *out) ? REPLAYSSM_OK
+                                                                        : REPLAYSSM_ERR_UNSUPPORTED;
+}
+
 REPLAYSSM_API int64_t replayssm_mamba2_decode_noalloc_bytes(const replayssm_dims* dims) {
   if (check_dims(dims) != REPLAYSSM_OK || dims->kind != REPLAYSSM_MAMBA2) return 0;
   return NoallocLayout(*dims).total;

@@ -1566,8 +1566,10 @@ bool gram_eligible(const replayssm_dims& d, const replayssm_state& s, int K) {
 // NP x depth x (units per head) a multiple of the consumer groups (each
 // group then sees every fill of the prep stages it reads, so no parity wait
 // can take an older phase) and at least 4 state stages, the most heads in
-// flight (NP x depth), ties to more stages. (b512 K = 4 verify: 7 x 2 with
-// 4 stages 205 us, 6 x 2 213 us, 6 x 1 with 8 stages 215 us.)
+// flight (NP x depth), ties to more stages. (b512 K = 4 verify, measured
+// before the prep stages held the value terms: 7 x 2 with 4 stages 205 us,
+// 6 x 2 213 us, 6 x 1 with 8 stages 215 us. With them 7 x 2 needs 244 KB at
+// d_k = d_v = 128 and 6 x 2 is the one that fits.)
 struct GramConfig {
   int NS, NP, depth;
   size_t smem;
@@ -1827,6 +1829,55 @@ size_t delta_fused_smem(const replayssm_dims& d, int K, bool read16) {
   const int RB = fused_rows(d.dk, ts, d.dv);
   return DFusedSmem(RB, d.dk, d.dv, d.window, K, kFGroups, vector_slots(1, d.dv / RB), 1, 1,
                     d.kind == REPLAYSSM_KDA, ts, ti).total + 1024;
+}
+
+bool delta_kernel_config(const replayssm_dims& d, int K, bool read16, size_t optin,
+                         replayssm_delta_config& out) {
+  // The choice launch_delta makes, by sizes alone: the tensor-core kernel
+  // where gram_eligible admits the sizes and gram_config fits, else the
+  // fused kernel as launch_fused configures it.
+  out = replayssm_delta_config{};
+  const bool kda = d.kind == REPLAYSSM_KDA, in16 = d.in_dtype == REPLAYSSM_BF16;
+  const char* env = std::getenv("REPLAYSSM_DELTA_TENSOR_CORES");
+  const bool tc = !(env && env[0] == '0');
+  if (tc && K >= 2 && d.kind == REPLAYSSM_GDN && read16 && in16 && (d.dk == 64 || d.dk == 128) &&
+      d.dv % kGRows == 0 && d.window <= kGramN && K <= kGramQ) {
+    const GramConfig c = gram_config(d.dk, d.dv, d.window, K, optin);
+    if (c.NP > 0) {
+      out.tensor_cores = 1;
+      out.prep_warps = c.NP;
+      out.depth = c.depth;
+      out.state_stages = c.NS;
+      out.vector_slots = c.NP * c.depth;
+      out.consumer_groups = kGGroups;
+      out.consumer_warps_per_group = 2;
+      out.rows_per_unit = kGRows;
+      out.units_per_head = d.dv / kGRows;
+      out.threads = 32 * (2 * kGGroups + 1 + c.NP);
+      out.smem_bytes = (int64_t)c.smem;
+      return true;
+    }
+  }
+  const int ts = read16 ? 2 : 4, ti = in16 ? 2 : 4;
+  const int RB = fused_rows(d.dk, ts, d.dv);
+  int GU = RB % 64 == 0 ? 2 : 1;
+  const int KMAX = K == 1 ? 1 : K <= 4 ? 4 : 8;
+  if (RB / GU > 128 || K > KMAX) return false;
+  FusedConfig c{0, 0, 0, 0, 0};
+  if (K == 1 && ts == 2) c = decode_config(RB, d.dk, d.dv, d.window, kda, ti, optin, GU);
+  if (c.NP == 0) c = fused_config(RB, d.dk, d.dv, d.window, K, GU, kda, ts, ti, optin);
+  if (c.NP == 0) return false;
+  out.prep_warps = c.NP;
+  out.depth = c.depth;
+  out.state_stages = c.NS;
+  out.vector_slots = c.NSL;
+  out.consumer_groups = kFGroups;
+  out.consumer_warps_per_group = GU;
+  out.rows_per_unit = RB;
+  out.units_per_head = d.dv / RB;
+  out.threads = 32 * (kFGroups * GU + 1 + c.NP);
+  out.smem_bytes = (int64_t)c.smem;
+  return true;
 }
 
 cudaError_t launch_delta_decode(const replayssm_dims& d, const replayssm_state& s, const void* q,

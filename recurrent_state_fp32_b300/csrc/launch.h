@@ -85,6 +85,10 @@ cudaError_t launch_delta_verify(const replayssm_dims& d, const replayssm_state& 
                                 const float* beta, float scale, float* o, cudaStream_t st);
 // Shared memory the fused delta decode / verify block needs at least.
 size_t delta_fused_smem(const replayssm_dims& d, int K, bool read16);
+// The delta kernel's launch configuration for these sizes (no CUDA call);
+// false if none fits in optin bytes of shared memory per block.
+bool delta_kernel_config(const replayssm_dims& d, int K, bool read16, size_t optin,
+                         replayssm_delta_config& out);
 cudaError_t launch_delta_fold(const replayssm_dims& d, const replayssm_state& s, int k_next,
                               int force, cudaStream_t st);
 // consolidate(k_next = 1) then decode: the decode grid, then the fold grid
