@@ -1795,6 +1795,8 @@ cudaError_t launch_delta(const replayssm_dims& d, const replayssm_state& s, int 
            s.ring_head, s.ring_len, s.status, s.sync, flags};
   const bool rd16 = s.S_read != nullptr, in16 = d.in_dtype == REPLAYSSM_BF16;
   const bool kda = d.kind == REPLAYSSM_KDA;
+  // (delta_kernel_config repeats this choice, and launch_fused's, by sizes
+  // alone for the host-side query: a change here goes there too)
   if (gram_eligible(d, s, K)) {
     bool launched = false;
     const bf16* S = reinterpret_cast<const bf16*>(s.S_read);
