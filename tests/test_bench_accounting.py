@@ -78,7 +78,7 @@ def test_delta_bytes_per_token():
         out = H * d * 4
         want = state * 2 + 2 * token + 7.5 * entry + out + (state * 10 + 16 * entry) / 16
         assert per_token(layer(kind, "bf16")) == want
-        # the per-token figures of the scope table's roofline floors
+        # bytes per sequence and token of the b256 layers, BF16 read copy
         assert want == {"gdn": 1_583_744, "kda": 1_754_432}[kind]
 
 
